@@ -1,0 +1,53 @@
+"""Host checks of the seeded workload generator (CPU)."""
+import torch
+
+import workloads as W
+
+
+def test_tiny_workload_shapes_and_indices():
+    w = W.WORKLOADS[0]
+    p = W.make_problem(w)
+    assert p.q.shape == (2, 16, 576) and p.q.dtype == torch.bfloat16
+    assert p.kv_bf16.shape == (4, 64, 576)
+    assert p.page_table.shape == (2, 4)
+    for r in range(2):
+        assert sorted(p.page_table[r].tolist()) == [0, 1, 2, 3]
+    for t in range(2):
+        row = p.topk[t]
+        assert (row >= 0).all() and len(set(row.tolist())) == 128 and row.max() < 256
+
+
+def test_padded_tail_and_distinct():
+    w = W.small_variant(W.WORKLOADS[4], num_requests=3, ctx_lo=300, ctx_hi=900, topk=256, tail_pad=51)
+    p = W.make_problem(w)
+    for t in range(p.topk.shape[0]):
+        row = p.topk[t].tolist()
+        valid = [x for x in row if x != -1]
+        assert row[len(valid):] == [-1] * (256 - len(valid))
+        assert len(valid) == 205 and len(set(valid)) == 205
+        assert max(valid) < int(p.ctx[t])
+
+
+def test_mtp_causal_prefix_and_page_pool():
+    w = W.small_variant(W.WORKLOADS[3], num_requests=2, ctx_lo=100, ctx_hi=130, topk=160)
+    p = W.make_problem(w)
+    assert p.topk.shape == (8, 160)
+    for t in range(8):
+        r, i = divmod(t, 4)
+        visible = int(p.ctx[r]) - 3 + i
+        valid = [x for x in p.topk[t].tolist() if x != -1]
+        assert len(valid) == min(visible, 160) and max(valid) < visible
+    used = [x for x in p.page_table.flatten().tolist() if x != -1]
+    assert sorted(used) == list(range(p.num_pages))
+
+
+def test_raw_chunk_is_reproducible():
+    w = W.small_variant(W.WORKLOADS[1], num_requests=2, ctx_lo=200, ctx_hi=300, topk=64)
+    a = W.make_problem(w)
+    b = W.make_problem(w)
+    la, ra = a.raw_chunk(0)
+    lb, rb = b.raw_chunk(0)
+    assert torch.equal(la, lb) and torch.equal(ra, rb)
+    pages = [0, 2]
+    lat, rope = a.raw_pages(pages)
+    assert torch.equal(lat[64:128], la[128:192]) and torch.equal(rope[:64], ra[:64])
