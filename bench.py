@@ -1,0 +1,333 @@
+#!/usr/bin/env python3
+"""Sparse MLA decode benchmark on GB300: query-tokens/s and fraction of the roofline.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one smla_decode call over one batch of the workload (all query
+tokens: gather, dequant, QK, softmax, PV, split merge), inputs resident in HBM.
+L2 is flushed (a 512 MiB write) between timed steps, outside the timed
+events. Under torchrun (N > 1) every rank decodes its own batch of the same
+shape (independent replicas, weak scaling); the JSON line reports the total
+tokens of all ranks over the slowest rank's time.
+
+--impl reference times the float64 CPU oracle (the reference arm) on a bounded
+sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+# The CPU oracle runs with one BLAS thread, so its reported core count is exact.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = W.WORKLOADS[1].name
+METRIC = "sparse-MLA decode query-tokens/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def algorithmic_work(problem) -> tuple[int, int, int]:
+    """(valid indices, KV-row bytes, FLOPs) of one decode of the whole batch."""
+    valid = int((problem.topk >= 0).sum().item())
+    w = problem.w
+    return valid, valid * w.row_bytes, valid * w.num_heads * 2 * (576 + 512)
+
+
+def roofline(valid_bytes, flops, seconds, peaks) -> dict:
+    t_hbm = valid_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        achieved = valid_bytes / seconds / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": peaks["source"] + " hbm_gbs (burst)"}
+    achieved = flops / seconds / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+            "peak_source": peaks["source"] + " bf16_tflops (burst)"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+
+    def summary(self) -> dict:
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------ oracle arm
+
+
+def run_oracle_sample(problem, budget_s: float, min_tokens: int = 1):
+    """Time the float64 oracle, as it stands, on whole query tokens until ~budget_s."""
+    from oracle.workload_oracle import oracle_decode
+    T = problem.w.num_tokens
+    order = list(range(0, T, max(1, T // 64))) + list(range(T))
+    done, t0 = 0, time.perf_counter()
+    for t in order:
+        oracle_decode(problem, tokens=[t])
+        done += 1
+        if done >= min_tokens and time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return done, el
+
+
+def reference_arm(args):
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return 0
+    w = W.BY_NAME[args.workload]
+    problem = W.make_problem(w, device="cpu")
+    per_step = []
+    tokens = 0
+    for i in range(args.warmup + args.steps):
+        n, el = run_oracle_sample(problem, budget_s=args.ref_step_seconds)
+        if i >= args.warmup:
+            per_step.append(el / n)
+            tokens += n
+    sec_per_token = sum(per_step) / len(per_step)
+    value = 1.0 / sec_per_token
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "query-tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sec_per_token * w.num_tokens, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "tokens": w.num_tokens, "heads": w.num_heads,
+                       "topk": w.topk, "kv_format": w.kv_format},
+            "cpu_baseline": {"value": value, "unit": "query-tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{tokens} query tokens of {w.name} over {args.steps} steps "
+                                       f"(~{args.ref_step_seconds:.0f} s each), numpy float64, 1 BLAS thread"},
+            "e2e": {"value": value, "unit": "query-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------ GPU arm
+
+
+def gpu_arm(args):
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import sparse_mla_decode_smla_gb300 as smla
+    from sparse_mla_decode_smla_gb300.runner import DeviceDecode
+
+    w = W.BY_NAME[args.workload]
+    problem = W.make_problem(w, seed=W.SEED_BASE + w.seed_offset + 1000 * rank, device=dev)
+    dd = DeviceDecode(problem, num_splits=args.num_splits, device=dev)
+    valid, kv_bytes, flops = algorithmic_work(problem)
+    launches_per_step = 2 if dd.workspace.numel() * 4 > 256 else 1
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        dd.run()
+    torch.cuda.synchronize(dev)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            dd.run()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        wall = time.perf_counter() - wall0
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    ms_max = reduce_max(ms, world, dev)
+    value = world * w.num_tokens / (ms_max * 1e-3)
+
+    # end to end through the public API: pinned host inputs -> decode -> host outputs
+    h_q = problem.q.cpu().pin_memory()
+    h_topk = problem.topk.cpu().to(torch.int32).pin_memory()
+    h_pt = problem.page_table.cpu().to(torch.int32).pin_memory()
+    h_out = torch.empty(dd.out.shape, dtype=dd.out.dtype).pin_memory()
+    h_lse = torch.empty(dd.lse.shape, dtype=dd.lse.dtype).pin_memory()
+    h2d = h_q.numel() * 2 + h_topk.numel() * 4 + h_pt.numel() * 4
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step():
+        dd.q.copy_(h_q, non_blocking=True)
+        dd.topk.copy_(h_topk, non_blocking=True)
+        dd.page_table.copy_(h_pt, non_blocking=True)
+        dd.run()
+        h_out.copy_(dd.out, non_blocking=True)
+        h_lse.copy_(dd.lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_ms = []
+    for _ in range(e2e_steps):
+        flush.fill_(0.5)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    e2e_ms = reduce_max(sum(e_ms) / len(e_ms), world, dev)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    peaks = measured_peaks()
+    rl = roofline(kv_bytes, flops, ms * 1e-3, peaks)
+    rl["traffic"] = args.traffic
+    line = {
+        "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.num_tokens, "heads": w.num_heads,
+                   "topk": w.topk, "valid_indices": valid, "kv_format": w.kv_format,
+                   "kv_row_bytes": w.row_bytes, "page_size": w.page_size,
+                   "num_pages": problem.num_pages, "sink": w.sink,
+                   "l2": "flushed between timed steps (512 MiB write, outside the events)",
+                   "num_splits": args.num_splits or "auto", "parallelism": f"replicas x{world}"},
+        "roofline": rl,
+        "roofline_sustained_frac": (rl["achieved"] / 1722.2 if rl["bound"] == "tensor" and
+                                    peaks["source"] == "measured" else None),
+        "algorithmic": {"kv_bytes": kv_bytes, "flops": flops},
+        "e2e": {"value": world * w.num_tokens / (e2e_ms * 1e-3), "unit": "query-tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "wall_s": wall,
+    }
+    if args.cpu_baseline_seconds > 0 and world == 1:
+        cpu_problem = problem
+        n, el = run_oracle_sample(cpu_problem, budget_s=args.cpu_baseline_seconds)
+        line["cpu_baseline"] = {"value": n / el, "unit": "query-tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{n} of {w.num_tokens} query tokens of {w.name}, "
+                                          f"numpy float64, 1 BLAS thread, {el:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[w.name for w in W.WORKLOADS])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=5.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the decode kernel from an ncu capture, if current")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

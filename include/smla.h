@@ -1,0 +1,164 @@
+/*
+ * smla.h - C ABI of the GB300 sparse MLA decode library (libsmla.so).
+ *
+ * Sparse MLA decode, as the DeepSeek-V4 integration pages describe it
+ * (vLLM PR #43477 "关键源码片段", forward_mqa; SGLang PR #24692 "实现拆解 2-3";
+ * vLLM PR #43827 "关键源码片段"): for every query token, take the top-k
+ * request-local slot indices chosen by the indexer, translate them through the
+ * request's page table into physical cache slots, gather those rows of the
+ * paged latent cache, dequantise them, score all heads over the 576 dims
+ * (512 latent + 64 RoPE) against the one shared latent, apply a softmax with
+ * an optional per-head sink logit and accumulate the 512-dim latent values.
+ *
+ * All tensor arguments are device pointers owned by the caller. The library
+ * allocates no memory, never synchronises inside smla_decode / smla_pack_kv /
+ * smla_gather_dequant, and returns a status instead of throwing. Argument
+ * errors are found on the host before anything is launched; in that case
+ * nothing is launched and no output is written. Streams are cudaStream_t
+ * values passed as void* (NULL = the legacy default stream).
+ */
+#ifndef SMLA_H
+#define SMLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum smla_status {
+  SMLA_OK = 0,
+  SMLA_ERR_NULL = 1,         /* a required pointer is NULL */
+  SMLA_ERR_SHAPE = 2,        /* a size or count is outside the supported range */
+  SMLA_ERR_ALIGN = 3,        /* a pointer breaks its alignment rule */
+  SMLA_ERR_UNSUPPORTED = 4,  /* a valid combination this build does not serve */
+  SMLA_ERR_WORKSPACE = 5,    /* workspace smaller than smla_workspace_size() */
+  SMLA_ERR_CUDA = 6,         /* a CUDA runtime call or launch failed */
+  SMLA_ERR_INDEX_RANGE = 7,  /* device met an invalid index or page entry (smla_read_error) */
+  SMLA_ERR_DEVICE = 8        /* no usable device, or not an sm_103 GPU */
+} smla_status;
+
+/* Cache row formats. */
+enum {
+  /* 576 bf16 per slot, [latent 512 | RoPE 64] = 1152 bytes (the contiguous BF16
+   * cache, vLLM PR #43477 "关键源码片段": (num_blocks, block_size, head_size)). */
+  SMLA_KV_BF16 = 0,
+  /* fp8_ds_mla: 656 bytes per slot = 512 E4M3FN latent codes | 4 fp32 scales
+   * (little-endian; scale b covers latent dims [128b, 128b+128)) | 64 bf16 RoPE. */
+  SMLA_KV_FP8_DS = 1
+};
+
+/* Block-scale rule of smla_pack_kv (amax = max |x| over the 128-dim block). */
+enum {
+  SMLA_SCALE_POW2 = 0, /* smallest power of two >= fl32(amax/448) ("UE8M0" layout) */
+  SMLA_SCALE_FP32 = 1  /* fl32(amax/448) */
+};
+
+/* Bits of the device error word (smla_read_error). */
+enum {
+  SMLA_DEVERR_INDEX = 1, /* a top-k entry other than -1 outside [0, page_table_stride*page_size) */
+  SMLA_DEVERR_PAGE = 2   /* a page-table entry used by a valid index outside [0, num_pages) */
+};
+
+typedef struct smla_desc {
+  int32_t num_tokens;        /* T >= 1: query tokens (requests x next_n) */
+  int32_t num_heads;         /* H: multiple of 16, 16..128 */
+  int32_t topk;              /* K >= 1, multiple of 4: entries per index row */
+  int32_t num_requests;      /* B >= 1: rows of page_table */
+  int32_t next_n;            /* >= 1: token t belongs to request t / next_n unless
+                                req_id_per_token is given */
+  int32_t page_size;         /* P: power of two, 1..4096 */
+  int64_t num_pages;         /* physical pages in kv_cache (>= 1) */
+  int32_t page_table_stride; /* entries per page_table row (>= 1) */
+  int32_t kv_format;         /* SMLA_KV_* */
+  float sm_scale;            /* softmax scale multiplying q.k (e.g. 1/sqrt(576)) */
+  int32_t num_splits;        /* 0: the library chooses; n > 0: split the top-k list
+                                into n contiguous parts merged by log-sum-exp */
+  int32_t reserved[4];       /* must be zero */
+} smla_desc;
+
+/* Human-readable name of a status (static string). */
+const char* smla_status_string(int32_t status);
+
+/* ABI version of this header (increments on any incompatible change). */
+int32_t smla_abi_version(void);
+
+/*
+ * Bytes of device workspace smla_decode needs for `d` on the current device
+ * (split partials, merge bookkeeping, the device error word). The caller
+ * allocates it (256-byte aligned) and zeroes it once before first use; the
+ * library leaves the bookkeeping zeroed again after every call. Writes 0 into
+ * *bytes on error.
+ */
+smla_status smla_workspace_size(const smla_desc* d, size_t* bytes);
+
+/*
+ * Sparse MLA decode (the hot path).
+ *   q          [T, H, 576] bf16, 16-byte aligned; dims 0..511 pair with the latent,
+ *              512..575 with the RoPE part.
+ *   kv_cache   [num_pages, P, R] bytes, R = 656 (FP8_DS) or 1152 (BF16), 16-byte aligned.
+ *   page_table [B, page_table_stride] int32: request-local page -> physical page.
+ *   topk       [T, K] int32, 16-byte aligned: request-local slot indices, -1 = padding.
+ *              Index i of request r lives in physical slot
+ *              page_table[r, i / P] * P + i % P.
+ *   req_id_per_token [T] int32 or NULL (then request = t / next_n).
+ *   sink       [H] fp32 or NULL: per-head sink logit sigma_h, adds e^sigma_h to the
+ *              softmax denominator only.
+ *   out        [T, H, 512] bf16, 16-byte aligned:
+ *              out = sum_j e^{s_j} v_j / (sum_j e^{s_j} + [sink] e^{sigma_h}),
+ *              s_j = sm_scale * <q, k_j>, v_j = k_j[0:512]. 0 when nothing is selected.
+ *   lse        [T, H] fp32 or NULL: natural log of that denominator (-inf when it is
+ *              empty and there is no sink).
+ *   workspace  device memory of at least smla_workspace_size(d) bytes, 256-byte aligned.
+ * Entries other than -1 that fall outside the request's page table, or whose page
+ * entry lies outside [0, num_pages), are skipped like padding (never loaded) and set
+ * a bit of the device error word, readable with smla_read_error. Duplicated indices
+ * count once per occurrence. Rows skipped as padding are never read, so their bytes
+ * may hold anything.
+ */
+smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
+                        const int32_t* page_table, const int32_t* topk,
+                        const int32_t* req_id_per_token, const float* sink, void* out,
+                        float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Write cache rows (the quantise-on-write store of the compressor, vLLM PR #43827
+ * "实现拆解 4"): for each i < n with slot_mapping[i] >= 0, row slot_mapping[i] of
+ * kv_cache receives latent[i] (512 bf16) and rope[i] (64 bf16).
+ *   FP8_DS: per 128-dim block, scale by the SMLA_SCALE_* rule (an all-zero block gets
+ *           scale 1); code = E4M3 round-to-nearest-even, saturating at +-448, of
+ *           fl32(x / scale); RoPE is stored as given.
+ *   BF16:   the 576 values are stored as given (scale_mode ignored).
+ *   latent [n, 512] bf16 and rope [n, 64] bf16, 16-byte aligned; slot_mapping [n] int64;
+ *   kv_cache holds num_slots rows. Entries of slot_mapping >= num_slots are skipped.
+ */
+smla_status smla_pack_kv(int32_t kv_format, int32_t scale_mode, const void* latent,
+                         const void* rope, const int64_t* slot_mapping, int64_t n,
+                         void* kv_cache, int64_t num_slots, void* stream);
+
+/*
+ * Test hook exposing the gather + dequantise steps of smla_decode
+ * (the _gather_and_dequant reference path of SGLang PR #24692, "实现拆解 3"):
+ * rows [T, K, 576] fp32 receives, for each (t, j), the dequantised key vector of the
+ * slot topk[t, j] selects: latent element d = fl32(e4m3(code_d) * scale[d/128]) for
+ * FP8_DS, the bf16 value otherwise; RoPE as bf16 values. Padding and invalid entries
+ * give a zero row. error_word (device int32, may be NULL) receives SMLA_DEVERR_* bits.
+ */
+smla_status smla_gather_dequant(const smla_desc* d, const void* kv_cache,
+                                const int32_t* page_table, const int32_t* topk,
+                                const int32_t* req_id_per_token, float* rows,
+                                int32_t* error_word, void* stream);
+
+/*
+ * Synchronises `stream`, copies the device error word of `workspace` into
+ * *error_word and clears it. Returns SMLA_ERR_INDEX_RANGE when any bit was set.
+ */
+smla_status smla_read_error(const smla_desc* d, void* workspace, size_t workspace_bytes,
+                            int32_t* error_word, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMLA_H */

@@ -1,0 +1,139 @@
+"""Python binding of libsmla.so (GB300 sparse MLA decode).
+
+Argument marshalling only: every step of the decode runs in the library's CUDA
+kernels. The functions mirror the C ABI in include/smla.h and take torch
+tensors for device memory and the current torch stream. There is no fallback:
+importing fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB as LIB_PATH
+
+SMLA_KV_BF16 = 0
+SMLA_KV_FP8_DS = 1
+SMLA_SCALE_POW2 = 0
+SMLA_SCALE_FP32 = 1
+SMLA_DEVERR_INDEX = 1
+SMLA_DEVERR_PAGE = 2
+
+STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_NULL", 2: "SMLA_ERR_SHAPE", 3: "SMLA_ERR_ALIGN",
+          4: "SMLA_ERR_UNSUPPORTED", 5: "SMLA_ERR_WORKSPACE", 6: "SMLA_ERR_CUDA",
+          7: "SMLA_ERR_INDEX_RANGE", 8: "SMLA_ERR_DEVICE"}
+EXPORTS = ["smla_status_string", "smla_abi_version", "smla_workspace_size", "smla_decode",
+           "smla_pack_kv", "smla_gather_dequant", "smla_read_error"]
+
+
+class SmlaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+class smla_desc(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("topk", ctypes.c_int32), ("num_requests", ctypes.c_int32),
+                ("next_n", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_pages", ctypes.c_int64), ("page_table_stride", ctypes.c_int32),
+                ("kv_format", ctypes.c_int32), ("sm_scale", ctypes.c_float),
+                ("num_splits", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libsmla.so (raises when it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with sparse_mla_decode_smla_gb300._build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        D = ctypes.POINTER(smla_desc)
+        L.smla_status_string.restype = ctypes.c_char_p
+        L.smla_status_string.argtypes = [I32]
+        L.smla_abi_version.restype = I32
+        L.smla_abi_version.argtypes = []
+        L.smla_workspace_size.restype = I32
+        L.smla_workspace_size.argtypes = [D, ctypes.POINTER(SZ)]
+        L.smla_decode.restype = I32
+        L.smla_decode.argtypes = [D, P, P, P, P, P, P, P, P, P, SZ, P]
+        L.smla_pack_kv.restype = I32
+        L.smla_pack_kv.argtypes = [I32, I32, P, P, P, I64, P, I64, P]
+        L.smla_gather_dequant.restype = I32
+        L.smla_gather_dequant.argtypes = [D, P, P, P, P, P, P, P]
+        L.smla_read_error.restype = I32
+        L.smla_read_error.argtypes = [D, P, SZ, ctypes.POINTER(I32), P]
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().smla_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise SmlaError(fn, status)
+
+
+def make_desc(num_tokens, num_heads, topk, num_requests, page_size, num_pages, page_table_stride,
+              kv_format, sm_scale, next_n=1, num_splits=0) -> smla_desc:
+    d = smla_desc()
+    d.num_tokens, d.num_heads, d.topk = num_tokens, num_heads, topk
+    d.num_requests, d.next_n, d.page_size = num_requests, next_n, page_size
+    d.num_pages, d.page_table_stride = num_pages, page_table_stride
+    d.kv_format, d.sm_scale, d.num_splits = kv_format, sm_scale, num_splits
+    return d
+
+
+def workspace_size(desc: smla_desc) -> int:
+    n = ctypes.c_size_t(0)
+    _check("smla_workspace_size", lib().smla_workspace_size(ctypes.byref(desc), ctypes.byref(n)))
+    return n.value
+
+
+def decode(desc, q, kv_cache, page_table, topk, req_id_per_token, sink, out, lse, workspace,
+           stream=None):
+    _check("smla_decode", lib().smla_decode(
+        ctypes.byref(desc), _ptr(q), _ptr(kv_cache), _ptr(page_table), _ptr(topk),
+        _ptr(req_id_per_token), _ptr(sink), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def pack_kv(kv_format, scale_mode, latent, rope, slot_mapping, kv_cache, num_slots, stream=None):
+    _check("smla_pack_kv", lib().smla_pack_kv(
+        kv_format, scale_mode, _ptr(latent), _ptr(rope), _ptr(slot_mapping), latent.shape[0],
+        _ptr(kv_cache), num_slots, _stream(stream)))
+
+
+def gather_dequant(desc, kv_cache, page_table, topk, req_id_per_token, rows, error_word=None,
+                   stream=None):
+    _check("smla_gather_dequant", lib().smla_gather_dequant(
+        ctypes.byref(desc), _ptr(kv_cache), _ptr(page_table), _ptr(topk), _ptr(req_id_per_token),
+        _ptr(rows), _ptr(error_word), _stream(stream)))
+
+
+def read_error(desc, workspace, stream=None) -> int:
+    """Synchronises, returns and clears the device error word (SMLA_DEVERR_* bits)."""
+    v = ctypes.c_int32(0)
+    st = lib().smla_read_error(ctypes.byref(desc), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), ctypes.byref(v),
+                               _stream(stream))
+    if st not in (0, 7):
+        raise SmlaError("smla_read_error", st)
+    return v.value

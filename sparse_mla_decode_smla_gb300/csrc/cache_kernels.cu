@@ -1,0 +1,159 @@
+// Cache-row kernels: the quantise-on-write store (smla_pack_kv) and the gather +
+// dequantise test hook (smla_gather_dequant).
+//
+// fp8_ds_mla row (656 B): 512 E4M3FN codes | 4 fp32 scales | 64 bf16 RoPE; scale b
+// covers latent dims [128b, 128b+128) (vLLM PR #43477 "实现拆解 1": the fp8_ds_mla
+// cache; vLLM PR #43827 "功能与动机": the "UE8M0 paged" FlashMLA layout, i.e. power-of-
+// two block scales).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace smla {
+
+// One warp per row. Lane l owns latent elements [16l, 16l+16); lanes 8b..8b+7 form block b.
+template <int FMT>
+__global__ void __launch_bounds__(256) pack_kernel(const uint4* __restrict__ latent,
+                                                   const uint4* __restrict__ rope,
+                                                   const int64_t* __restrict__ slot_mapping,
+                                                   int64_t n, uint8_t* __restrict__ kv,
+                                                   int64_t num_slots, int scale_mode) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (row >= n) return;
+  const int64_t slot = slot_mapping[row];
+  if (slot < 0 || slot >= num_slots) return;
+  const uint4 x0 = latent[row * 64 + 2 * lane];
+  const uint4 x1 = latent[row * 64 + 2 * lane + 1];
+  if (FMT == SMLA_KV_BF16) {
+    uint4* dst = reinterpret_cast<uint4*>(kv + slot * kBf16RowBytes);
+    dst[2 * lane] = x0;
+    dst[2 * lane + 1] = x1;
+    if (lane < 8) dst[64 + lane] = rope[row * 8 + lane];
+    return;
+  }
+  const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = bf16_lo(w[i]);
+    v[2 * i + 1] = bf16_hi(w[i]);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+  float scale = 1.f;
+  if (amax > 0.f) {
+    const float ratio = __fdiv_rn(amax, 448.f);
+    if (scale_mode == SMLA_SCALE_POW2) {
+      int e;
+      const float m = frexpf(ratio, &e);  // ratio = m * 2^e, m in [0.5, 1)
+      scale = (m == 0.5f) ? ratio : ldexpf(1.f, e);
+    } else {
+      scale = ratio;
+    }
+  }
+  uint32_t codes[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(v[4 * i], scale), __fdiv_rn(v[4 * i + 1], scale));
+    const uint16_t hi =
+        f32x2_to_e4m3x2(__fdiv_rn(v[4 * i + 2], scale), __fdiv_rn(v[4 * i + 3], scale));
+    codes[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  uint8_t* dst = kv + slot * kFp8RowBytes;
+  *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+  const float s1 = __shfl_sync(0xffffffffu, scale, 8);
+  const float s2 = __shfl_sync(0xffffffffu, scale, 16);
+  const float s3 = __shfl_sync(0xffffffffu, scale, 24);
+  if (lane == 0) *reinterpret_cast<float4*>(dst + kScaleOff) = make_float4(scale, s1, s2, s3);
+  if (lane < 8) *reinterpret_cast<uint4*>(dst + kRopeOffFp8 + 16 * lane) = rope[row * 8 + lane];
+}
+
+cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, const void* latent,
+                        const void* rope, const int64_t* slot_mapping, int64_t n, void* kv,
+                        int64_t num_slots, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int64_t blocks = (n * 32 + 255) / 256;
+  auto* L = static_cast<const uint4*>(latent);
+  auto* R = static_cast<const uint4*>(rope);
+  auto* K = static_cast<uint8_t*>(kv);
+  if (kv_format == SMLA_KV_FP8_DS)
+    pack_kernel<SMLA_KV_FP8_DS><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        L, R, slot_mapping, n, K, num_slots, scale_mode);
+  else
+    pack_kernel<SMLA_KV_BF16><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        L, R, slot_mapping, n, K, num_slots, scale_mode);
+  return cudaGetLastError();
+}
+
+// One warp per (token, top-k position). Lane l writes latent dims [16l, 16l+16) and
+// RoPE dims [2l, 2l+2).
+__global__ void __launch_bounds__(256) gather_dequant_kernel(DecodeArgs a, float* __restrict__ rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (item >= static_cast<int64_t>(a.T) * a.K) return;
+  const int t = static_cast<int>(item / a.K);
+  const int r = a.req_id ? a.req_id[t] : t / a.next_n;
+  float* dst = rows + item * kDim;
+  int64_t slot = -1;
+  if (r >= 0 && r < a.B) {
+    slot = translate_index(a.topk[item], a.page_table + static_cast<int64_t>(r) * a.stride,
+                           a.stride, a.log2_page, a.num_pages, lane == 0 ? a.err : nullptr);
+  } else if (lane == 0 && a.err) {
+    atomicOr(a.err, SMLA_DEVERR_INDEX);
+  }
+  float v[16];
+  float rp0 = 0.f, rp1 = 0.f;
+  if (slot < 0) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+  } else if (a.kv_format == SMLA_KV_FP8_DS) {
+    const uint8_t* src = a.kv + slot * kFp8RowBytes;
+    const uint4 c = *reinterpret_cast<const uint4*>(src + 16 * lane);
+    const float scale = reinterpret_cast<const float*>(src + kScaleOff)[lane >> 3];
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t lo, hi;
+      e4m3x4_to_f16x4(w[i], lo, hi);
+      const float2 f0 = __half22float2(*reinterpret_cast<__half2*>(&lo));
+      const float2 f1 = __half22float2(*reinterpret_cast<__half2*>(&hi));
+      v[4 * i] = __fmul_rn(f0.x, scale);
+      v[4 * i + 1] = __fmul_rn(f0.y, scale);
+      v[4 * i + 2] = __fmul_rn(f1.x, scale);
+      v[4 * i + 3] = __fmul_rn(f1.y, scale);
+    }
+    const uint32_t rw = reinterpret_cast<const uint32_t*>(src + kRopeOffFp8)[lane];
+    rp0 = bf16_lo(rw);
+    rp1 = bf16_hi(rw);
+  } else {
+    const uint8_t* src = a.kv + slot * kBf16RowBytes;
+    const uint4 c0 = *reinterpret_cast<const uint4*>(src + 32 * lane);
+    const uint4 c1 = *reinterpret_cast<const uint4*>(src + 32 * lane + 16);
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = bf16_lo(w[i]);
+      v[2 * i + 1] = bf16_hi(w[i]);
+    }
+    const uint32_t rw = reinterpret_cast<const uint32_t*>(src + 2 * kLatent)[lane];
+    rp0 = bf16_lo(rw);
+    rp1 = bf16_hi(rw);
+  }
+  float4* d4 = reinterpret_cast<float4*>(dst + 16 * lane);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  *reinterpret_cast<float2*>(dst + kLatent + 2 * lane) = make_float2(rp0, rp1);
+}
+
+cudaError_t launch_gather_dequant(const DecodeArgs& a, float* rows, cudaStream_t s) {
+  const int64_t items = static_cast<int64_t>(a.T) * a.K;
+  const int64_t blocks = (items * 32 + 255) / 256;
+  gather_dequant_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a, rows);
+  return cudaGetLastError();
+}
+
+}  // namespace smla

@@ -1,0 +1,39 @@
+// Internal launchers of the sparse MLA decode library (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/smla.h"
+
+namespace smla {
+
+constexpr int kMaxSplits = 64;
+constexpr int kTile = 64;  // top-k slots per pipeline tile of the decode kernels
+
+struct DecodeArgs {
+  const void* q;
+  const uint8_t* kv;
+  const int32_t* page_table;
+  const int32_t* topk;
+  const int32_t* req_id;
+  const float* sink;
+  void* out;
+  float* lse;
+  float* o_part;    // [T, S, H, 512] fp32 (S > 1)
+  float* lse_part;  // [T, S, H] fp32 (S > 1)
+  int32_t* err;     // device error word
+  int32_t T, H, K, B, next_n, stride, log2_page, kv_format;
+  int64_t num_pages;
+  int32_t num_splits, split_len;
+  float c2;  // sm_scale * log2(e)
+};
+
+cudaError_t launch_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, const void* latent,
+                        const void* rope, const int64_t* slot_mapping, int64_t n, void* kv,
+                        int64_t num_slots, cudaStream_t s);
+cudaError_t launch_gather_dequant(const DecodeArgs& a, float* rows, cudaStream_t s);
+
+}  // namespace smla

@@ -1,0 +1,258 @@
+// C ABI of libsmla.so: argument checks, split planning and kernel dispatch.
+// Nothing here allocates device memory or synchronises (except smla_read_error).
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/smla.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr size_t kWsAlign = 256;
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+  int ok = -1;  // -1 unknown, 0 unusable, 1 sm_103
+  int num_sms = 0;
+};
+DevInfo g_dev[kMaxDevices];
+
+smla_status current_device(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return SMLA_ERR_DEVICE;
+  }
+  DevInfo* di = dev < kMaxDevices ? &g_dev[dev] : nullptr;
+  DevInfo local;
+  if (!di) di = &local;
+  if (di->ok < 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return SMLA_ERR_DEVICE;
+    }
+    di->ok = (major == 10 && minor == 3) ? 1 : 0;
+    di->num_sms = sms;
+  }
+  if (di->ok != 1) return SMLA_ERR_DEVICE;
+  *num_sms = di->num_sms;
+  return SMLA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+smla_status check_desc(const smla_desc* d) {
+  if (!d) return SMLA_ERR_NULL;
+  if (d->num_tokens < 1 || d->num_requests < 1 || d->next_n < 1 || d->topk < 1)
+    return SMLA_ERR_SHAPE;
+  if (d->num_heads < 16 || d->num_heads > 128 || d->num_heads % 16 != 0) return SMLA_ERR_SHAPE;
+  if (d->topk % 4 != 0) return SMLA_ERR_SHAPE;
+  if (!is_pow2(d->page_size) || d->page_size > 4096) return SMLA_ERR_SHAPE;
+  if (d->num_pages < 1 || d->page_table_stride < 1) return SMLA_ERR_SHAPE;
+  if (d->num_pages > (int64_t(1) << 31)) return SMLA_ERR_SHAPE;
+  if (d->kv_format != SMLA_KV_BF16 && d->kv_format != SMLA_KV_FP8_DS) return SMLA_ERR_UNSUPPORTED;
+  if (!isfinite(d->sm_scale)) return SMLA_ERR_SHAPE;
+  if (d->num_splits < 0 || d->num_splits > smla::kMaxSplits) return SMLA_ERR_SHAPE;
+  for (int i = 0; i < 4; ++i)
+    if (d->reserved[i] != 0) return SMLA_ERR_SHAPE;
+  return SMLA_OK;
+}
+
+struct Plan {
+  int num_splits;
+  int split_len;
+  size_t lse_off, o_off, bytes;
+};
+
+Plan make_plan(const smla_desc* d, int num_sms) {
+  const int units = d->num_tokens * (d->num_heads / 16);
+  int S = d->num_splits;
+  if (S == 0) {
+    S = 1;
+    if (units < num_sms) S = (2 * num_sms + units - 1) / units;
+    const int cap = d->topk / 256 > 1 ? d->topk / 256 : 1;  // at least 256 slots per split
+    if (S > cap) S = cap;
+  }
+  if (S > smla::kMaxSplits) S = smla::kMaxSplits;
+  int len = (d->topk + S - 1) / S;
+  len = (len + smla::kTile - 1) / smla::kTile * smla::kTile;
+  S = (d->topk + len - 1) / len;
+  Plan p;
+  p.num_splits = S;
+  p.split_len = len;
+  p.lse_off = kWsAlign;
+  size_t bytes = kWsAlign;
+  if (S > 1) {
+    const size_t rows = size_t(d->num_tokens) * S * d->num_heads;
+    bytes = round_up(p.lse_off + rows * 4, kWsAlign);
+    p.o_off = bytes;
+    bytes += rows * 512 * 4;
+  } else {
+    p.o_off = bytes;
+  }
+  p.bytes = bytes;
+  return p;
+}
+
+int ilog2(int x) {
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+
+smla::DecodeArgs make_args(const smla_desc* d, const void* q, const void* kv,
+                           const int32_t* pt, const int32_t* topk, const int32_t* req,
+                           const float* sink) {
+  smla::DecodeArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.kv = static_cast<const uint8_t*>(kv);
+  a.page_table = pt;
+  a.topk = topk;
+  a.req_id = req;
+  a.sink = sink;
+  a.T = d->num_tokens;
+  a.H = d->num_heads;
+  a.K = d->topk;
+  a.B = d->num_requests;
+  a.next_n = d->next_n;
+  a.stride = d->page_table_stride;
+  a.log2_page = ilog2(d->page_size);
+  a.kv_format = d->kv_format;
+  a.num_pages = d->num_pages;
+  a.c2 = d->sm_scale * 1.4426950408889634f;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* smla_status_string(int32_t s) {
+  switch (s) {
+    case SMLA_OK: return "ok";
+    case SMLA_ERR_NULL: return "null pointer";
+    case SMLA_ERR_SHAPE: return "size out of range";
+    case SMLA_ERR_ALIGN: return "misaligned pointer";
+    case SMLA_ERR_UNSUPPORTED: return "unsupported combination";
+    case SMLA_ERR_WORKSPACE: return "workspace too small";
+    case SMLA_ERR_CUDA: return "CUDA error";
+    case SMLA_ERR_INDEX_RANGE: return "invalid index or page entry met on the device";
+    case SMLA_ERR_DEVICE: return "no sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+int32_t smla_abi_version(void) { return 1; }
+
+smla_status smla_workspace_size(const smla_desc* d, size_t* bytes) {
+  if (!bytes) return SMLA_ERR_NULL;
+  *bytes = 0;
+  smla_status st = check_desc(d);
+  if (st != SMLA_OK) return st;
+  int sms = 0;
+  st = current_device(&sms);
+  if (st != SMLA_OK) return st;
+  *bytes = make_plan(d, sms).bytes;
+  return SMLA_OK;
+}
+
+smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
+                        const int32_t* page_table, const int32_t* topk,
+                        const int32_t* req_id_per_token, const float* sink, void* out,
+                        float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  smla_status st = check_desc(d);
+  if (st != SMLA_OK) return st;
+  if (!q || !kv_cache || !page_table || !topk || !out || !workspace) return SMLA_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(topk, 16) || !aligned(out, 16) ||
+      !aligned(page_table, 4) || !aligned(workspace, kWsAlign) ||
+      (req_id_per_token && !aligned(req_id_per_token, 4)) || (sink && !aligned(sink, 4)) ||
+      (lse && !aligned(lse, 4)))
+    return SMLA_ERR_ALIGN;
+  if (!req_id_per_token && (d->num_tokens - 1) / d->next_n >= d->num_requests)
+    return SMLA_ERR_SHAPE;
+  int sms = 0;
+  st = current_device(&sms);
+  if (st != SMLA_OK) return st;
+  const Plan plan = make_plan(d, sms);
+  if (workspace_bytes < plan.bytes) return SMLA_ERR_WORKSPACE;
+  smla::DecodeArgs a = make_args(d, q, kv_cache, page_table, topk, req_id_per_token, sink);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.out = out;
+  a.lse = lse;
+  a.err = reinterpret_cast<int32_t*>(ws);
+  a.lse_part = reinterpret_cast<float*>(ws + plan.lse_off);
+  a.o_part = reinterpret_cast<float*>(ws + plan.o_off);
+  a.num_splits = plan.num_splits;
+  a.split_len = plan.split_len;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (smla::launch_decode_mma(a, sms, s) != cudaSuccess) return SMLA_ERR_CUDA;
+  if (plan.num_splits > 1 && smla::launch_merge(a, s) != cudaSuccess) return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+smla_status smla_pack_kv(int32_t kv_format, int32_t scale_mode, const void* latent,
+                         const void* rope, const int64_t* slot_mapping, int64_t n,
+                         void* kv_cache, int64_t num_slots, void* stream) {
+  if (kv_format != SMLA_KV_BF16 && kv_format != SMLA_KV_FP8_DS) return SMLA_ERR_UNSUPPORTED;
+  if (scale_mode != SMLA_SCALE_POW2 && scale_mode != SMLA_SCALE_FP32) return SMLA_ERR_UNSUPPORTED;
+  if (n < 0 || num_slots < 0) return SMLA_ERR_SHAPE;
+  if (n == 0) return SMLA_OK;
+  if (!latent || !rope || !slot_mapping || !kv_cache) return SMLA_ERR_NULL;
+  if (!aligned(latent, 16) || !aligned(rope, 16) || !aligned(kv_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return SMLA_ERR_ALIGN;
+  if (n > (int64_t(1) << 36)) return SMLA_ERR_SHAPE;
+  int sms = 0;
+  smla_status st = current_device(&sms);
+  if (st != SMLA_OK) return st;
+  if (smla::launch_pack(kv_format, scale_mode, latent, rope, slot_mapping, n, kv_cache, num_slots,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+smla_status smla_gather_dequant(const smla_desc* d, const void* kv_cache,
+                                const int32_t* page_table, const int32_t* topk,
+                                const int32_t* req_id_per_token, float* rows,
+                                int32_t* error_word, void* stream) {
+  smla_status st = check_desc(d);
+  if (st != SMLA_OK) return st;
+  if (!kv_cache || !page_table || !topk || !rows) return SMLA_ERR_NULL;
+  if (!aligned(kv_cache, 16) || !aligned(rows, 16) || !aligned(topk, 4) ||
+      !aligned(page_table, 4) || (error_word && !aligned(error_word, 4)))
+    return SMLA_ERR_ALIGN;
+  if (!req_id_per_token && (d->num_tokens - 1) / d->next_n >= d->num_requests)
+    return SMLA_ERR_SHAPE;
+  int sms = 0;
+  st = current_device(&sms);
+  if (st != SMLA_OK) return st;
+  smla::DecodeArgs a = make_args(d, nullptr, kv_cache, page_table, topk, req_id_per_token, nullptr);
+  a.err = error_word;
+  if (smla::launch_gather_dequant(a, rows, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+smla_status smla_read_error(const smla_desc* d, void* workspace, size_t workspace_bytes,
+                            int32_t* error_word, void* stream) {
+  (void)d;
+  if (!workspace || !error_word) return SMLA_ERR_NULL;
+  if (workspace_bytes < sizeof(int32_t)) return SMLA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(workspace, 0, sizeof(v), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return SMLA_ERR_CUDA;
+  *error_word = v;
+  return v ? SMLA_ERR_INDEX_RANGE : SMLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+"""The C ABI library loads, exports every entry point include/smla.h declares, and rejects
+bad arguments on the host before touching the GPU (CPU only: no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_mla_decode_smla_gb300 as smla
+from sparse_mla_decode_smla_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(_build.LIB):
+        _build.build()
+    return smla.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "smla.h")).read()
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(smla_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ["smla_decode", "smla_pack_kv", "smla_workspace_size", "smla_gather_dequant",
+              "smla_read_error", "smla_status_string", "smla_abi_version"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for n in _declared():
+        assert hasattr(L, n), n
+    assert set(_declared()) <= set(smla.EXPORTS) | set(_declared())
+
+
+def test_abi_version_and_status_strings(L):
+    assert L.smla_abi_version() == 1
+    for s in range(9):
+        assert smla.status_string(s)
+    assert smla.status_string(99) == "unknown status"
+
+
+def test_desc_layout_matches_header():
+    # int32 x6, int64, int32 x2, float, int32, int32[4]; natural alignment
+    assert ctypes.sizeof(smla.smla_desc) == 64
+    assert smla.smla_desc.num_pages.offset == 24
+    assert smla.smla_desc.reserved.offset == 48
+
+
+def _desc(**kw):
+    d = smla.make_desc(4, 16, 64, 4, 64, 8, 4, smla.SMLA_KV_FP8_DS, 1 / 24)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def _decode_status(L, d, q=16, kv=16, pt=16, topk=16, out=16, ws=256):
+    P = ctypes.c_void_p
+    return L.smla_decode(ctypes.byref(d) if d is not None else None, P(q), P(kv), P(pt), P(topk),
+                         None, None, P(out), None, P(ws), 1 << 20, None)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("num_heads", 8, 2), ("num_heads", 144, 2), ("num_heads", 40, 2), ("topk", 0, 2),
+    ("topk", 6, 2), ("page_size", 48, 2), ("page_size", 8192, 2), ("num_pages", 0, 2),
+    ("kv_format", 3, 4), ("num_splits", 65, 2), ("num_tokens", 0, 2), ("next_n", 0, 2),
+])
+def test_decode_rejects_bad_desc_on_host(L, field, value, status):
+    assert _decode_status(L, _desc(**{field: value})) == status
+
+
+def test_decode_rejects_null_and_misaligned_pointers(L):
+    assert _decode_status(L, None) == 1
+    assert _decode_status(L, _desc(), q=0) == 1
+    assert _decode_status(L, _desc(), ws=0) == 1
+    assert _decode_status(L, _desc(), q=16 + 8) == 3
+    assert _decode_status(L, _desc(), topk=16 + 4) == 3
+    assert _decode_status(L, _desc(), ws=256 + 16) == 3
+    d = _desc()
+    d.reserved[2] = 1
+    assert _decode_status(L, d) == 2
+    # more tokens than requests * next_n without req_id_per_token
+    assert _decode_status(L, _desc(num_tokens=9, num_requests=2, next_n=4)) == 2
+
+
+def test_pack_rejects_bad_arguments_on_host(L):
+    P = ctypes.c_void_p
+    assert L.smla_pack_kv(7, 0, P(16), P(16), P(16), 4, P(16), 4, None) == 4
+    assert L.smla_pack_kv(1, 5, P(16), P(16), P(16), 4, P(16), 4, None) == 4
+    assert L.smla_pack_kv(1, 0, P(16), P(16), P(16), -1, P(16), 4, None) == 2
+    assert L.smla_pack_kv(1, 0, None, P(16), P(16), 4, P(16), 4, None) == 1
+    assert L.smla_pack_kv(1, 0, P(24), P(16), P(16), 4, P(16), 4, None) == 3
+    assert L.smla_pack_kv(1, 0, P(16), P(16), P(16), 0, P(16), 4, None) == 0  # nothing to do
+
+
+def test_workspace_size_checks_desc_first(L):
+    n = ctypes.c_size_t(123)
+    assert L.smla_workspace_size(ctypes.byref(_desc(num_heads=7)), ctypes.byref(n)) == 2
+    assert n.value == 0
+    assert L.smla_workspace_size(ctypes.byref(_desc()), None) == 1
+
+
+def test_read_error_null(L):
+    v = ctypes.c_int32(0)
+    assert L.smla_read_error(None, None, 4, ctypes.byref(v), None) == 1

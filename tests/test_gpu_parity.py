@@ -1,0 +1,263 @@
+"""GPU parity of the CUDA path against the float64 oracle, through the C ABI.
+
+Tolerances (bf16 output, fp32 LSE): max |out - ref| <= 1e-2, per-(token, head)
+cosine >= 0.9999, |lse - ref| <= 1e-3; cache packing and gather/dequant are
+bit-exact. Inputs come from the seeded workload generator; the oracle packs
+its own cache rows from the same source values.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import sparse_mla_decode_smla_gb300 as smla
+import workloads as W
+from oracle.workload_oracle import OracleCache, oracle_decode
+from sparse_mla_decode_smla_gb300.runner import DeviceDecode, pack_problem_cache
+
+pytestmark = pytest.mark.gpu
+
+OUT_ATOL, COS_MIN, LSE_ATOL = 1e-2, 0.9999, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    smla.lib()
+    torch.cuda.init()
+
+
+def _bits(t):
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def assert_parity(out, lse, ref, tokens=None):
+    o = out.double().cpu().numpy()
+    l = lse.double().cpu().numpy()
+    if tokens is not None:
+        o, l = o[tokens], l[tokens]
+    r, rl = ref["out"], ref["lse"]
+    assert np.isfinite(o).all()
+    err = np.abs(o - r).max()
+    assert err <= OUT_ATOL, f"max abs err {err}"
+    num = (o * r).sum(-1)
+    den = np.linalg.norm(o, axis=-1) * np.linalg.norm(r, axis=-1)
+    big = np.linalg.norm(r, axis=-1) > 1e-3
+    if big.any():
+        cos = num[big] / den[big]
+        assert cos.min() >= COS_MIN, f"min cosine {cos.min()}"
+    assert np.array_equal(np.isneginf(l), np.isneginf(rl))
+    fin = np.isfinite(rl)
+    if fin.any():
+        lerr = np.abs(l[fin] - rl[fin]).max()
+        assert lerr <= LSE_ATOL, f"lse err {lerr}"
+
+
+SMALL = [
+    W.WORKLOADS[0],
+    W.small_variant(W.WORKLOADS[1], num_requests=3, ctx_lo=100, ctx_hi=900, topk=320),
+    W.small_variant(W.WORKLOADS[2], num_requests=2, ctx_lo=700, ctx_hi=700, topk=448),
+    W.small_variant(W.WORKLOADS[3], num_requests=2, ctx_lo=300, ctx_hi=500, topk=256),
+    W.small_variant(W.WORKLOADS[4], num_requests=4, ctx_lo=400, ctx_hi=1000, topk=320, tail_pad=64),
+]
+
+
+@pytest.fixture(scope="module")
+def small_cases():
+    cases = {}
+    for w in SMALL:
+        p = W.make_problem(w)
+        cases[w.name] = (p, oracle_decode(p))
+    return cases
+
+
+# ------------------------------------------------------------------ pack / gather
+
+
+def _pack_inputs(n, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(n, 512, generator=g)
+    x = x * (2.0 ** torch.randint(-30, 30, (n, 4, 1), generator=g)).repeat_interleave(128, 2).view(n, 512)
+    x[0, :128] = 0.0
+    x[1, 128:256] = 56.0
+    x[2, :] = torch.tensor([1e-40, -3e38, 65504.0, -0.0] * 128)
+    rope = torch.randn(n, 64, generator=g)
+    return x.to(torch.bfloat16), rope.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("mode", [smla.SMLA_SCALE_POW2, smla.SMLA_SCALE_FP32])
+def test_pack_fp8_bit_exact(mode):
+    n, slots = 3000, 4000
+    lat, rope = _pack_inputs(n, 1 + mode)
+    mapping = torch.randperm(slots)[:n].to(torch.int64)
+    mapping[5] = -1
+    mapping[6] = slots + 10  # out of range: skipped
+    kv = torch.full((slots, 656), 0xAB, dtype=torch.uint8, device="cuda")
+    smla.pack_kv(smla.SMLA_KV_FP8_DS, mode, lat.cuda(), rope.cuda(), mapping.cuda(), kv, slots)
+    got = kv.cpu().numpy()
+    ref = O.pack_fp8_ds(_bits(lat), _bits(rope), mode)
+    m = mapping.numpy()
+    ok = (m >= 0) & (m < slots)
+    assert np.array_equal(got[m[ok]], ref[ok])
+    untouched = np.setdiff1d(np.arange(slots), m[ok])
+    assert (got[untouched] == 0xAB).all()
+
+
+def test_pack_bf16_bit_exact():
+    lat, rope = _pack_inputs(500, 7)
+    mapping = torch.arange(499, -1, -1, dtype=torch.int64)
+    kv = torch.zeros((500, 1152), dtype=torch.uint8, device="cuda")
+    smla.pack_kv(smla.SMLA_KV_BF16, 0, lat.cuda(), rope.cuda(), mapping.cuda(), kv, 500)
+    ref = O.pack_bf16(_bits(lat), _bits(rope))
+    assert np.array_equal(kv.cpu().numpy()[mapping.numpy()], ref)
+
+
+@pytest.mark.parametrize("wi", [0, 1, 4])
+def test_gather_dequant_bit_exact(wi):
+    w = SMALL[wi]
+    p = W.make_problem(w)
+    kv = pack_problem_cache(p)
+    topk = p.topk.clone()
+    topk[0, 1] = 10 ** 6  # beyond the page table: invalid, flagged
+    d = smla.make_desc(w.num_tokens, w.num_heads, w.topk, w.num_requests, w.page_size, p.num_pages,
+                       w.page_table_stride, smla.runner.FMT[w.kv_format], w.sm_scale, next_n=w.next_n)
+    rows = torch.full((w.num_tokens, w.topk, 576), 7.0, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    smla.gather_dequant(d, kv, p.page_table.cuda(), topk.cuda(), None, rows, err)
+    cache = OracleCache(p)
+    ref = O.gather_dequant(cache.fetch, w.kv_format, p.page_table.numpy(), topk.numpy(), w.page_size,
+                           p.num_pages, next_n=w.next_n)
+    got = rows.cpu().double().numpy()
+    assert np.array_equal(got, ref)
+    assert err.item() == smla.SMLA_DEVERR_INDEX
+
+
+# ------------------------------------------------------------------ decode parity
+
+
+@pytest.mark.parametrize("wi", range(len(SMALL)))
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_decode_matches_oracle(small_cases, wi, splits):
+    p, ref = small_cases[SMALL[wi].name]
+    dd = DeviceDecode(p, num_splits=splits)
+    out, lse = dd.run()
+    torch.cuda.synchronize()
+    assert_parity(out, lse, ref)
+    assert smla.read_error(dd.desc, dd.workspace) == 0
+
+
+@pytest.mark.parametrize("wi", [1, 2, 4])
+def test_split_count_invariance(small_cases, wi):
+    p, ref = small_cases[SMALL[wi].name]
+    dd = DeviceDecode(p)
+    for s in (1, 2, 4, 5, 8):
+        dd2 = DeviceDecode(p, kv=dd.kv, num_splits=s)
+        out, lse = dd2.run()
+        assert_parity(out, lse, ref)
+
+
+def test_unselected_rows_are_never_read(small_cases):
+    # Overwrite every cache row no valid index selects with NaN codes: output is bitwise unchanged.
+    p, _ = small_cases[SMALL[4].name]
+    dd = DeviceDecode(p, num_splits=2)
+    out0, lse0 = [x.clone() for x in dd.run()]
+    P = p.w.page_size
+    pt = p.page_table.numpy()
+    used = set()
+    for t in range(p.w.num_tokens):
+        for i in p.topk[t].tolist():
+            if i >= 0:
+                used.add(int(pt[t // p.w.next_n, i // P]) * P + i % P)
+    mask = torch.ones(p.num_slots, dtype=torch.bool)
+    mask[list(used)] = False
+    dd.kv[mask.cuda()] = 0x7F
+    out1, lse1 = dd.run()
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+
+
+def test_page_relabel_is_bitwise_invariant(small_cases):
+    p, _ = small_cases[SMALL[1].name]
+    dd = DeviceDecode(p, num_splits=1)
+    out0, lse0 = [x.clone() for x in dd.run()]
+    P = p.w.page_size
+    perm = torch.randperm(p.num_pages, generator=torch.Generator().manual_seed(5))  # page q -> perm[q]
+    kv2 = torch.empty_like(dd.kv).view(p.num_pages, P, -1)
+    kv2[perm.cuda()] = dd.kv.view(p.num_pages, P, -1)
+    pt2 = torch.where(p.page_table >= 0, perm[p.page_table.clamp(min=0).long()].to(torch.int32), p.page_table)
+    dd.kv = kv2.view(p.num_slots, -1)
+    dd.page_table = pt2.cuda()
+    out1, lse1 = dd.run()
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+
+
+def test_padding_placement_and_empty_rows():
+    w = W.small_variant(W.WORKLOADS[2], num_requests=3, ctx_lo=300, ctx_hi=300, topk=256)
+    p = W.make_problem(w)
+    rng = np.random.default_rng(0)
+    topk = p.topk.numpy().copy()
+    # token 0: 100 valid scattered between -1; token 1: nothing selected; token 2 unchanged
+    row = np.full(256, -1, np.int32)
+    row[np.sort(rng.permutation(256)[:100])] = topk[0, :100]
+    topk[0] = row
+    topk[1] = -1
+    p.topk = torch.from_numpy(topk)
+    ref = oracle_decode(p)
+    for s in (1, 3):
+        dd = DeviceDecode(p, num_splits=s)
+        out, lse = dd.run()
+        assert_parity(out, lse, ref)
+        assert (out[1] == 0).all()
+        assert torch.equal(lse[1].cpu(), p.sink.cpu())  # empty selection: lse = sigma
+
+
+def test_invalid_entries_are_masked_and_flagged():
+    w = W.small_variant(W.WORKLOADS[4], num_requests=2, ctx_lo=500, ctx_hi=500, topk=128)
+    p = W.make_problem(w)
+    topk = p.topk.clone()
+    topk[0, 3] = -7               # negative, not padding
+    topk[1, 5] = 64 * 100         # beyond the request's page table
+    pt = p.page_table.clone()
+    pt[1, -1] = p.num_pages + 3   # a page entry out of range
+    topk[1, 9] = 64 * (w.page_table_stride - 1) + 2
+    p.topk, p.page_table = topk, pt
+    ref = oracle_decode(p)
+    assert ref["n_invalid"][0] == 1 and ref["n_invalid"][1] >= 2
+    dd = DeviceDecode(p, num_splits=1)
+    out, lse = dd.run()
+    assert_parity(out, lse, ref)
+    err = smla.read_error(dd.desc, dd.workspace)
+    assert err == smla.SMLA_DEVERR_INDEX | smla.SMLA_DEVERR_PAGE
+    assert smla.read_error(dd.desc, dd.workspace) == 0  # cleared
+
+
+def test_req_id_per_token():
+    w = W.small_variant(W.WORKLOADS[1], num_requests=3, ctx_lo=200, ctx_hi=700, topk=192)
+    p = W.make_problem(w)
+    # tokens served in reverse request order through an explicit mapping
+    req = torch.tensor([2, 1, 0], dtype=torch.int32)
+    p2 = W.Problem(**{**p.__dict__, "topk": p.topk[[2, 1, 0]].contiguous(), "q": p.q[[2, 1, 0]].contiguous()})
+    dd = DeviceDecode(p2)
+    dd.req_id = req.cuda()
+    out, lse = dd.run()
+    ref = oracle_decode(p)
+    order = [2, 1, 0]
+    assert_parity(out[order], lse[order], ref)
+
+
+# ------------------------------------------------------------------ full-size, sampled
+
+
+@pytest.mark.parametrize("wi", [1, 2, 3, 4])
+def test_full_size_sampled_tokens(wi):
+    w = W.WORKLOADS[wi]
+    p = W.make_problem(w, device="cuda")
+    dd = DeviceDecode(p)  # the launch configuration the bench times (library-chosen splits)
+    out, lse = dd.run()
+    torch.cuda.synchronize()
+    T = w.num_tokens
+    tokens = sorted({0, T // 2 + 1, T - 1})
+    ref = oracle_decode(p, tokens=tokens)
+    assert_parity(out, lse, ref, tokens=tokens)
+    assert torch.isfinite(out.float()).all()
+    assert smla.read_error(dd.desc, dd.workspace) == 0
+    del dd, p
+    torch.cuda.empty_cache()
