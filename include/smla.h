@@ -157,6 +157,39 @@ smla_status smla_gather_dequant(const smla_desc* d, const void* kv_cache,
 smla_status smla_read_error(const smla_desc* d, void* workspace, size_t workspace_bytes,
                             int32_t* error_word, void* stream);
 
+/*
+ * Size of the library-owned scratch array used by smla_decode_noalloc (16 MiB per device).
+ */
+#define SMLA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * smla_decode without a caller-provided workspace. The pages have no counterpart for
+ * this entry point: it exists for callers that cannot call cudaMalloc or own a device
+ * allocator -- for example a plugin or callback running inside another serving engine
+ * that has reserved the GPU's memory up front and forbids allocation on its hot path
+ * (cudaMalloc synchronises the device and may fail once the pool is taken), or a
+ * binding that only ever receives the engine's own input and output buffers.
+ *
+ * The split partials and the device error word live in a file-scope __device__ array
+ * of SMLA_NOALLOC_SCRATCH_BYTES bytes inside libsmla.so. Every GPU that loads the
+ * library holds that array until the process exits. The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress) with that device current; make
+ * that first call before any stream capture. The entry point itself calls no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Arguments are those of smla_decode minus the workspace. A call whose split partials
+ * would not fit in the array returns SMLA_ERR_WORKSPACE before launching anything
+ * (choose num_splits = 1, which needs no partials, or fewer splits). All calls share
+ * the one array, and its contents persist from call to call: calls that overlap on
+ * the GPU (different streams, or different host threads) race on it and must be
+ * serialised by the caller. The device error word is cleared at the start of each
+ * call; it is not readable through this entry point.
+ */
+smla_status smla_decode_noalloc(const smla_desc* d, const void* q, const void* kv_cache,
+                                const int32_t* page_table, const int32_t* topk,
+                                const int32_t* req_id_per_token, const float* sink, void* out,
+                                float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

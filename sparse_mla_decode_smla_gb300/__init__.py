@@ -23,7 +23,8 @@ STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_NULL", 2: "SMLA_ERR_SHAPE", 3: "SMLA_ERR_AL
           4: "SMLA_ERR_UNSUPPORTED", 5: "SMLA_ERR_WORKSPACE", 6: "SMLA_ERR_CUDA",
           7: "SMLA_ERR_INDEX_RANGE", 8: "SMLA_ERR_DEVICE"}
 EXPORTS = ["smla_status_string", "smla_abi_version", "smla_workspace_size", "smla_decode",
-           "smla_pack_kv", "smla_gather_dequant", "smla_read_error"]
+           "smla_pack_kv", "smla_gather_dequant", "smla_read_error", "smla_decode_noalloc"]
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class SmlaError(RuntimeError):
@@ -65,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.smla_pack_kv.argtypes = [I32, I32, P, P, P, I64, P, I64, P]
         L.smla_gather_dequant.restype = I32
         L.smla_gather_dequant.argtypes = [D, P, P, P, P, P, P, P]
+        L.smla_decode_noalloc.restype = I32
+        L.smla_decode_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P]
         L.smla_read_error.restype = I32
         L.smla_read_error.argtypes = [D, P, SZ, ctypes.POINTER(I32), P]
         _lib = L
@@ -113,6 +116,19 @@ def decode(desc, q, kv_cache, page_table, topk, req_id_per_token, sink, out, lse
         ctypes.byref(desc), _ptr(q), _ptr(kv_cache), _ptr(page_table), _ptr(topk),
         _ptr(req_id_per_token), _ptr(sink), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def decode_noalloc(desc, q, kv_cache, page_table, topk, req_id_per_token, sink, out, lse,
+                   stream=None):
+    """smla_decode with the library's own scratch array instead of a workspace.
+
+    For callers that cannot allocate device memory. Calls share one scratch array per
+    device, so overlapping calls race; the first call on a device must precede any
+    stream capture.
+    """
+    _check("smla_decode_noalloc", lib().smla_decode_noalloc(
+        ctypes.byref(desc), _ptr(q), _ptr(kv_cache), _ptr(page_table), _ptr(topk),
+        _ptr(req_id_per_token), _ptr(sink), _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def pack_kv(kv_format, scale_mode, latent, rope, slot_mapping, kv_cache, num_slots, stream=None):

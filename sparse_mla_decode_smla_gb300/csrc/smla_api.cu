@@ -256,3 +256,54 @@ smla_status smla_read_error(const smla_desc* d, void* workspace, size_t workspac
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Workspace-free entry point: the scratch lives in this file-scope device array.
+// ---------------------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[SMLA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch, looked up once per device with that device current.
+void* g_noalloc_addr[kMaxDevices];
+
+smla_status noalloc_scratch(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return SMLA_ERR_DEVICE;
+  }
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return SMLA_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = p;
+  }
+  *ptr = g_noalloc_addr[dev];
+  return SMLA_OK;
+}
+
+}  // namespace
+
+extern "C" smla_status smla_decode_noalloc(const smla_desc* d, const void* q, const void* kv_cache,
+                                           const int32_t* page_table, const int32_t* topk,
+                                           const int32_t* req_id_per_token, const float* sink,
+                                           void* out, float* lse, void* stream) {
+  smla_status st = check_desc(d);
+  if (st != SMLA_OK) return st;
+  if (!q || !kv_cache || !page_table || !topk || !out) return SMLA_ERR_NULL;
+  int sms = 0;
+  st = current_device(&sms);
+  if (st != SMLA_OK) return st;
+  if (make_plan(d, sms).bytes > SMLA_NOALLOC_SCRATCH_BYTES) return SMLA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != SMLA_OK) return st;
+  // the error word (first 4 bytes) is the only part that must start at zero
+  if (cudaMemsetAsync(scratch, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SMLA_ERR_CUDA;
+  return smla_decode(d, q, kv_cache, page_table, topk, req_id_per_token, sink, out, lse, scratch,
+                     SMLA_NOALLOC_SCRATCH_BYTES, stream);
+}
