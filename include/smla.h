@@ -58,7 +58,8 @@ enum {
 /* Bits of the device error word (smla_read_error). */
 enum {
   SMLA_DEVERR_INDEX = 1, /* a top-k entry other than -1 outside [0, page_table_stride*page_size) */
-  SMLA_DEVERR_PAGE = 2   /* a page-table entry used by a valid index outside [0, num_pages) */
+  SMLA_DEVERR_PAGE = 2,  /* a page-table entry used by a valid index outside [0, num_pages) */
+  SMLA_DEVERR_TIMEOUT = 4 /* an internal pipeline wait gave up (bounded waits; outputs invalid) */
 };
 
 typedef struct smla_desc {

@@ -1,31 +1,36 @@
-// Sparse MLA decode, warp-level tensor-core path (mma.sync m16n8k16), one CTA per
-// (query token, top-k split, group of 16 heads).
+// Sparse MLA decode, warp-level tensor-core path (mma.sync m16n8k16). One CTA per
+// (query token, top-k split, group of 16 heads); 4 consumer warps + 1 producer warp.
 //
 // What it computes (vLLM PR #43477 "关键源码片段", forward_mqa; SGLang PR #24692
 // "实现拆解 2": tiled sparse decode with online softmax, split merge, sink): for each
 // selected slot j, s_j = sm_scale * <q_h, k_j> over 576 dims, out_h = softmax-weighted
 // sum of v_j = k_j[0:512].
 //
-// Design (4 warps, warp w owns latent block w = dims [128w, 128w+128)):
-//  * Gather: the top-k list of the split is walked in tiles of 64 slots. Threads 0..63
-//    translate each slot's index through the page table one tile ahead of use; all 128
-//    threads then copy whole rows into a 2-stage shared-memory ring with 16-byte
-//    cp.async (zero-fill for padding: padded rows are never read from HBM).
-//  * QK: warp w multiplies its 128 latent dims (+ RoPE dims [16w, 16w+16)) for all 64
-//    slots. q is held in registers as A fragments (f16 for the latent, bf16 for RoPE).
-//    B fragments are built straight from the staged E4M3 bytes with cvt.rn.f16x2.e4m3x2:
-//    the k order inside an mma is permuted so that each thread reads 16 contiguous bytes
-//    of one row, and q is permuted the same way. The per-128 scale multiplies the fp32
-//    partial score of block w (exact for the fp32 product it replaces up to rounding).
+// Producer warp: walks the split's top-k list 32 slots at a time. Index loads run two
+// tiles ahead and page-table loads one tile ahead, so the dependent-load chain stays off
+// the critical path. Each valid slot's whole 656-byte row is fetched with one bulk copy
+// (cp.async.bulk, TMA engine) into a 4-stage shared-memory ring; the stage's mbarrier
+// counts the bytes. Padding and invalid entries are never fetched.
+//
+// Consumer warps (warp w owns latent block w = dims [128w, 128w+128)):
+//  * QK: warp w multiplies its 128 latent dims (+ RoPE dims [16w, 16w+16)) for the 32
+//    slots of the stage. q sits in registers as A fragments (f16 for the latent, bf16 for
+//    RoPE). B fragments are built from the staged E4M3 bytes with cvt.rn.f16x2.e4m3x2:
+//    the k order inside an mma is permuted so each thread reads 16 contiguous bytes of a
+//    row, and q is permuted the same way. The per-128 scale multiplies the fp32 partial
+//    score of block w.
 //  * The four partial scores are summed through shared memory; warp w then owns slots
-//    [16w, 16w+16) of the tile for the masked online softmax (base-2, running max).
+//    [8w, 8w+8) of the stage for the masked base-2 online softmax.
 //  * PV: O^T[dims, heads] = V^T P^T. Warp w accumulates its 128 output dims. A fragments
 //    (V^T) come from the staged bytes of four rows, paired by prmt and converted; the
-//    B fragments are the probabilities times scale_w[j] / r_w, where r_w is the running
-//    maximum of scale_w over the slots seen (keeps the f16 operand in [0, 1]).
-//  * Epilogue: o = O * r_w / l and lse = (m + log2 l) * ln 2. With one split the sink is
-//    applied here and bf16 out / fp32 lse are written; otherwise the fp32 partials go to
-//    the workspace and the merge kernel finishes.
+//    B fragments are p * scale_w[j] / r_w, with r_w the running maximum of scale_w over
+//    the slots seen (keeps the f16 operand in [0, 1]).
+//  * Epilogue: o = O * r_w / l, lse = (m + log2 l) * ln 2. With one split the sink is
+//    applied here; otherwise fp32 partials go to the workspace for the merge kernel.
+// Slots that are never fetched keep whatever finite bytes the ring held (it starts
+// zeroed): their score is replaced by -inf, so their probability is exactly 0.
+// All waits are mbarrier waits bounded in time; a wait that gives up sets
+// SMLA_DEVERR_TIMEOUT and the CTA leaves after its copies in flight have landed.
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -34,43 +39,43 @@
 namespace smla {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kStages = 2;  // 2 x 64-row stages: bf16 fits, and two CTAs per SM for fp8_ds
-constexpr int kRing = kStages + 1;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kSlots = 32;  // slots per stage
 
 template <int FMT>
-struct Fmt {
-  static constexpr int kRowBytes = FMT == SMLA_KV_FP8_DS ? kFp8RowBytes : kBf16RowBytes;
-  static constexpr int kChunks = kRowBytes / 16;
+struct Cfg {
+  static constexpr bool kFp8 = FMT == SMLA_KV_FP8_DS;
+  static constexpr int kRowBytes = kFp8 ? kFp8RowBytes : kBf16RowBytes;
+  static constexpr int kStages = kFp8 ? 4 : 3;
+  static constexpr size_t kRing = size_t(kStages) * kSlots * kRowBytes;
+  static constexpr size_t kRed = 4 * 4 * 32 * 16;  // partial scores [warp][nt][lane] float4
+  static constexpr size_t kPbuf = 4 * 32 * 16;     // probabilities [nt][lane] float4
+  static constexpr size_t kSmall = 64 * 4 + 64 * 4 + 16 * 4;  // maxima, row sums, stage masks
+  static constexpr size_t kBars = (2 * kStages + 4) * 8;
+  static constexpr size_t kSmem = kRing + kRed + kPbuf + kSmall + kBars;
 };
-
-template <int FMT>
-constexpr size_t smem_bytes() {
-  return size_t(kStages) * kTile * Fmt<FMT>::kRowBytes  // stage ring
-         + 4 * 8 * 32 * 16                              // partial scores
-         + 4 * 32 * 8 * 4                               // probabilities
-         + 64 * 4 + 64 * 4                              // tile maxima, row sums
-         + kRing * kTile * 8                            // physical slot ring
-         + kRing * 2 * 4;                               // valid masks
-}
 
 __device__ __forceinline__ float fmax4(float a, float b, float c, float d) {
   return fmaxf(fmaxf(a, b), fmaxf(c, d));
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads) decode_mma_kernel(const DecodeArgs p) {
-  constexpr bool kFp8 = FMT == SMLA_KV_FP8_DS;
-  constexpr int RB = Fmt<FMT>::kRowBytes;
-  constexpr int CH = Fmt<FMT>::kChunks;
+__global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeArgs p) {
+  using C = Cfg<FMT>;
+  constexpr bool kFp8 = C::kFp8;
+  constexpr int RB = C::kRowBytes;
+  constexpr int NST = C::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* stage = smem;
-  float4* red = reinterpret_cast<float4*>(smem + size_t(kStages) * kTile * RB);
-  float* pbuf = reinterpret_cast<float*>(red + 4 * 8 * 32);
-  float* mx = pbuf + 4 * 32 * 8;
+  uint8_t* ring = smem;
+  float4* red = reinterpret_cast<float4*>(smem + C::kRing);
+  float4* pbuf = reinterpret_cast<float4*>(smem + C::kRing + C::kRed);
+  float* mx = reinterpret_cast<float*>(smem + C::kRing + C::kRed + C::kPbuf);
   float* lsum = mx + 64;
-  int64_t* ring = reinterpret_cast<int64_t*>(lsum + 64);
-  uint32_t* ring_mask = reinterpret_cast<uint32_t*>(ring + kRing * kTile);
+  uint32_t* meta = reinterpret_cast<uint32_t*>(lsum + 64);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kRing + C::kRed + C::kPbuf + C::kSmall);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + NST), cbar0 = smem_u32(bars + 2 * NST);
+  const uint32_t ring_s = smem_u32(ring);
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, g = lane >> 2, c = lane & 3;
   const int HG = p.H >> 4;
@@ -83,14 +88,79 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const DecodeArgs p
 
   const int r = p.req_id ? __ldg(p.req_id + t) : t / p.next_n;
   const bool req_ok = r >= 0 && r < p.B;
-  if (!req_ok && tid == 0 && hg == 0 && split == 0) atomicOr(p.err, SMLA_DEVERR_INDEX);
   const int32_t* pt_row = p.page_table + int64_t(req_ok ? r : 0) * p.stride;
   const int32_t* idx_row = p.topk + int64_t(t) * p.K;
   const int j0 = split * p.split_len;
   const int j1 = min(p.K, j0 + p.split_len);
-  const int ntiles = req_ok ? max(0, (j1 - j0 + kTile - 1) / kTile) : 0;
+  const int ntiles = req_ok ? max(0, (j1 - j0 + kSlots - 1) / kSlots) : 0;
 
-  // ---- q fragments (registers for the whole kernel)
+  // ---- set-up: zeroed ring (never-fetched slots must hold finite bytes), barriers
+  {
+    uint4* z = reinterpret_cast<uint4*>(ring);
+    for (size_t k = tid; k < C::kRing / 16; k += kThreads) z[k] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (tid == 0) {
+      for (int s = 0; s < NST; ++s) {
+        mbar_init(full0 + 8 * s, 1);
+        mbar_init(empty0 + 8 * s, kConsumerWarps);
+      }
+      for (int k = 0; k < 4; ++k) mbar_init(cbar0 + 8 * k, kConsumerWarps);
+      if (!req_ok) atomicOr(p.err, SMLA_DEVERR_INDEX);
+    }
+    __syncthreads();
+  }
+
+  // =================================================================== producer warp
+  if (w == kConsumerWarps) {
+    auto idx_at = [&](int tile) -> int32_t {
+      const int j = j0 + tile * kSlots + lane;
+      return (tile < ntiles && j < j1) ? __ldg(idx_row + j) : -1;
+    };
+    auto page_of = [&](int32_t idx) -> int32_t {
+      return (idx >= 0 && (idx >> p.log2_page) < p.stride) ? __ldg(pt_row + (idx >> p.log2_page)) : -1;
+    };
+    int32_t idx_a = idx_at(0), idx_b = idx_at(1);
+    int32_t pg_a = page_of(idx_a);
+    int issued = 0;
+    bool ok = true;
+    for (int i = 0; i < ntiles; ++i) {
+      const int32_t idx_c = idx_a, pg_c = pg_a;
+      idx_a = idx_b;
+      idx_b = idx_at(i + 2);
+      pg_a = page_of(idx_a);
+      const int st = i % NST;
+      if (!mbar_wait(empty0 + 8 * st, ((i / NST) & 1) ^ 1)) {
+        ok = false;
+        break;
+      }
+      int64_t phys = -1;
+      if (idx_c != -1) {
+        if (idx_c < 0 || (idx_c >> p.log2_page) >= p.stride) {
+          atomicOr(p.err, SMLA_DEVERR_INDEX);
+        } else if (pg_c < 0 || pg_c >= p.num_pages) {
+          atomicOr(p.err, SMLA_DEVERR_PAGE);
+        } else {
+          phys = (int64_t(pg_c) << p.log2_page) + (idx_c & ((1 << p.log2_page) - 1));
+        }
+      }
+      const uint32_t vmask = __ballot_sync(0xffffffffu, phys >= 0);
+      if (lane == 0) {
+        meta[st] = vmask;
+        mbar_arrive_expect_tx(full0 + 8 * st, uint32_t(__popc(vmask)) * RB);
+      }
+      __syncwarp();
+      if (phys >= 0)
+        bulk_g2s(ring_s + (st * kSlots + lane) * RB, p.kv + phys * RB, RB, full0 + 8 * st);
+      issued = i + 1;
+    }
+    if (!ok && lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
+    // never leave while copies into this CTA's shared memory are in flight
+    for (int i = max(0, issued - NST); i < issued; ++i)
+      if (!mbar_wait(full0 + 8 * (i % NST), (i / NST) & 1)) break;
+    return;
+  }
+
+  // =================================================================== consumer warps
   const __nv_bfloat16* qt =
       reinterpret_cast<const __nv_bfloat16*>(p.q) + (int64_t(t) * p.H + h0) * kDim;
   uint32_t qa[8][4];
@@ -125,42 +195,6 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const DecodeArgs p
     qr[0] = rv.x; qr[1] = rv8.x; qr[2] = rv.y; qr[3] = rv8.y;
   }
 
-  // ---- slot bookkeeping
-  auto load_idx = [&](int tile) -> int32_t {
-    const int j = j0 + tile * kTile + tid;
-    return (tile < ntiles && j < j1) ? __ldg(idx_row + j) : -1;
-  };
-  auto issue = [&](int tile) {
-    const uint32_t st = smem_u32(stage + (tile % kStages) * kTile * RB);
-    const int64_t* ph = ring + (tile % kRing) * kTile;
-    for (int L = tid; L < kTile * CH; L += kThreads) {
-      const int row = L / CH, ch = L - row * CH;
-      const int64_t s = ph[row];
-      const uint8_t* src = s >= 0 ? p.kv + s * RB + ch * 16 : p.kv;
-      cp_async16(st + row * RB + ch * 16, src, s >= 0 ? 16 : 0);
-    }
-  };
-  auto publish = [&](int tile, int64_t phys) {  // threads 0..63
-    const int e = tile % kRing;
-    ring[e * kTile + tid] = phys;
-    const uint32_t m = __ballot_sync(0xffffffffu, phys >= 0);
-    if (lane == 0) ring_mask[e * 2 + w] = m;
-  };
-
-  if (tid < kTile) {
-#pragma unroll 1
-    for (int s = 0; s < kStages; ++s)
-      publish(s, translate_index(load_idx(s), pt_row, p.stride, p.log2_page, p.num_pages, p.err));
-  }
-  __syncthreads();
-#pragma unroll 1
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (s < ntiles) issue(s);
-    cp_async_commit();
-  }
-  int32_t idx_reg = tid < kTile ? load_idx(kStages) : -1;
-
-  // ---- running state
   float O[8][2][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
@@ -172,49 +206,48 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const DecodeArgs p
   float mo[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
   const int oh[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
   float r_w = 0.f;
+  uint32_t cb_phase = 0;  // sync points completed by the 4 consumer warps
+  bool ok = true;
+  // consumer-only barrier (bounded): every consumer warp arrives once, then all wait
+  // cbar 0..2 complete once per computed stage (parity = cb_phase & 1); cbar 3 once.
+  auto csync = [&](int k, uint32_t parity) -> bool {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cbar0 + 8 * k);
+    const bool r = mbar_wait(cbar0 + 8 * k, parity & 1);
+    __syncwarp();
+    return r;
+  };
 
-#pragma unroll 1
-  for (int i = 0; i < ntiles; ++i) {
-    __syncthreads();  // stage (i-1) free, ring entry for tile i+kStages-1 visible
-    if (i + kStages - 1 < ntiles) issue(i + kStages - 1);
-    cp_async_commit();
-    // look-ahead index translation for tile i+kStages: issue the page-table load now,
-    // use it after this tile's compute.
-    int32_t page_raw = -1;
-    int32_t idx_cur = idx_reg;
-    if (tid < kTile) {
-      if (idx_cur >= 0 && (idx_cur >> p.log2_page) < p.stride)
-        page_raw = __ldg(pt_row + (idx_cur >> p.log2_page));
-      idx_reg = load_idx(i + kStages + 1);
+  for (int i = 0; i < ntiles && ok; ++i) {
+    const int st = i % NST;
+    if (!mbar_wait(full0 + 8 * st, (i / NST) & 1)) {
+      ok = false;
+      break;
     }
-    cp_async_wait<kStages - 1>();
-    __syncthreads();
-
-    const int e_ring = i % kRing;
-    const uint32_t msk0 = ring_mask[e_ring * 2], msk1 = ring_mask[e_ring * 2 + 1];
-    if ((msk0 | msk1) != 0u) {
-      const uint32_t st = smem_u32(stage + (i % kStages) * kTile * RB);
+    const uint32_t msk = meta[st];
+    if (msk != 0u) {
+      const uint32_t sb = ring_s + st * kSlots * RB;
       // ---- QK partial over latent block w (+ RoPE quarter w)
-      float sc[8][2];
+      float sc[4][2];
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const uint32_t rb = st + (8 * nt + g) * RB;
+      for (int nt = 0; nt < 4; ++nt) {
+        const uint32_t rb = sb + (8 * nt + g) * RB;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         if (kFp8) {
           float accr[4] = {0.f, 0.f, 0.f, 0.f};
           const uint4 v0 = lds128(rb + 128 * w + 32 * c);
           const uint4 v1 = lds128(rb + 128 * w + 32 * c + 16);
           const uint32_t wd[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          const uint2 rv = lds64(rb + kRopeOffFp8 + 2 * (16 * w + 4 * c));
+          mma_bf16(accr, qr, rv.x, rv.y);
 #pragma unroll
           for (int s = 0; s < 8; ++s) {
             uint32_t b0, b1;
             e4m3x4_to_f16x4(wd[s], b0, b1);
             mma_f16(acc, qa[s], b0, b1);
           }
-          const uint2 rv = lds64(rb + kRopeOffFp8 + 2 * (16 * w + 4 * c));
-          mma_bf16(accr, qr, rv.x, rv.y);
-          sc[nt][0] = lds_f32(st + (8 * nt + 2 * c) * RB + kScaleOff + 4 * w);
-          sc[nt][1] = lds_f32(st + (8 * nt + 2 * c + 1) * RB + kScaleOff + 4 * w);
+          sc[nt][0] = lds_f32(sb + (8 * nt + 2 * c) * RB + kScaleOff + 4 * w);
+          sc[nt][1] = lds_f32(sb + (8 * nt + 2 * c + 1) * RB + kScaleOff + 4 * w);
           acc[0] = fmaf(acc[0], sc[nt][0], accr[0]);
           acc[1] = fmaf(acc[1], sc[nt][1], accr[1]);
           acc[2] = fmaf(acc[2], sc[nt][0], accr[2]);
@@ -234,33 +267,23 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const DecodeArgs p
           sc[nt][0] = 1.f;
           sc[nt][1] = 1.f;
         }
-        red[(w * 8 + nt) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        red[(w * 4 + nt) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       }
-      __syncthreads();
+      if (!(ok = csync(0, cb_phase))) break;
 
-      // ---- scores of slots [16w, 16w+16): sum partials, scale, mask, tile max
-      float s[2][4];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int nt = 2 * w + u;
-        float4 a = red[(0 * 8 + nt) * 32 + lane];
-        const float4 b = red[(1 * 8 + nt) * 32 + lane];
-        const float4 cc = red[(2 * 8 + nt) * 32 + lane];
-        const float4 d = red[(3 * 8 + nt) * 32 + lane];
-        a.x = (a.x + b.x) + (cc.x + d.x);
-        a.y = (a.y + b.y) + (cc.y + d.y);
-        a.z = (a.z + b.z) + (cc.z + d.z);
-        a.w = (a.w + b.w) + (cc.w + d.w);
-        const int sl = 16 * w + 8 * u + 2 * c;
-        const uint32_t mk = sl < 32 ? msk0 : msk1;
-        const bool v0 = (mk >> (sl & 31)) & 1u, v1 = (mk >> ((sl + 1) & 31)) & 1u;
-        s[u][0] = v0 ? a.x * p.c2 : -CUDART_INF_F;
-        s[u][1] = v1 ? a.y * p.c2 : -CUDART_INF_F;
-        s[u][2] = v0 ? a.z * p.c2 : -CUDART_INF_F;
-        s[u][3] = v1 ? a.w * p.c2 : -CUDART_INF_F;
+      // ---- scores of slots [8w, 8w+8): sum partials, scale, mask, stage max
+      float s4[4];
+      {
+        const float4 a = red[(0 * 4 + w) * 32 + lane], b = red[(1 * 4 + w) * 32 + lane];
+        const float4 cc = red[(2 * 4 + w) * 32 + lane], d = red[(3 * 4 + w) * 32 + lane];
+        const int sl = 8 * w + 2 * c;
+        const bool v0 = (msk >> sl) & 1u, v1 = (msk >> (sl + 1)) & 1u;
+        s4[0] = v0 ? ((a.x + b.x) + (cc.x + d.x)) * p.c2 : -CUDART_INF_F;
+        s4[1] = v1 ? ((a.y + b.y) + (cc.y + d.y)) * p.c2 : -CUDART_INF_F;
+        s4[2] = v0 ? ((a.z + b.z) + (cc.z + d.z)) * p.c2 : -CUDART_INF_F;
+        s4[3] = v1 ? ((a.w + b.w) + (cc.w + d.w)) * p.c2 : -CUDART_INF_F;
       }
-      float mg = fmax4(s[0][0], s[0][1], s[1][0], s[1][1]);
-      float mg8 = fmax4(s[0][2], s[0][3], s[1][2], s[1][3]);
+      float mg = fmaxf(s4[0], s4[1]), mg8 = fmaxf(s4[2], s4[3]);
       mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, 1));
       mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, 2));
       mg8 = fmaxf(mg8, __shfl_xor_sync(0xffffffffu, mg8, 1));
@@ -269,29 +292,21 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const DecodeArgs p
         mx[w * 16 + g] = mg;
         mx[w * 16 + g + 8] = mg8;
       }
-      __syncthreads();
+      if (!(ok = csync(1, cb_phase))) break;
 
-      // ---- online softmax (base 2) for the owned slots; probabilities to shared memory
+      // ---- online softmax (base 2) for the owned slots
       auto tmax = [&](int h) { return fmax4(mx[h], mx[16 + h], mx[32 + h], mx[48 + h]); };
       {
         const float ng = fmaxf(m_g, tmax(g)), ng8 = fmaxf(m_g8, tmax(g + 8));
         const float bg = ng == -CUDART_INF_F ? 0.f : ng;
         const float bg8 = ng8 == -CUDART_INF_F ? 0.f : ng8;
-        float pr[8];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          pr[4 * u + 0] = exp2f(s[u][0] - bg);
-          pr[4 * u + 1] = exp2f(s[u][1] - bg);
-          pr[4 * u + 2] = exp2f(s[u][2] - bg8);
-          pr[4 * u + 3] = exp2f(s[u][3] - bg8);
-        }
-        l_g = l_g * exp2f(m_g - bg) + ((pr[0] + pr[1]) + (pr[4] + pr[5]));
-        l_g8 = l_g8 * exp2f(m_g8 - bg8) + ((pr[2] + pr[3]) + (pr[6] + pr[7]));
+        const float p0 = exp2f(s4[0] - bg), p1 = exp2f(s4[1] - bg);
+        const float p2 = exp2f(s4[2] - bg8), p3 = exp2f(s4[3] - bg8);
+        l_g = l_g * exp2f(m_g - bg) + (p0 + p1);
+        l_g8 = l_g8 * exp2f(m_g8 - bg8) + (p2 + p3);
         m_g = ng;
         m_g8 = ng8;
-        float4* pb = reinterpret_cast<float4*>(pbuf + (w * 32 + lane) * 8);
-        pb[0] = make_float4(pr[0], pr[1], pr[2], pr[3]);
-        pb[1] = make_float4(pr[4], pr[5], pr[6], pr[7]);
+        pbuf[w * 32 + lane] = make_float4(p0, p1, p2, p3);
       }
       float alpha[4];
 #pragma unroll
@@ -300,17 +315,16 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const DecodeArgs p
         alpha[k] = exp2f(mo[k] - (n == -CUDART_INF_F ? 0.f : n));
         mo[k] = n;
       }
-      // running maximum of scale_w over the slots seen so far
-      float tm = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) tm = fmax4(tm, sc[nt][0], sc[nt][1], 0.f);
+      float tm = fmax4(sc[0][0], sc[0][1], sc[1][0], sc[1][1]);
+      tm = fmaxf(tm, fmax4(sc[2][0], sc[2][1], sc[3][0], sc[3][1]));
       tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
       tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
       const float r_new = fmaxf(r_w, tm);
       const float rr = r_new > 0.f ? r_w / r_new : 1.f;
       r_w = r_new;
       const float inv_r = r_new > 0.f ? 1.f / r_new : 0.f;
-      __syncthreads();
+      if (!(ok = csync(2, cb_phase))) break;
+      ++cb_phase;
 
       // ---- PV: O^T[128w.., heads] += V^T P^T
 #pragma unroll
@@ -321,9 +335,8 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const DecodeArgs p
           for (int e = 0; e < 4; ++e) O[mt][nt][e] *= alpha[2 * nt + (e & 1)] * rr;
 
 #pragma unroll
-      for (int kc = 0; kc < 4; ++kc) {
-        const float4* pb = reinterpret_cast<const float4*>(pbuf + (kc * 32 + lane) * 8);
-        const float4 pa = pb[0], pc = pb[1];
+      for (int kc = 0; kc < 2; ++kc) {
+        const float4 pa = pbuf[(2 * kc) * 32 + lane], pc = pbuf[(2 * kc + 1) * 32 + lane];
         const float f0 = sc[2 * kc][0] * inv_r, f1 = sc[2 * kc][1] * inv_r;
         const float f2 = sc[2 * kc + 1][0] * inv_r, f3 = sc[2 * kc + 1][1] * inv_r;
         uint32_t bh0[2], bh1[2];
@@ -338,7 +351,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const DecodeArgs p
           bh1[0] = pack_bf16x2(pa.z, pa.w);
           bh1[1] = pack_bf16x2(pc.z, pc.w);
         }
-        const uint32_t r0 = st + (16 * kc + 2 * c) * RB;
+        const uint32_t r0 = sb + (16 * kc + 2 * c) * RB;
         if (kFp8) {
           const uint32_t off = 128 * w + 16 * g;
           const uint4 X = lds128(r0 + off), Y = lds128(r0 + RB + off);
@@ -382,35 +395,27 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const DecodeArgs p
         }
       }
     }
-
-    // publish the translated slots of tile i+kStages (used two iterations from now)
-    if (tid < kTile) {
-      int64_t phys = -1;
-      if (idx_cur != -1) {
-        if (idx_cur < 0 || (idx_cur >> p.log2_page) >= p.stride) {
-          atomicOr(p.err, SMLA_DEVERR_INDEX);
-        } else if (page_raw < 0 || page_raw >= p.num_pages) {
-          atomicOr(p.err, SMLA_DEVERR_PAGE);
-        } else {
-          phys = (int64_t(page_raw) << p.log2_page) + (idx_cur & ((1 << p.log2_page) - 1));
-        }
-      }
-      publish(i + kStages, phys);
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
   }
-  cp_async_wait<0>();
+  if (!ok) {
+    if (lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
+    return;
+  }
 
   // ---- epilogue
   l_g += __shfl_xor_sync(0xffffffffu, l_g, 1);
   l_g += __shfl_xor_sync(0xffffffffu, l_g, 2);
   l_g8 += __shfl_xor_sync(0xffffffffu, l_g8, 1);
   l_g8 += __shfl_xor_sync(0xffffffffu, l_g8, 2);
-  __syncthreads();
   if (c == 0) {
     lsum[w * 16 + g] = l_g;
     lsum[w * 16 + g + 8] = l_g8;
   }
-  __syncthreads();
+  if (!csync(3, 0)) {
+    if (lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
+    return;
+  }
   const int S = p.num_splits;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -484,7 +489,6 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs p) {
     if (p.lse) p.lse[int64_t(t) * p.H + h] = lse;
   }
   __syncthreads();
-  // 16 heads x 512 dims, 4 consecutive dims per thread step
   for (int e = threadIdx.x * 4; e < 16 * kLatent; e += blockDim.x * 4) {
     const int hl = e / kLatent, d = e % kLatent;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -507,7 +511,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs p) {
 
 template <int FMT>
 cudaError_t launch_fmt(const DecodeArgs& a, cudaStream_t s) {
-  const size_t smem = smem_bytes<FMT>();
+  const size_t smem = Cfg<FMT>::kSmem;
   static int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
