@@ -164,11 +164,20 @@ def run_oracle_sample(problem, budget_s: float, min_tokens: int = 1):
     return done, el
 
 
+def workload_from_args(args) -> W.Workload:
+    w = W.BY_NAME[args.workload]
+    if args.ctx_hi:
+        w = W.small_variant(w, num_requests=args.requests or w.num_requests,
+                            ctx_lo=min(args.ctx_lo or w.ctx_lo, args.ctx_hi), ctx_hi=args.ctx_hi,
+                            topk=w.topk, tail_pad=w.tail_pad, name_suffix=f"ctx<={args.ctx_hi}")
+    return w
+
+
 def reference_arm(args):
     world, rank, _ = dist_env()
     if world > 1 and rank != 0:
         return 0
-    w = W.BY_NAME[args.workload]
+    w = workload_from_args(args)
     problem = W.make_problem(w, device="cpu")
     per_step = []
     tokens = 0
@@ -207,7 +216,7 @@ def gpu_arm(args):
     import sparse_mla_decode_smla_gb300 as smla
     from sparse_mla_decode_smla_gb300.runner import DeviceDecode
 
-    w = W.BY_NAME[args.workload]
+    w = workload_from_args(args)
     problem = W.make_problem(w, seed=W.SEED_BASE + w.seed_offset + 1000 * rank, device=dev)
     dd = DeviceDecode(problem, num_splits=args.num_splits, device=dev)
     valid, kv_bytes, flops = algorithmic_work(problem)
@@ -247,7 +256,7 @@ def gpu_arm(args):
     h_lse = torch.empty(dd.lse.shape, dtype=dd.lse.dtype).pin_memory()
     h2d = h_q.numel() * 2 + h_topk.numel() * 4 + h_pt.numel() * 4
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
-    e2e_steps = max(3, min(args.steps, 200))
+    e2e_steps = args.e2e_steps
 
     def e2e_step():
         dd.q.copy_(h_q, non_blocking=True)
@@ -257,10 +266,10 @@ def gpu_arm(args):
         h_out.copy_(dd.out, non_blocking=True)
         h_lse.copy_(dd.lse, non_blocking=True)
 
-    for _ in range(3):
+    for _ in range(3 if e2e_steps else 0):
         e2e_step()
     torch.cuda.synchronize(dev)
-    e_ms = []
+    e_ms = [float("nan")] if not e2e_steps else []
     for _ in range(e2e_steps):
         flush.fill_(0.5)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -321,6 +330,10 @@ def main(argv=None):
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=5.0)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--ctx-lo", type=int, default=0, help="smaller variant (profiling): context range low")
+    ap.add_argument("--ctx-hi", type=int, default=0, help="smaller variant (profiling): context range high")
+    ap.add_argument("--requests", type=int, default=0, help="smaller variant (profiling): requests")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the decode kernel from an ncu capture, if current")
     args = ap.parse_args(argv)

@@ -6,9 +6,10 @@
 // selected slot j, s_j = sm_scale * <q_h, k_j> over 576 dims, out_h = softmax-weighted
 // sum of v_j = k_j[0:512].
 //
-// Producer warp: walks the split's top-k list 32 slots at a time. Index loads run two
-// tiles ahead and page-table loads one tile ahead, so the dependent-load chain stays off
-// the critical path. Each valid slot's whole 656-byte row is fetched with one bulk copy
+// Producer warp: copies the split's index list into shared memory (one bulk copy), then
+// walks it 32 slots at a time. Page-table entries are fetched six stages ahead with
+// 4-byte cp.async into a shared ring, so the dependent index -> page -> row chain never
+// stalls the issue of row copies. Each valid slot's whole 656-byte row is fetched with one bulk copy
 // (cp.async.bulk, TMA engine) into a 4-stage shared-memory ring; the stage's mbarrier
 // counts the bytes. Padding and invalid entries are never fetched.
 //
@@ -19,8 +20,10 @@
 //    the k order inside an mma is permuted so each thread reads 16 contiguous bytes of a
 //    row, and q is permuted the same way. The per-128 scale multiplies the fp32 partial
 //    score of block w.
-//  * The four partial scores are summed through shared memory; warp w then owns slots
-//    [8w, 8w+8) of the stage for the masked base-2 online softmax.
+//  * The four partial scores meet in a double-buffered shared-memory array after one
+//    barrier; every warp then sums all four and runs the masked base-2 online softmax for
+//    all 32 slots (the same arithmetic in every warp, so all agree bit for bit). The
+//    probabilities are then already in the registers of the PV B fragments.
 //  * PV: O^T[dims, heads] = V^T P^T. Warp w accumulates its 128 output dims. A fragments
 //    (V^T) come from the staged bytes of four rows, paired by prmt and converted; the
 //    B fragments are p * scale_w[j] / r_w, with r_w the running maximum of scale_w over
@@ -39,21 +42,30 @@
 namespace smla {
 namespace {
 
+#ifndef SMLA_MMA_STAGES_FP8
+#define SMLA_MMA_STAGES_FP8 4
+#endif
+#ifndef SMLA_MMA_MIN_BLOCKS
+#define SMLA_MMA_MIN_BLOCKS 2
+#endif
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kSlots = 32;  // slots per stage
+constexpr int kPageAhead = 6;  // page-table entries are fetched this many stages ahead
+constexpr int kPageRing = 8;
 
 template <int FMT>
 struct Cfg {
   static constexpr bool kFp8 = FMT == SMLA_KV_FP8_DS;
   static constexpr int kRowBytes = kFp8 ? kFp8RowBytes : kBf16RowBytes;
-  static constexpr int kStages = kFp8 ? 4 : 3;
+  static constexpr int kStages = kFp8 ? SMLA_MMA_STAGES_FP8 : 3;
   static constexpr size_t kRing = size_t(kStages) * kSlots * kRowBytes;
-  static constexpr size_t kRed = 4 * 4 * 32 * 16;  // partial scores [warp][nt][lane] float4
-  static constexpr size_t kPbuf = 4 * 32 * 16;     // probabilities [nt][lane] float4
-  static constexpr size_t kSmall = 64 * 4 + 64 * 4 + 16 * 4;  // maxima, row sums, stage masks
-  static constexpr size_t kBars = (2 * kStages + 4) * 8;
-  static constexpr size_t kSmem = kRing + kRed + kPbuf + kSmall + kBars;
+  static constexpr size_t kRed = 2 * 4 * 4 * 32 * 16;  // partial scores [2][warp][nt][lane] float4
+  static constexpr size_t kSmall = 16 * 4;               // stage valid masks
+  static constexpr size_t kIdx = kMaxSplitLen * 4;       // the split's index list
+  static constexpr size_t kPages = kPageRing * kSlots * 4;  // page-table entries in flight
+  static constexpr size_t kBars = (2 * kStages + 2) * 8;
+  static constexpr size_t kSmem = kRing + kRed + kSmall + kIdx + kPages + kBars;
 };
 
 __device__ __forceinline__ float fmax4(float a, float b, float c, float d) {
@@ -61,7 +73,7 @@ __device__ __forceinline__ float fmax4(float a, float b, float c, float d) {
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeArgs p) {
+__global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kernel(const DecodeArgs p) {
   using C = Cfg<FMT>;
   constexpr bool kFp8 = C::kFp8;
   constexpr int RB = C::kRowBytes;
@@ -69,12 +81,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeArg
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   float4* red = reinterpret_cast<float4*>(smem + C::kRing);
-  float4* pbuf = reinterpret_cast<float4*>(smem + C::kRing + C::kRed);
-  float* mx = reinterpret_cast<float*>(smem + C::kRing + C::kRed + C::kPbuf);
-  float* lsum = mx + 64;
-  uint32_t* meta = reinterpret_cast<uint32_t*>(lsum + 64);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kRing + C::kRed + C::kPbuf + C::kSmall);
+  uint32_t* meta = reinterpret_cast<uint32_t*>(smem + C::kRing + C::kRed);
+  int32_t* sidx = reinterpret_cast<int32_t*>(smem + C::kRing + C::kRed + C::kSmall);
+  int32_t* spage = sidx + kMaxSplitLen;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kRing + C::kRed + C::kSmall + C::kIdx + C::kPages);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + NST), cbar0 = smem_u32(bars + 2 * NST);
+  const uint32_t idxbar = smem_u32(bars + 2 * NST + 1);
   const uint32_t ring_s = smem_u32(ring);
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, g = lane >> 2, c = lane & 3;
@@ -104,7 +116,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeArg
         mbar_init(full0 + 8 * s, 1);
         mbar_init(empty0 + 8 * s, kConsumerWarps);
       }
-      for (int k = 0; k < 4; ++k) mbar_init(cbar0 + 8 * k, kConsumerWarps);
+      mbar_init(cbar0, kConsumerWarps);
+      mbar_init(idxbar, 1);
       if (!req_ok) atomicOr(p.err, SMLA_DEVERR_INDEX);
     }
     __syncthreads();
@@ -112,22 +125,35 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeArg
 
   // =================================================================== producer warp
   if (w == kConsumerWarps) {
-    auto idx_at = [&](int tile) -> int32_t {
-      const int j = j0 + tile * kSlots + lane;
-      return (tile < ntiles && j < j1) ? __ldg(idx_row + j) : -1;
-    };
-    auto page_of = [&](int32_t idx) -> int32_t {
-      return (idx >= 0 && (idx >> p.log2_page) < p.stride) ? __ldg(pt_row + (idx >> p.log2_page)) : -1;
-    };
-    int32_t idx_a = idx_at(0), idx_b = idx_at(1);
-    int32_t pg_a = page_of(idx_a);
-    int issued = 0;
+    // the split's index list, one bulk copy (16-byte aligned: K % 4 == 0, j0 % 64 == 0)
+    const int nidx = j1 - j0;
     bool ok = true;
-    for (int i = 0; i < ntiles; ++i) {
-      const int32_t idx_c = idx_a, pg_c = pg_a;
-      idx_a = idx_b;
-      idx_b = idx_at(i + 2);
-      pg_a = page_of(idx_a);
+    if (ntiles > 0) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(idxbar, uint32_t(nidx) * 4u);
+        bulk_g2s(smem_u32(sidx), idx_row + j0, uint32_t(nidx) * 4u, idxbar);
+      }
+      ok = mbar_wait(idxbar, 0);
+    }
+    auto idx_of = [&](int tile) -> int32_t {
+      const int j = tile * kSlots + lane;
+      return (tile < ntiles && j < nidx) ? sidx[j] : -1;
+    };
+    // page-table entries travel by 4-byte cp.async into a shared ring, kPageAhead stages
+    // ahead of their use, so no lane ever waits on a dependent global load at issue time
+    auto fetch_page = [&](int tile) {
+      const int32_t idx = idx_of(tile);
+      if (idx >= 0 && (idx >> p.log2_page) < p.stride)
+        cp_async4(smem_u32(spage + (tile % kPageRing) * kSlots + lane), pt_row + (idx >> p.log2_page));
+      cp_async_commit();
+    };
+    if (ok)
+      for (int d = 0; d < kPageAhead; ++d) fetch_page(d);
+    int issued = 0;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      fetch_page(i + kPageAhead);
+      cp_async_wait<kPageAhead>();
+      const int32_t idx_c = idx_of(i);
       const int st = i % NST;
       if (!mbar_wait(empty0 + 8 * st, ((i / NST) & 1) ^ 1)) {
         ok = false;
@@ -137,10 +163,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeArg
       if (idx_c != -1) {
         if (idx_c < 0 || (idx_c >> p.log2_page) >= p.stride) {
           atomicOr(p.err, SMLA_DEVERR_INDEX);
-        } else if (pg_c < 0 || pg_c >= p.num_pages) {
-          atomicOr(p.err, SMLA_DEVERR_PAGE);
         } else {
-          phys = (int64_t(pg_c) << p.log2_page) + (idx_c & ((1 << p.log2_page) - 1));
+          const int32_t pg = spage[(i % kPageRing) * kSlots + lane];
+          if (pg < 0 || pg >= p.num_pages)
+            atomicOr(p.err, SMLA_DEVERR_PAGE);
+          else
+            phys = (int64_t(pg) << p.log2_page) + (idx_c & ((1 << p.log2_page) - 1));
         }
       }
       const uint32_t vmask = __ballot_sync(0xffffffffu, phys >= 0);
@@ -153,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeArg
         bulk_g2s(ring_s + (st * kSlots + lane) * RB, p.kv + phys * RB, RB, full0 + 8 * st);
       issued = i + 1;
     }
+    cp_async_wait<0>();
     if (!ok && lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
     // never leave while copies into this CTA's shared memory are in flight
     for (int i = max(0, issued - NST); i < issued; ++i)
@@ -202,14 +231,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeArg
     for (int j = 0; j < 2; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) O[i][j][e] = 0.f;
+  // running max (base-2 logits) and row sum of heads g and g+8; every consumer warp
+  // computes the same values for the whole stage, so no exchange is needed.
   float m_g = -CUDART_INF_F, m_g8 = -CUDART_INF_F, l_g = 0.f, l_g8 = 0.f;
-  float mo[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
-  const int oh[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
   float r_w = 0.f;
-  uint32_t cb_phase = 0;  // sync points completed by the 4 consumer warps
+  uint32_t n_done = 0;  // stages computed (cbar parity and partial-score buffer index)
   bool ok = true;
-  // consumer-only barrier (bounded): every consumer warp arrives once, then all wait
-  // cbar 0..2 complete once per computed stage (parity = cb_phase & 1); cbar 3 once.
+  // consumer-only barrier (bounded): each consumer warp arrives once, then all wait
   auto csync = [&](int k, uint32_t parity) -> bool {
     __syncwarp();
     if (lane == 0) mbar_arrive(cbar0 + 8 * k);
@@ -227,32 +255,51 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeArg
     const uint32_t msk = meta[st];
     if (msk != 0u) {
       const uint32_t sb = ring_s + st * kSlots * RB;
-      // ---- QK partial over latent block w (+ RoPE quarter w)
+      float4* rd = red + (n_done & 1) * (4 * 4 * 32);
+      // ---- QK partial over latent block w (+ RoPE quarter w) for the 32 slots.
+      // The four slot groups are independent accumulation chains; interleaving them
+      // (k step outer) keeps four mma.sync in flight instead of one.
       float sc[4][2];
+      float acc[4][4];
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const uint32_t rb = sb + (8 * nt + g) * RB;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (kFp8) {
-          float accr[4] = {0.f, 0.f, 0.f, 0.f};
-          const uint4 v0 = lds128(rb + 128 * w + 32 * c);
-          const uint4 v1 = lds128(rb + 128 * w + 32 * c + 16);
-          const uint32_t wd[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-          const uint2 rv = lds64(rb + kRopeOffFp8 + 2 * (16 * w + 4 * c));
-          mma_bf16(accr, qr, rv.x, rv.y);
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-          for (int s = 0; s < 8; ++s) {
-            uint32_t b0, b1;
-            e4m3x4_to_f16x4(wd[s], b0, b1);
-            mma_f16(acc, qa[s], b0, b1);
-          }
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+      if (kFp8) {
+        uint32_t wd[4][8];
+        float accr[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          const uint32_t rb = sb + (8 * nt + g) * RB + 128 * w + 32 * c;
+          const uint4 v0 = lds128(rb), v1 = lds128(rb + 16);
+          wd[nt][0] = v0.x; wd[nt][1] = v0.y; wd[nt][2] = v0.z; wd[nt][3] = v0.w;
+          wd[nt][4] = v1.x; wd[nt][5] = v1.y; wd[nt][6] = v1.z; wd[nt][7] = v1.w;
+          const uint2 rv = lds64(sb + (8 * nt + g) * RB + kRopeOffFp8 + 2 * (16 * w + 4 * c));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) accr[nt][e] = 0.f;
+          mma_bf16(accr[nt], qr, rv.x, rv.y);
           sc[nt][0] = lds_f32(sb + (8 * nt + 2 * c) * RB + kScaleOff + 4 * w);
           sc[nt][1] = lds_f32(sb + (8 * nt + 2 * c + 1) * RB + kScaleOff + 4 * w);
-          acc[0] = fmaf(acc[0], sc[nt][0], accr[0]);
-          acc[1] = fmaf(acc[1], sc[nt][1], accr[1]);
-          acc[2] = fmaf(acc[2], sc[nt][0], accr[2]);
-          acc[3] = fmaf(acc[3], sc[nt][1], accr[3]);
-        } else {
+        }
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt) {
+            uint32_t b0, b1;
+            e4m3x4_to_f16x4(wd[nt][s], b0, b1);
+            mma_f16(acc[nt], qa[s], b0, b1);
+          }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          acc[nt][0] = fmaf(acc[nt][0], sc[nt][0], accr[nt][0]);
+          acc[nt][1] = fmaf(acc[nt][1], sc[nt][1], accr[nt][1]);
+          acc[nt][2] = fmaf(acc[nt][2], sc[nt][0], accr[nt][2]);
+          acc[nt][3] = fmaf(acc[nt][3], sc[nt][1], accr[nt][3]);
+        }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          const uint32_t rb = sb + (8 * nt + g) * RB;
           const uint32_t base = rb + 2 * (128 * w + 32 * c);
           uint32_t wd[16];
 #pragma unroll
@@ -261,60 +308,66 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeArg
             wd[4 * k] = v.x; wd[4 * k + 1] = v.y; wd[4 * k + 2] = v.z; wd[4 * k + 3] = v.w;
           }
 #pragma unroll
-          for (int s = 0; s < 8; ++s) mma_bf16(acc, qa[s], wd[2 * s], wd[2 * s + 1]);
+          for (int s = 0; s < 8; ++s) mma_bf16(acc[nt], qa[s], wd[2 * s], wd[2 * s + 1]);
           const uint2 rv = lds64(rb + 2 * kLatent + 2 * (16 * w + 4 * c));
-          mma_bf16(acc, qr, rv.x, rv.y);
+          mma_bf16(acc[nt], qr, rv.x, rv.y);
           sc[nt][0] = 1.f;
           sc[nt][1] = 1.f;
         }
-        red[(w * 4 + nt) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       }
-      if (!(ok = csync(0, cb_phase))) break;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+        rd[(w * 4 + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+      if (!(ok = csync(0, n_done))) break;
 
-      // ---- scores of slots [8w, 8w+8): sum partials, scale, mask, stage max
-      float s4[4];
-      {
-        const float4 a = red[(0 * 4 + w) * 32 + lane], b = red[(1 * 4 + w) * 32 + lane];
-        const float4 cc = red[(2 * 4 + w) * 32 + lane], d = red[(3 * 4 + w) * 32 + lane];
-        const int sl = 8 * w + 2 * c;
+      // ---- full scores of heads g, g+8 for all 32 slots (slot 8nt + 2c + {0,1})
+      float sp[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const float4 a = rd[(0 * 4 + nt) * 32 + lane], b = rd[(1 * 4 + nt) * 32 + lane];
+        const float4 cc = rd[(2 * 4 + nt) * 32 + lane], d = rd[(3 * 4 + nt) * 32 + lane];
+        const int sl = 8 * nt + 2 * c;
         const bool v0 = (msk >> sl) & 1u, v1 = (msk >> (sl + 1)) & 1u;
-        s4[0] = v0 ? ((a.x + b.x) + (cc.x + d.x)) * p.c2 : -CUDART_INF_F;
-        s4[1] = v1 ? ((a.y + b.y) + (cc.y + d.y)) * p.c2 : -CUDART_INF_F;
-        s4[2] = v0 ? ((a.z + b.z) + (cc.z + d.z)) * p.c2 : -CUDART_INF_F;
-        s4[3] = v1 ? ((a.w + b.w) + (cc.w + d.w)) * p.c2 : -CUDART_INF_F;
+        sp[nt][0] = v0 ? ((a.x + b.x) + (cc.x + d.x)) * p.c2 : -CUDART_INF_F;
+        sp[nt][1] = v1 ? ((a.y + b.y) + (cc.y + d.y)) * p.c2 : -CUDART_INF_F;
+        sp[nt][2] = v0 ? ((a.z + b.z) + (cc.z + d.z)) * p.c2 : -CUDART_INF_F;
+        sp[nt][3] = v1 ? ((a.w + b.w) + (cc.w + d.w)) * p.c2 : -CUDART_INF_F;
       }
-      float mg = fmaxf(s4[0], s4[1]), mg8 = fmaxf(s4[2], s4[3]);
+      float mg = fmax4(sp[0][0], sp[0][1], sp[1][0], sp[1][1]);
+      mg = fmaxf(mg, fmax4(sp[2][0], sp[2][1], sp[3][0], sp[3][1]));
+      float mg8 = fmax4(sp[0][2], sp[0][3], sp[1][2], sp[1][3]);
+      mg8 = fmaxf(mg8, fmax4(sp[2][2], sp[2][3], sp[3][2], sp[3][3]));
       mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, 1));
       mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, 2));
       mg8 = fmaxf(mg8, __shfl_xor_sync(0xffffffffu, mg8, 1));
       mg8 = fmaxf(mg8, __shfl_xor_sync(0xffffffffu, mg8, 2));
-      if (c == 0) {
-        mx[w * 16 + g] = mg;
-        mx[w * 16 + g + 8] = mg8;
-      }
-      if (!(ok = csync(1, cb_phase))) break;
-
-      // ---- online softmax (base 2) for the owned slots
-      auto tmax = [&](int h) { return fmax4(mx[h], mx[16 + h], mx[32 + h], mx[48 + h]); };
-      {
-        const float ng = fmaxf(m_g, tmax(g)), ng8 = fmaxf(m_g8, tmax(g + 8));
-        const float bg = ng == -CUDART_INF_F ? 0.f : ng;
-        const float bg8 = ng8 == -CUDART_INF_F ? 0.f : ng8;
-        const float p0 = exp2f(s4[0] - bg), p1 = exp2f(s4[1] - bg);
-        const float p2 = exp2f(s4[2] - bg8), p3 = exp2f(s4[3] - bg8);
-        l_g = l_g * exp2f(m_g - bg) + (p0 + p1);
-        l_g8 = l_g8 * exp2f(m_g8 - bg8) + (p2 + p3);
-        m_g = ng;
-        m_g8 = ng8;
-        pbuf[w * 32 + lane] = make_float4(p0, p1, p2, p3);
-      }
-      float alpha[4];
+      // ---- online softmax (base 2)
+      const float ng = fmaxf(m_g, mg), ng8 = fmaxf(m_g8, mg8);
+      const float bg = ng == -CUDART_INF_F ? 0.f : ng;
+      const float bg8 = ng8 == -CUDART_INF_F ? 0.f : ng8;
+      const float ag = exp2f(m_g - bg), ag8 = exp2f(m_g8 - bg8);
+      float sum_g = 0.f, sum_g8 = 0.f;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float n = fmaxf(mo[k], tmax(oh[k]));
-        alpha[k] = exp2f(mo[k] - (n == -CUDART_INF_F ? 0.f : n));
-        mo[k] = n;
+      for (int nt = 0; nt < 4; ++nt) {
+        sp[nt][0] = exp2f(sp[nt][0] - bg);
+        sp[nt][1] = exp2f(sp[nt][1] - bg);
+        sp[nt][2] = exp2f(sp[nt][2] - bg8);
+        sp[nt][3] = exp2f(sp[nt][3] - bg8);
+        sum_g += sp[nt][0] + sp[nt][1];
+        sum_g8 += sp[nt][2] + sp[nt][3];
       }
+      sum_g += __shfl_xor_sync(0xffffffffu, sum_g, 1);
+      sum_g += __shfl_xor_sync(0xffffffffu, sum_g, 2);
+      sum_g8 += __shfl_xor_sync(0xffffffffu, sum_g8, 1);
+      sum_g8 += __shfl_xor_sync(0xffffffffu, sum_g8, 2);
+      l_g = l_g * ag + sum_g;
+      l_g8 = l_g8 * ag8 + sum_g8;
+      m_g = ng;
+      m_g8 = ng8;
+      // rescale factors of the O columns this thread holds (heads 2c, 2c+1, 2c+8, 2c+9),
+      // computed by the lanes that own those heads' rows
+      const float alpha[4] = {__shfl_sync(0xffffffffu, ag, 8 * c), __shfl_sync(0xffffffffu, ag, 8 * c + 4),
+                              __shfl_sync(0xffffffffu, ag8, 8 * c), __shfl_sync(0xffffffffu, ag8, 8 * c + 4)};
       float tm = fmax4(sc[0][0], sc[0][1], sc[1][0], sc[1][1]);
       tm = fmaxf(tm, fmax4(sc[2][0], sc[2][1], sc[3][0], sc[3][1]));
       tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
@@ -323,33 +376,36 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeArg
       const float rr = r_new > 0.f ? r_w / r_new : 1.f;
       r_w = r_new;
       const float inv_r = r_new > 0.f ? 1.f / r_new : 0.f;
-      if (!(ok = csync(2, cb_phase))) break;
-      ++cb_phase;
 
       // ---- PV: O^T[128w.., heads] += V^T P^T
+      // rescale only when some running maximum moved (rare after the first stages)
+      const bool same = alpha[0] == 1.f && alpha[1] == 1.f && alpha[2] == 1.f && alpha[3] == 1.f && rr == 1.f;
+      if (!__all_sync(0xffffffffu, same)) {
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
+        for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+          for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) O[mt][nt][e] *= alpha[2 * nt + (e & 1)] * rr;
+            for (int e = 0; e < 4; ++e) O[mt][nt][e] *= alpha[2 * nt + (e & 1)] * rr;
+      }
 
 #pragma unroll
       for (int kc = 0; kc < 2; ++kc) {
-        const float4 pa = pbuf[(2 * kc) * 32 + lane], pc = pbuf[(2 * kc + 1) * 32 + lane];
         const float f0 = sc[2 * kc][0] * inv_r, f1 = sc[2 * kc][1] * inv_r;
         const float f2 = sc[2 * kc + 1][0] * inv_r, f3 = sc[2 * kc + 1][1] * inv_r;
+        const float* pa = sp[2 * kc];
+        const float* pc = sp[2 * kc + 1];
         uint32_t bh0[2], bh1[2];
         if (kFp8) {
-          bh0[0] = pack_f16x2(pa.x * f0, pa.y * f1);
-          bh0[1] = pack_f16x2(pc.x * f2, pc.y * f3);
-          bh1[0] = pack_f16x2(pa.z * f0, pa.w * f1);
-          bh1[1] = pack_f16x2(pc.z * f2, pc.w * f3);
+          bh0[0] = pack_f16x2(pa[0] * f0, pa[1] * f1);
+          bh0[1] = pack_f16x2(pc[0] * f2, pc[1] * f3);
+          bh1[0] = pack_f16x2(pa[2] * f0, pa[3] * f1);
+          bh1[1] = pack_f16x2(pc[2] * f2, pc[3] * f3);
         } else {
-          bh0[0] = pack_bf16x2(pa.x, pa.y);
-          bh0[1] = pack_bf16x2(pc.x, pc.y);
-          bh1[0] = pack_bf16x2(pa.z, pa.w);
-          bh1[1] = pack_bf16x2(pc.z, pc.w);
+          bh0[0] = pack_bf16x2(pa[0], pa[1]);
+          bh0[1] = pack_bf16x2(pc[0], pc[1]);
+          bh1[0] = pack_bf16x2(pa[2], pa[3]);
+          bh1[1] = pack_bf16x2(pc[2], pc[3]);
         }
         const uint32_t r0 = sb + (16 * kc + 2 * c) * RB;
         if (kFp8) {
@@ -394,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeArg
           }
         }
       }
+      ++n_done;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * st);
@@ -403,25 +460,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(const DecodeArg
     return;
   }
 
-  // ---- epilogue
-  l_g += __shfl_xor_sync(0xffffffffu, l_g, 1);
-  l_g += __shfl_xor_sync(0xffffffffu, l_g, 2);
-  l_g8 += __shfl_xor_sync(0xffffffffu, l_g8, 1);
-  l_g8 += __shfl_xor_sync(0xffffffffu, l_g8, 2);
-  if (c == 0) {
-    lsum[w * 16 + g] = l_g;
-    lsum[w * 16 + g + 8] = l_g8;
-  }
-  if (!csync(3, 0)) {
-    if (lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
-    return;
-  }
+  // ---- epilogue: row sums and maxima of this thread's O columns come from their owners
+  const float Lh[4] = {__shfl_sync(0xffffffffu, l_g, 8 * c), __shfl_sync(0xffffffffu, l_g, 8 * c + 4),
+                       __shfl_sync(0xffffffffu, l_g8, 8 * c), __shfl_sync(0xffffffffu, l_g8, 8 * c + 4)};
+  const float Mh[4] = {__shfl_sync(0xffffffffu, m_g, 8 * c), __shfl_sync(0xffffffffu, m_g, 8 * c + 4),
+                       __shfl_sync(0xffffffffu, m_g8, 8 * c), __shfl_sync(0xffffffffu, m_g8, 8 * c + 4)};
   const int S = p.num_splits;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int h = oh[k];
-    const float L = (lsum[h] + lsum[16 + h]) + (lsum[32 + h] + lsum[48 + h]);
-    const float lse0 = L > 0.f ? (mo[k] + log2f(L)) * kLn2 : -CUDART_INF_F;
+    const int h = (k >> 1) * 8 + 2 * c + (k & 1);
+    const float L = Lh[k];
+    const float lse0 = L > 0.f ? (Mh[k] + log2f(L)) * kLn2 : -CUDART_INF_F;
     float f = L > 0.f ? r_w / L : 0.f;
     float lse_out = lse0;
     if (S == 1 && p.sink) {

@@ -9,7 +9,8 @@
 namespace smla {
 
 constexpr int kMaxSplits = 64;
-constexpr int kTile = 64;  // top-k slots per pipeline tile of the decode kernels
+constexpr int kTile = 64;       // split lengths are multiples of this
+constexpr int kMaxSplitLen = 2048;  // index entries of one split staged in shared memory
 
 struct DecodeArgs {
   const void* q;

@@ -59,6 +59,7 @@ smla_status check_desc(const smla_desc* d) {
   if (d->kv_format != SMLA_KV_BF16 && d->kv_format != SMLA_KV_FP8_DS) return SMLA_ERR_UNSUPPORTED;
   if (!isfinite(d->sm_scale)) return SMLA_ERR_SHAPE;
   if (d->num_splits < 0 || d->num_splits > smla::kMaxSplits) return SMLA_ERR_SHAPE;
+  if (d->topk > smla::kMaxSplits * smla::kMaxSplitLen) return SMLA_ERR_SHAPE;
   for (int i = 0; i < 4; ++i)
     if (d->reserved[i] != 0) return SMLA_ERR_SHAPE;
   return SMLA_OK;
@@ -79,6 +80,8 @@ Plan make_plan(const smla_desc* d, int num_sms) {
     const int cap = d->topk / 256 > 1 ? d->topk / 256 : 1;  // at least 256 slots per split
     if (S > cap) S = cap;
   }
+  const int min_splits = (d->topk + smla::kMaxSplitLen - 1) / smla::kMaxSplitLen;
+  if (S < min_splits) S = min_splits;
   if (S > smla::kMaxSplits) S = smla::kMaxSplits;
   int len = (d->topk + S - 1) / S;
   len = (len + smla::kTile - 1) / smla::kTile * smla::kTile;
