@@ -6,12 +6,14 @@
 // selected slot j, s_j = sm_scale * <q_h, k_j> over 576 dims, out_h = softmax-weighted
 // sum of v_j = k_j[0:512].
 //
-// Producer warp: copies the split's index list into shared memory (one bulk copy), then
-// walks it 32 slots at a time. Page-table entries are fetched six stages ahead with
-// 4-byte cp.async into a shared ring, so the dependent index -> page -> row chain never
-// stalls the issue of row copies. Each valid slot's whole 656-byte row is fetched with one bulk copy
-// (cp.async.bulk, TMA engine) into a 4-stage shared-memory ring; the stage's mbarrier
-// counts the bytes. Padding and invalid entries are never fetched.
+// Producer warps (two): the split's index list is copied into shared memory (one bulk
+// copy), then walked 32 slots at a time, each producer warp taking 16 slots of a stage.
+// Page-table entries are fetched six stages ahead with 4-byte cp.async into a shared
+// ring, so the dependent index -> page -> row chain never stalls the issue of row copies.
+// Each valid slot's whole 656-byte row is one bulk copy (cp.async.bulk) into a 4-stage
+// shared-memory ring; the stage's mbarrier counts the bytes. Bulk copies issued by one
+// warp serialise on the TMA engine, so the copies of a stage come from two warps.
+// Padding and invalid entries are never fetched.
 //
 // Consumer warps (warp w owns latent block w = dims [128w, 128w+128)):
 //  * QK: warp w multiplies its 128 latent dims (+ RoPE dims [16w, 16w+16)) for the 32
@@ -49,7 +51,10 @@ namespace {
 #define SMLA_MMA_MIN_BLOCKS 2
 #endif
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
+// Two producer warps, each issuing the bulk copies of half of every stage: bulk copies
+// from a single warp serialise (about 14 GB/s per SM), several issuing warps do not.
+constexpr int kProducerWarps = 2;
+constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
 constexpr int kSlots = 32;  // slots per stage
 constexpr int kPageAhead = 6;  // page-table entries are fetched this many stages ahead
 constexpr int kPageRing = 8;
@@ -81,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   float4* red = reinterpret_cast<float4*>(smem + C::kRing);
-  uint32_t* meta = reinterpret_cast<uint32_t*>(smem + C::kRing + C::kRed);
+  uint16_t* meta = reinterpret_cast<uint16_t*>(smem + C::kRing + C::kRed);  // [stage][producer]
   int32_t* sidx = reinterpret_cast<int32_t*>(smem + C::kRing + C::kRed + C::kSmall);
   int32_t* spage = sidx + kMaxSplitLen;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kRing + C::kRed + C::kSmall + C::kIdx + C::kPages);
@@ -113,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
     fence_proxy_async_smem();
     if (tid == 0) {
       for (int s = 0; s < NST; ++s) {
-        mbar_init(full0 + 8 * s, 1);
+        mbar_init(full0 + 8 * s, kProducerWarps);  // one expect_tx arrival per producer warp
         mbar_init(empty0 + 8 * s, kConsumerWarps);
       }
       mbar_init(cbar0, kConsumerWarps);
@@ -124,27 +129,30 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
   }
 
   // =================================================================== producer warp
-  if (w == kConsumerWarps) {
+  if (w >= kConsumerWarps) {
+    const int pw = w - kConsumerWarps;          // producer warp: slots [16 pw, 16 pw + 16)
+    const bool act = lane < kSlots / kProducerWarps;
+    const int myslot = (kSlots / kProducerWarps) * pw + lane;
     // the split's index list, one bulk copy (16-byte aligned: K % 4 == 0, j0 % 64 == 0)
     const int nidx = j1 - j0;
     bool ok = true;
     if (ntiles > 0) {
-      if (lane == 0) {
+      if (pw == 0 && lane == 0) {
         mbar_arrive_expect_tx(idxbar, uint32_t(nidx) * 4u);
         bulk_g2s(smem_u32(sidx), idx_row + j0, uint32_t(nidx) * 4u, idxbar);
       }
       ok = mbar_wait(idxbar, 0);
     }
     auto idx_of = [&](int tile) -> int32_t {
-      const int j = tile * kSlots + lane;
-      return (tile < ntiles && j < nidx) ? sidx[j] : -1;
+      const int j = tile * kSlots + myslot;
+      return (act && tile < ntiles && j < nidx) ? sidx[j] : -1;
     };
     // page-table entries travel by 4-byte cp.async into a shared ring, kPageAhead stages
     // ahead of their use, so no lane ever waits on a dependent global load at issue time
     auto fetch_page = [&](int tile) {
       const int32_t idx = idx_of(tile);
       if (idx >= 0 && (idx >> p.log2_page) < p.stride)
-        cp_async4(smem_u32(spage + (tile % kPageRing) * kSlots + lane), pt_row + (idx >> p.log2_page));
+        cp_async4(smem_u32(spage + (tile % kPageRing) * kSlots + myslot), pt_row + (idx >> p.log2_page));
       cp_async_commit();
     };
     if (ok)
@@ -164,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
         if (idx_c < 0 || (idx_c >> p.log2_page) >= p.stride) {
           atomicOr(p.err, SMLA_DEVERR_INDEX);
         } else {
-          const int32_t pg = spage[(i % kPageRing) * kSlots + lane];
+          const int32_t pg = spage[(i % kPageRing) * kSlots + myslot];
           if (pg < 0 || pg >= p.num_pages)
             atomicOr(p.err, SMLA_DEVERR_PAGE);
           else
@@ -173,12 +181,12 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
       }
       const uint32_t vmask = __ballot_sync(0xffffffffu, phys >= 0);
       if (lane == 0) {
-        meta[st] = vmask;
+        meta[2 * st + pw] = uint16_t(vmask);
         mbar_arrive_expect_tx(full0 + 8 * st, uint32_t(__popc(vmask)) * RB);
       }
       __syncwarp();
       if (phys >= 0)
-        bulk_g2s(ring_s + (st * kSlots + lane) * RB, p.kv + phys * RB, RB, full0 + 8 * st);
+        bulk_g2s(ring_s + (st * kSlots + myslot) * RB, p.kv + phys * RB, RB, full0 + 8 * st);
       issued = i + 1;
     }
     cp_async_wait<0>();
@@ -252,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
       ok = false;
       break;
     }
-    const uint32_t msk = meta[st];
+    const uint32_t msk = uint32_t(meta[2 * st]) | (uint32_t(meta[2 * st + 1]) << 16);
     if (msk != 0u) {
       const uint32_t sb = ring_s + st * kSlots * RB;
       float4* rd = red + (n_done & 1) * (4 * 4 * 32);

@@ -71,12 +71,22 @@ struct Plan {
   size_t lse_off, o_off, bytes;
 };
 
+bool use_tc(const smla_desc* d) {
+  return d->kv_format == SMLA_KV_FP8_DS && d->num_heads >= smla::kTcMinHeads;
+}
+
 Plan make_plan(const smla_desc* d, int num_sms) {
-  const int units = d->num_tokens * (d->num_heads / 16);
   int S = d->num_splits;
   if (S == 0) {
     S = 1;
-    if (units < num_sms) S = (2 * num_sms + units - 1) / units;
+    if (use_tc(d)) {
+      // one CTA pair per (token, split), one pair per two SMs: fill one wave at most
+      const int pairs = num_sms / 2;
+      if (d->num_tokens < pairs) S = pairs / d->num_tokens;
+    } else {
+      const int units = d->num_tokens * (d->num_heads / 16);
+      if (units < num_sms) S = (2 * num_sms + units - 1) / units;
+    }
     const int cap = d->topk / 256 > 1 ? d->topk / 256 : 1;  // at least 256 slots per split
     if (S > cap) S = cap;
   }
@@ -195,7 +205,8 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
   a.num_splits = plan.num_splits;
   a.split_len = plan.split_len;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (smla::launch_decode_mma(a, sms, s) != cudaSuccess) return SMLA_ERR_CUDA;
+  const cudaError_t e = use_tc(d) ? smla::launch_decode_tc(a, s) : smla::launch_decode_mma(a, sms, s);
+  if (e != cudaSuccess) return SMLA_ERR_CUDA;
   if (plan.num_splits > 1 && smla::launch_merge(a, s) != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;
 }
