@@ -46,8 +46,35 @@ def measured_peaks() -> dict:
         with open(path) as f:
             d = json.load(f)
         return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", 0.0)) or None,
                 "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the decode
+# kernel, from one ncu capture of this bench's own command on the named workload, with
+# the SHA-256 of the kernel sources at capture time. A capture of an older kernel (the
+# hash differs) is not reported.
+TRAFFIC = {
+}
+KERNEL_SOURCES = ("common.cuh", "kernels.h", "tcgen05.cuh", "decode_tc.cu", "decode_mma.cu")
+
+
+def kernel_sources_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "sparse_mla_decode_smla_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    rec = TRAFFIC.get((workload, kernel))
+    if rec is None or rec[1] != kernel_sources_sha():
+        return None
+    return rec[0]
 
 
 def algorithmic_work(problem) -> tuple[int, int, int]:
@@ -229,22 +256,33 @@ def gpu_arm(args):
         dd.run()
     torch.cuda.synchronize(dev)
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    def events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:  # create the CUDA events now, so the library can record into them
+            e.record(stream)
+        return evs
+
+    starts, ends = events(args.steps), events(args.steps)
+    # the decode kernel alone (the split merge, when there is one, follows it)
+    k_starts, k_ends = events(args.steps), events(args.steps)
+    torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize(dev)
         wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(float(i))
+            smla.set_kernel_events(k_starts[i], k_ends[i])
             starts[i].record(stream)
             dd.run()
             ends[i].record(stream)
+        smla.set_kernel_events()
         torch.cuda.synchronize(dev)
         barrier(world)
         wall = time.perf_counter() - wall0
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(step_ms) / len(step_ms)
+    kernel_ms = sum(s.elapsed_time(e) for s, e in zip(k_starts, k_ends)) / args.steps
     ms_max = reduce_max(ms, world, dev)
     value = world * w.num_tokens / (ms_max * 1e-3)
 
@@ -285,8 +323,11 @@ def gpu_arm(args):
             torch.distributed.destroy_process_group()
         return 0
     peaks = measured_peaks()
-    rl = roofline(kv_bytes, flops, ms * 1e-3, peaks)
-    rl["traffic"] = args.traffic
+    rl = roofline(kv_bytes, flops, kernel_ms * 1e-3, peaks)
+    rl["kernel"] = dd.kernel_name
+    rl["kernel_ms"] = kernel_ms
+    rl["traffic"] = args.traffic if args.traffic is not None else recorded_traffic(w.name, dd.kernel_name)
+    step_rl = roofline(kv_bytes, flops, ms * 1e-3, peaks)
     line = {
         "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
@@ -299,8 +340,10 @@ def gpu_arm(args):
                    "l2": "flushed between timed steps (512 MiB write, outside the events)",
                    "num_splits": args.num_splits or "auto", "parallelism": f"replicas x{world}"},
         "roofline": rl,
-        "roofline_sustained_frac": (rl["achieved"] / 1722.2 if rl["bound"] == "tensor" and
-                                    peaks["source"] == "measured" else None),
+        "roofline_step_frac": step_rl["frac"],
+        "roofline_sustained_frac": (rl["achieved"] / peaks["bf16_tflops_sustained"]
+                                    if rl["bound"] == "tensor" and peaks.get("bf16_tflops_sustained")
+                                    else None),
         "algorithmic": {"kv_bytes": kv_bytes, "flops": flops},
         "e2e": {"value": world * w.num_tokens / (e2e_ms * 1e-3), "unit": "query-tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

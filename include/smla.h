@@ -124,6 +124,20 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
                         float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Measurement hook (the pages' interface has none): time the main decode kernel on its
+ * own, apart from the split merge that may follow it.
+ *   start, stop  cudaEvent_t handles (passed as void*) created and destroyed by the
+ *                caller; both NULL turns recording off, exactly one NULL is
+ *                SMLA_ERR_NULL.
+ * While set, every smla_decode / smla_decode_noalloc call made from this host thread
+ * records `start` on its stream just before the decode kernel is launched and `stop`
+ * just after it (before the merge kernel, when there is one). The setting belongs to
+ * the calling host thread only. Recording failures make the decode call return
+ * SMLA_ERR_CUDA.
+ */
+smla_status smla_set_kernel_events(void* start, void* stop);
+
+/*
  * Write cache rows (the quantise-on-write store of the compressor, vLLM PR #43827
  * "实现拆解 4"): for each i < n with slot_mapping[i] >= 0, row slot_mapping[i] of
  * kv_cache receives latent[i] (512 bf16) and rope[i] (64 bf16).

@@ -23,7 +23,8 @@ STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_NULL", 2: "SMLA_ERR_SHAPE", 3: "SMLA_ERR_AL
           4: "SMLA_ERR_UNSUPPORTED", 5: "SMLA_ERR_WORKSPACE", 6: "SMLA_ERR_CUDA",
           7: "SMLA_ERR_INDEX_RANGE", 8: "SMLA_ERR_DEVICE"}
 EXPORTS = ["smla_status_string", "smla_abi_version", "smla_workspace_size", "smla_decode",
-           "smla_pack_kv", "smla_gather_dequant", "smla_read_error", "smla_decode_noalloc"]
+           "smla_pack_kv", "smla_gather_dequant", "smla_read_error", "smla_decode_noalloc",
+           "smla_set_kernel_events"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -68,6 +69,8 @@ def lib() -> ctypes.CDLL:
         L.smla_gather_dequant.argtypes = [D, P, P, P, P, P, P, P]
         L.smla_decode_noalloc.restype = I32
         L.smla_decode_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P]
+        L.smla_set_kernel_events.restype = I32
+        L.smla_set_kernel_events.argtypes = [P, P]
         L.smla_read_error.restype = I32
         L.smla_read_error.argtypes = [D, P, SZ, ctypes.POINTER(I32), P]
         _lib = L
@@ -129,6 +132,19 @@ def decode_noalloc(desc, q, kv_cache, page_table, topk, req_id_per_token, sink, 
     _check("smla_decode_noalloc", lib().smla_decode_noalloc(
         ctypes.byref(desc), _ptr(q), _ptr(kv_cache), _ptr(page_table), _ptr(topk),
         _ptr(req_id_per_token), _ptr(sink), _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def set_kernel_events(start=None, stop=None):
+    """Record `start` / `stop` (torch.cuda.Event, already created) around the decode kernel
+    of every later decode call from this thread; no arguments turns recording off."""
+    def handle(ev):
+        if ev is None:
+            return None
+        h = int(ev.cuda_event)
+        if h == 0:
+            raise ValueError("the event has not been created yet: record it once first")
+        return ctypes.c_void_p(h)
+    _check("smla_set_kernel_events", lib().smla_set_kernel_events(handle(start), handle(stop)))
 
 
 def pack_kv(kv_format, scale_mode, latent, rope, slot_mapping, kv_cache, num_slots, stream=None):

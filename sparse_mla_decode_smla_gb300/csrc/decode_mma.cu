@@ -516,54 +516,61 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
 
 // Merge of split partials by log-sum-exp, then the sink (SGLang PR #24692 "关键文件":
 // _merge_partial_attn, _apply_attn_sink). One CTA per (token, 16 heads).
-__global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs p) {
-  __shared__ float wts[16][kMaxSplits];
-  __shared__ float fac[16];
-  const int HG = p.H >> 4;
-  const int t = blockIdx.x / HG, h0 = (blockIdx.x % HG) * 16;
+// Split merge: one warp per (token, head). Lane s (and s + 32) reads lse_s; the warp
+// reduces M = max_s lse_s and W = sum_s e^{lse_s - M}; then every lane accumulates 16 of
+// the 512 output dims over the splits with four coalesced 16-byte loads per split.
+constexpr int kMergeWarps = 8;
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const DecodeArgs p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);  // t * H + h
+  if (row >= int64_t(p.T) * p.H) return;
+  const int t = int(row / p.H), h = int(row % p.H);
   const int S = p.num_splits;
-  if (threadIdx.x < 16) {
-    const int h = h0 + threadIdx.x;
-    const float* lp = p.lse_part + int64_t(t) * S * p.H + h;
-    float M = -CUDART_INF_F;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, lp[int64_t(s) * p.H]);
-    float W = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float x = lp[int64_t(s) * p.H];
-      const float wt = (M == -CUDART_INF_F || x == -CUDART_INF_F) ? 0.f : expf(x - M);
-      wts[threadIdx.x][s] = wt;
-      W += wt;
-    }
-    const float lse0 = W > 0.f ? M + logf(W) : -CUDART_INF_F;
-    float lse = lse0;
-    float f = W > 0.f ? 1.f / W : 0.f;
-    if (p.sink) {
-      const float sg = __ldg(p.sink + h);
-      lse = fmaxf(lse0, sg) + log1pf(expf(-fabsf(lse0 - sg)));
-      f *= expf(lse0 - lse);
-    }
-    fac[threadIdx.x] = f;
-    if (p.lse) p.lse[int64_t(t) * p.H + h] = lse;
+  const float* lp = p.lse_part + int64_t(t) * S * p.H + h;
+  const float x0 = lane < S ? lp[int64_t(lane) * p.H] : -CUDART_INF_F;
+  const float x1 = lane + 32 < S ? lp[int64_t(lane + 32) * p.H] : -CUDART_INF_F;
+  float M = fmaxf(x0, x1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float w0 = (M == -CUDART_INF_F || x0 == -CUDART_INF_F) ? 0.f : expf(x0 - M);
+  const float w1 = (M == -CUDART_INF_F || x1 == -CUDART_INF_F) ? 0.f : expf(x1 - M);
+  float W = w0 + w1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+  const float lse0 = W > 0.f ? M + logf(W) : -CUDART_INF_F;
+  float lse = lse0;
+  float f = W > 0.f ? 1.f / W : 0.f;
+  if (p.sink) {
+    const float sg = __ldg(p.sink + h);
+    lse = fmaxf(lse0, sg) + log1pf(expf(-fabsf(lse0 - sg)));
+    f *= expf(lse0 - lse);
   }
-  __syncthreads();
-  for (int e = threadIdx.x * 4; e < 16 * kLatent; e += blockDim.x * 4) {
-    const int hl = e / kLatent, d = e % kLatent;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < S; ++s) {
-      const float wt = wts[hl][s];
-      if (wt == 0.f) continue;
-      const float4 o = *reinterpret_cast<const float4*>(
-          p.o_part + ((int64_t(t) * S + s) * p.H + h0 + hl) * kLatent + d);
-      acc.x = fmaf(wt, o.x, acc.x);
-      acc.y = fmaf(wt, o.y, acc.y);
-      acc.z = fmaf(wt, o.z, acc.z);
-      acc.w = fmaf(wt, o.w, acc.w);
+  if (lane == 0 && p.lse) p.lse[row] = lse;
+
+  float4 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* op = reinterpret_cast<const float4*>(p.o_part + (int64_t(t) * S * p.H + h) * kLatent) + lane;
+  const int64_t sstride = int64_t(p.H) * (kLatent / 4);  // float4 between splits
+#pragma unroll 2
+  for (int s = 0; s < S; ++s) {
+    const float wt = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+    if (wt == 0.f) continue;  // uniform across the warp
+    float4 o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = __ldcs(op + s * sstride + 32 * k);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc[k].x = fmaf(wt, o[k].x, acc[k].x);
+      acc[k].y = fmaf(wt, o[k].y, acc[k].y);
+      acc[k].z = fmaf(wt, o[k].z, acc[k].z);
+      acc[k].w = fmaf(wt, o[k].w, acc[k].w);
     }
-    const float f = fac[hl];
-    uint2 pk = make_uint2(pack_bf16x2(acc.x * f, acc.y * f), pack_bf16x2(acc.z * f, acc.w * f));
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) +
-                              (int64_t(t) * p.H + h0 + hl) * kLatent + d) = pk;
   }
+  uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + row * kLatent) + lane;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    dst[32 * k] = make_uint2(pack_bf16x2(acc[k].x * f, acc[k].y * f), pack_bf16x2(acc[k].z * f, acc[k].w * f));
 }
 
 template <int FMT>
@@ -591,7 +598,8 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, int /*num_sms*/, cudaStream_t
 }
 
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
-  merge_kernel<<<static_cast<unsigned>(a.T * (a.H >> 4)), 256, 0, s>>>(a);
+  const int64_t rows = int64_t(a.T) * a.H;
+  merge_kernel<<<static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps), 32 * kMergeWarps, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -44,6 +44,7 @@
 // read back with smla_trace_read). Off in normal builds: the macro expands to nothing.
 #ifdef SMLA_TRACE
 __device__ unsigned long long g_trace[2][64][12];
+__device__ unsigned long long g_span[4096][2];
 #define TRACE(ev, tile)                                                                    \
   do {                                                                                     \
     if (blockIdx.x < 2 && (tile) < 64) g_trace[blockIdx.x][(tile)][(ev)] = globaltimer_ns(); \
@@ -109,6 +110,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
   const uint32_t peer = crank ^ 1u;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+#ifdef SMLA_TRACE
+  if (threadIdx.x == 0 && blockIdx.x < 4096) g_span[blockIdx.x][0] = globaltimer_ns();
+#endif
   const int item = blockIdx.x >> 1;
   const int split = item % p.num_splits;
   const int t = item / p.num_splits;
@@ -545,6 +549,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
     tc::fence_after();
     tc::dealloc(tm, 512);
   }
+#ifdef SMLA_TRACE
+  if (threadIdx.x == 0 && blockIdx.x < 4096) g_span[blockIdx.x][1] = globaltimer_ns();
+#endif
 }
 
 }  // namespace
@@ -569,5 +576,8 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
 #ifdef SMLA_TRACE
 extern "C" int smla_trace_read(unsigned long long* host) {
   return int(cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace)));
+}
+extern "C" int smla_span_read(unsigned long long* host) {
+  return int(cudaMemcpyFromSymbol(host, g_span, sizeof(g_span)));
 }
 #endif

@@ -18,6 +18,10 @@ struct DevInfo {
 };
 DevInfo g_dev[kMaxDevices];
 
+// Events of smla_set_kernel_events, per host thread (NULL: no recording).
+thread_local cudaEvent_t t_ev_start = nullptr;
+thread_local cudaEvent_t t_ev_stop = nullptr;
+
 smla_status current_device(int* num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
@@ -205,9 +209,18 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
   a.num_splits = plan.num_splits;
   a.split_len = plan.split_len;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (t_ev_start && cudaEventRecord(t_ev_start, s) != cudaSuccess) return SMLA_ERR_CUDA;
   const cudaError_t e = use_tc(d) ? smla::launch_decode_tc(a, s) : smla::launch_decode_mma(a, sms, s);
   if (e != cudaSuccess) return SMLA_ERR_CUDA;
+  if (t_ev_stop && cudaEventRecord(t_ev_stop, s) != cudaSuccess) return SMLA_ERR_CUDA;
   if (plan.num_splits > 1 && smla::launch_merge(a, s) != cudaSuccess) return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+smla_status smla_set_kernel_events(void* start, void* stop) {
+  if ((start == nullptr) != (stop == nullptr)) return SMLA_ERR_NULL;
+  t_ev_start = static_cast<cudaEvent_t>(start);
+  t_ev_stop = static_cast<cudaEvent_t>(stop);
   return SMLA_OK;
 }
 

@@ -56,6 +56,10 @@ class DeviceDecode:
         self.workspace = torch.zeros((ws + 255) // 256 * 256 // 4, dtype=torch.int32, device=device)
         self.out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((T, H), dtype=torch.float32, device=device) if with_lse else None
+        # the decode kernel the library dispatches to for this batch (the fp8_ds cache with
+        # 64 or more heads takes the tensor-core pair kernel)
+        self.kernel_name = ("decode_tc_kernel" if w.kv_format == "fp8_ds" and H >= 64
+                            else "decode_mma_kernel")
 
     def run(self, stream=None):
         decode(self.desc, self.q, self.kv, self.page_table, self.topk, self.req_id, self.sink,

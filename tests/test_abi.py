@@ -107,3 +107,10 @@ def test_workspace_size_checks_desc_first(L):
 def test_read_error_null(L):
     v = ctypes.c_int32(0)
     assert L.smla_read_error(None, None, 4, ctypes.byref(v), None) == 1
+
+
+def test_kernel_events_hook_needs_both_or_neither(L):
+    P = ctypes.c_void_p
+    assert L.smla_set_kernel_events(P(16), None) == 1
+    assert L.smla_set_kernel_events(None, P(16)) == 1
+    assert L.smla_set_kernel_events(None, None) == 0

@@ -243,6 +243,28 @@ def test_req_id_per_token():
     assert_parity(out[order], lse[order], ref)
 
 
+def test_kernel_events_bracket_the_decode_kernel():
+    # the measurement hook records its events around the decode kernel only: the interval
+    # is positive and no longer than the whole call (decode + split merge)
+    w = W.small_variant(W.WORKLOADS[2], num_requests=2, ctx_lo=2048, ctx_hi=2048, topk=2048)
+    dd = DeviceDecode(W.make_problem(w), num_splits=4)
+    s = torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in evs:
+        e.record(s)
+    dd.run()
+    ref_out = dd.out.clone()
+    smla.set_kernel_events(evs[1], evs[2])
+    evs[0].record(s)
+    dd.run()
+    evs[3].record(s)
+    smla.set_kernel_events()
+    torch.cuda.synchronize()
+    k_ms, all_ms = evs[1].elapsed_time(evs[2]), evs[0].elapsed_time(evs[3])
+    assert 0.0 < k_ms <= all_ms
+    assert torch.equal(dd.out, ref_out)
+
+
 # ------------------------------------------------------------------ full-size, sampled
 
 
