@@ -468,6 +468,8 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
     return;
   }
 
+  // the main loop is over: the split merge, if one follows, may start launching
+  if (tid == 0) pdl_trigger();
   // ---- epilogue: row sums and maxima of this thread's O columns come from their owners
   const float Lh[4] = {__shfl_sync(0xffffffffu, l_g, 8 * c), __shfl_sync(0xffffffffu, l_g, 8 * c + 4),
                        __shfl_sync(0xffffffffu, l_g8, 8 * c), __shfl_sync(0xffffffffu, l_g8, 8 * c + 4)};
@@ -521,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
 // the 512 output dims over the splits with four coalesced 16-byte loads per split.
 constexpr int kMergeWarps = 8;
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const DecodeArgs p) {
+  pdl_wait();  // the decode grid's partials are complete and visible
   const int lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);  // t * H + h
   if (row >= int64_t(p.T) * p.H) return;
@@ -599,8 +602,19 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, int /*num_sms*/, cudaStream_t
 
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
   const int64_t rows = int64_t(a.T) * a.H;
-  merge_kernel<<<static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps), 32 * kMergeWarps, 0, s>>>(a);
-  return cudaGetLastError();
+  // launched with programmatic stream serialisation: its launch overlaps the decode grid's
+  // tail, and the kernel waits (pdl_wait) for the decode results before reading them
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps));
+  cfg.blockDim = dim3(32 * kMergeWarps);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_kernel, a);
 }
 
 }  // namespace smla

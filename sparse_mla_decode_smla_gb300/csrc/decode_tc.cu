@@ -93,7 +93,7 @@ constexpr size_t kOffTmem = kOffPhys + 64 * 8;
 constexpr size_t kOffBars = kOffTmem + 16;
 enum {
   B_RAW_FULL = 0, B_RAW_EMPTY = 3, B_K_FULL = 6, B_K_FREE = 8, B_S_FULL = 10, B_S_FREE = 11,
-  B_XS_FULL = 12, B_RP_FULL = 14, B_P_READY = 16, B_FIN = 18, B_IDX = 19, B_COUNT = 20
+  B_XS_FULL = 12, B_RP_FULL = 14, B_P_READY = 16, B_FIN = 18, B_IDX = 19, B_Q = 20, B_COUNT = 21
 };
 constexpr size_t kSmemTc = kOffBars + B_COUNT * 8 + 1024;  // + alignment slack
 static_assert(kSmemTc <= 232448, "shared memory budget");
@@ -146,6 +146,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
       mbar_init(bar(B_S_FREE), 4);
       mbar_init(bar(B_FIN), 1);
       mbar_init(bar(B_IDX), 1);
+      mbar_init(bar(B_Q), 1);
       tc::fence_mbarrier_init_cluster();
       if (!req_ok && crank == 0 && split == 0) atomicOr(p.err, SMLA_DEVERR_INDEX);
     }
@@ -156,23 +157,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
   }
   const uint32_t tm = *reinterpret_cast<volatile uint32_t*>(sm + kOffTmem);
 
-  // softmax warps place q_c in TMEM (A operand of QK): lane h = head h, 144 columns
+  // softmax warps place q_c in TMEM (A operand of QK): lane h = head h, 144 columns. The
+  // 576 bytes of each head's row this CTA needs (latent dims [256c, 256c+256), RoPE dims
+  // [32c, 32c+32)) arrive by two bulk copies into the (still idle) K-tile area, one
+  // round trip for all heads, then go from shared memory into TMEM.
   if (warp >= 4 && warp < 8) {
+    constexpr uint32_t kQRow = 592;  // 576 + 16: conflict-free 16-byte row reads
     const int q4 = warp & 3;
     const int h = 32 * q4 + lane;
     const uint32_t lrow = tm + (uint32_t(32 * q4) << 16) + kTmQ;
-    const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                       (int64_t(t) * p.H + (h < p.H ? h : 0)) * kDim);
+    const int nheads = req_ok ? min(p.H, 128) : 0;
+    const bool have = h < nheads;
+    const uint32_t qs = sb + uint32_t(kOffKtile) + uint32_t(h) * kQRow;
+    if (h == 0 && nheads > 0) mbar_arrive_expect_tx(bar(B_Q), uint32_t(nheads) * 576u);
+    if (have) {
+      const uint8_t* qrow = reinterpret_cast<const uint8_t*>(p.q) + (int64_t(t) * p.H + h) * (2 * kDim);
+      bulk_g2s(qs, qrow + 512 * crank, 512, bar(B_Q));
+      bulk_g2s(qs + 512, qrow + 1024 + 64 * crank, 64, bar(B_Q));
+    }
+    const bool got = nheads == 0 || mbar_wait(bar(B_Q), 0);
+    if (!got && lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
 #pragma unroll 1
     for (int ch = 0; ch < 9; ++ch) {
       uint32_t wv[16];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        // local 16-byte chunk c16 = 4ch + k: latent dims [8*c16, +8) for c16 < 32, else RoPE
-        const int c16 = 4 * ch + k;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (h < p.H && req_ok)
-          v = __ldg(qrow + (c16 < 32 ? (32 * crank + c16) : (64 + 4 * crank + (c16 - 32))));
+        if (have && got) v = lds128(qs + 16 * (4 * ch + k));
         wv[4 * k] = v.x; wv[4 * k + 1] = v.y; wv[4 * k + 2] = v.z; wv[4 * k + 3] = v.w;
       }
       tc::st16(lrow + 16 * ch, wv);
@@ -356,7 +367,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
         mbar_arrive(bar(B_K_FULL + b));
         mbar_arrive(bar(B_RAW_EMPTY + st));
       }
-    }
+    }    // all K tiles are dequantised: the split merge, if one follows, may start launching
+    if (tid == 0) pdl_trigger();
   }
   // ------------------------------------------------------------------ softmax + epilogue
   else {
@@ -371,7 +383,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
     const bool rp_armer = !owner && lane == 0 && (q4 & 1) == 0;      // first non-owner thread
     float m = -CUDART_INF_F, l = 0.f;
 
-    // rescale this thread's O row (256 columns) by a; waits for the previous PV first
+    // rescale this thread's O row (256 columns) by a; waits for the previous PV first. The
+    // TMEM loads and stores are warp-wide: the whole warp calls this when any lane needs
+    // it (a = 1 leaves a row unchanged).
     auto correct_o = [&](int i, float a) -> bool {
       if (i > 0 && !mbar_wait(bar(B_K_FREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1)) return false;
       tc::fence_after();
@@ -420,7 +434,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
         if (lane == 0) TRACE(6 + (q4 & 1) * 0, i);
         fence_proxy_async_smem();  // the peer's P rows are read by the tensor core
         const float a = reinterpret_cast<const float*>(sm + kOffAlpha)[b * 64 + prow];
-        if (a != 1.f && i > 0 && !correct_o(i, a)) { ok = false; break; }
+        if (i > 0 && __any_sync(0xffffffffu, a != 1.f) && !correct_o(i, a)) { ok = false; break; }
       } else {
         if (!mbar_wait(bar(B_XS_FULL + b), (i >> 1) & 1)) { ok = false; break; }
         if (lane == 0) TRACE(7, i);
@@ -468,7 +482,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
         tc::st_async_b32(tc::mapa(sb + uint32_t(kOffAlpha + (b * 64 + orow) * 4), peer), f2u(a), rbar);
         fence_proxy_async_smem();  // my P rows are read by the tensor core
         if (lane == 0) TRACE(8, i);
-        if (a != 1.f && i > 0 && !correct_o(i, a)) { ok = false; break; }
+        if (i > 0 && __any_sync(0xffffffffu, a != 1.f) && !correct_o(i, a)) { ok = false; break; }
       }
       tc::fence_before();
       __syncwarp();
@@ -506,33 +520,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
         ok = mbar_wait(bar(B_K_FREE + (last & 1)), (last >> 1) & 1);
         tc::fence_after();
       }
-      if (ok && h < p.H) {
+      // TMEM loads are warp-wide: every lane takes part, only real heads store
+      if (__all_sync(0xffffffffu, ok)) {
         const int64_t orow_g = S == 1 ? int64_t(t) * p.H + h : (int64_t(t) * S + split) * p.H + h;
+        // four 16-column loads in flight per wait
 #pragma unroll 1
-        for (int k = 0; k < 16; ++k) {
-          uint32_t v[16];
+        for (int k4 = 0; k4 < 4; ++k4) {
+          uint32_t v4[4][16];
           if (ntiles > 0) {
-            tc::ld16(lrow + kTmO + 16 * k, v);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tc::ld16(lrow + kTmO + 64 * k4 + 16 * j, v4[j]);
             tc::wait_ld();
           } else {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = 0u;
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v4[j][e] = 0u;
           }
-          const int col = 256 * int(crank) + 16 * k;
-          if (S == 1) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow_g * kLatent + col);
-            uint32_t o[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              o[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * f, __uint_as_float(v[2 * e + 1]) * f);
-            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-          } else {
-            float4* dst = reinterpret_cast<float4*>(p.o_part + orow_g * kLatent + col);
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t* v = v4[j];
+            const int col = 256 * int(crank) + 64 * k4 + 16 * j;
+            if (h >= p.H) {
+            } else if (S == 1) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow_g * kLatent + col);
+              uint32_t o[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              dst[e] = make_float4(__uint_as_float(v[4 * e]) * f, __uint_as_float(v[4 * e + 1]) * f,
-                                   __uint_as_float(v[4 * e + 2]) * f, __uint_as_float(v[4 * e + 3]) * f);
+              for (int e = 0; e < 8; ++e)
+                o[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * f, __uint_as_float(v[2 * e + 1]) * f);
+              dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+              dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            } else {
+              float4* dst = reinterpret_cast<float4*>(p.o_part + orow_g * kLatent + col);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dst[e] = make_float4(__uint_as_float(v[4 * e]) * f, __uint_as_float(v[4 * e + 1]) * f,
+                                     __uint_as_float(v[4 * e + 2]) * f, __uint_as_float(v[4 * e + 3]) * f);
+            }
           }
         }
       }

@@ -145,6 +145,18 @@ def test_decode_matches_oracle(small_cases, wi, splits):
     assert smla.read_error(dd.desc, dd.workspace) == 0
 
 
+@pytest.mark.parametrize("heads", [32, 48, 80, 96, 112])
+def test_decode_other_head_counts(heads):
+    # head counts between the workloads' 16/64/128: the 80..112 cases leave part of a warp's
+    # 32 TMEM lanes without a head in the tensor-core kernel
+    w = W.small_variant(W.WORKLOADS[2], num_requests=2, ctx_lo=500, ctx_hi=900, topk=320).replace(
+        num_heads=heads, name=f"fp8_H{heads}")
+    p = W.make_problem(w)
+    for splits in (1, 2):
+        out, lse = DeviceDecode(p, num_splits=splits).run()
+        assert_parity(out, lse, oracle_decode(p))
+
+
 @pytest.mark.parametrize("wi", [1, 2, 4])
 def test_split_count_invariance(small_cases, wi):
     p, ref = small_cases[SMALL[wi].name]
