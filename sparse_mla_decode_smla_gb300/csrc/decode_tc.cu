@@ -410,13 +410,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
       if (lane == 0 && q4 == 0) TRACE(5, i);
       tc::fence_after();
       float s[64];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t v[16];
-        tc::ld16(lrow + kTmS + 16 * k, v);
+      {
+        uint32_t v[64];
+        tc::ld64(lrow + kTmS, v);
         tc::wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) s[16 * k + e] = __uint_as_float(v[e]);
+        for (int e = 0; e < 64; ++e) s[e] = __uint_as_float(v[e]);
       }
       tc::fence_before();
       __syncwarp();
