@@ -19,8 +19,9 @@
 //    half of each valid row (256 latent bytes, the 4 scales, 32 RoPE values = 336 bytes)
 //    as two bulk copies into a 3-stage ring. Bulk copies issued by one warp serialise on
 //    the TMA engine; four issuing warps keep the gather near the per-SM limit.
-//  * warps 0-3, dequant: e4m3 * scale -> bf16, written as the 128-byte-swizzled K tile
-//    [64 slots x 288 dims] (two buffers). The same bytes serve as B of QK (K-major) and
+//  * warps 0-3, dequant: e4m3 * scale -> bf16, written as the swizzled K tile [64 slots x
+//    288 dims]: four 128-byte-swizzled latent panels and a 64-byte-swizzled RoPE panel
+//    (two buffers). The same bytes serve as B of QK (K-major) and
 //    as B of PV (MN-major view of the 256 latent dims).
 //  * warp 12, MMA issuer (one thread): QK = 18 x tcgen05.mma M128 N64 K16 with q (bf16) as
 //    the A operand in TMEM; PV = 4 x tcgen05.mma M128 N256 K16 with P from shared memory.
@@ -64,14 +65,17 @@ constexpr int kThreadsTc = 32 * (kMmaWarp + 1);
 constexpr int kN = 64;             // slots per tile
 constexpr int kStagesTc = 3;       // raw half-row ring
 constexpr int kHalfRow = 336;      // 256 latent + 16 scales + 64 RoPE bytes
-constexpr int kPanel = kN * 128;   // one 64-dim swizzled panel of a tile: 8 KB
-constexpr int kKtile = 5 * kPanel;  // 4 latent panels + 1 RoPE panel
+constexpr int kPanel = kN * 128;   // one 64-dim 128-byte-swizzled panel of a tile: 8 KB
+constexpr int kRopePanel = kN * 64;  // the CTA's 32 RoPE dims, 64-byte swizzle: 4 KB
+constexpr int kKtile = 4 * kPanel + kRopePanel;  // 4 latent panels + the RoPE panel
 constexpr int kPtile = 128 * 128;  // P [128 heads x 64 slots] bf16
 constexpr int kXsRow = 272;        // 64 fp32 + padding (conflict-free row reads)
 constexpr int kXs = 64 * kXsRow;
 constexpr int kMetaRing = 8;
 constexpr int kAheadTc = 4;        // page-table look-ahead (tiles)
 constexpr int kPageRingTc = 6;
+constexpr int kIdxAhead = 8;       // index look-ahead (tiles)
+constexpr int kIdxRing = 16;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 // TMEM columns (512 allocated)
@@ -84,7 +88,7 @@ constexpr size_t kOffPtile = kOffKtile + 2 * size_t(kKtile);
 constexpr size_t kOffRaw = kOffPtile + 2 * size_t(kPtile);
 constexpr size_t kOffXs = kOffRaw + size_t(kStagesTc) * kN * kHalfRow;
 constexpr size_t kOffIdx = kOffXs + 2 * size_t(kXs);
-constexpr size_t kOffPages = kOffIdx + size_t(kMaxSplitLen) * 4;
+constexpr size_t kOffPages = kOffIdx + size_t(kIdxRing) * kN * 4;
 constexpr size_t kOffMeta = kOffPages + size_t(kPageRingTc) * kN * 4;
 constexpr size_t kOffAlpha = kOffMeta + kMetaRing * 8;
 constexpr size_t kOffFin = kOffAlpha + 2 * 64 * 4;
@@ -97,6 +101,10 @@ enum {
 };
 constexpr size_t kSmemTc = kOffBars + B_COUNT * 8 + 1024;  // + alignment slack
 static_assert(kSmemTc <= 232448, "shared memory budget");
+// q staging at start-up: 128 rows of 576 bytes (+16 for conflict-free 16-byte reads) in the
+// K-tile and P-tile area, which the pipeline first writes after the start-up barrier
+constexpr uint32_t kQRow = 592;
+static_assert(128 * kQRow <= kOffRaw, "q staging fits below the raw ring");
 
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
@@ -159,10 +167,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
 
   // softmax warps place q_c in TMEM (A operand of QK): lane h = head h, 144 columns. The
   // 576 bytes of each head's row this CTA needs (latent dims [256c, 256c+256), RoPE dims
-  // [32c, 32c+32)) arrive by two bulk copies into the (still idle) K-tile area, one
+  // [32c, 32c+32)) arrive by two bulk copies into the (still idle) K/P-tile area, one
   // round trip for all heads, then go from shared memory into TMEM.
   if (warp >= 4 && warp < 8) {
-    constexpr uint32_t kQRow = 592;  // 576 + 16: conflict-free 16-byte row reads
     const int q4 = warp & 3;
     const int h = 32 * q4 + lane;
     const uint32_t lrow = tm + (uint32_t(32 * q4) << 16) + kTmQ;
@@ -203,32 +210,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
     const int pw = warp - 8;                 // slots [16 pw, 16 pw + 16) of every tile
     const bool act = lane < kN / kProducersTc;
     const int myslot = (kN / kProducersTc) * pw + lane;
-    int32_t* sidx = reinterpret_cast<int32_t*>(sm + kOffIdx);
-    int32_t* spage = reinterpret_cast<int32_t*>(sm + kOffPages);
+    int32_t* sidx = reinterpret_cast<int32_t*>(sm + kOffIdx);    // index ring
+    int32_t* spage = reinterpret_cast<int32_t*>(sm + kOffPages);  // page-table entry ring
     uint16_t* meta = reinterpret_cast<uint16_t*>(sm + kOffMeta);
-    if (ntiles > 0) {
-      if (pw == 0 && lane == 0) {
-        mbar_arrive_expect_tx(bar(B_IDX), uint32_t(nidx) * 4u);
-        bulk_g2s(smem_u32(sidx), idx_row + j0, uint32_t(nidx) * 4u, bar(B_IDX));
-      }
-      ok = mbar_wait(bar(B_IDX), 0);
-    }
+    // Each lane fetches its own slot's index kIdxAhead tiles ahead and, once that has
+    // landed, its page-table entry kAheadTc tiles ahead, both by 4-byte cp.async. Every
+    // iteration commits one group {index of tile i+kIdxAhead, page entry of tile
+    // i+kAheadTc}; iterations before tile 0 only prime the two rings.
+    auto in_split = [&](int tile) { return act && tile < ntiles && tile * kN + myslot < nidx; };
     auto idx_of = [&](int tile) -> int32_t {
-      const int j = tile * kN + myslot;
-      return (act && tile < ntiles && j < nidx) ? sidx[j] : -1;
+      return in_split(tile) ? sidx[(tile % kIdxRing) * kN + myslot] : -1;
     };
-    auto fetch_page = [&](int tile) {
-      const int32_t idx = idx_of(tile);
-      if (idx >= 0 && (idx >> p.log2_page) < p.stride)
-        cp_async4(smem_u32(spage + (tile % kPageRingTc) * kN + myslot), pt_row + (idx >> p.log2_page));
-      cp_async_commit();
-    };
-    if (ok)
-      for (int d = 0; d < kAheadTc; ++d) fetch_page(d);
     int issued = 0;
-    for (int i = 0; i < ntiles && ok; ++i) {
-      fetch_page(i + kAheadTc);
-      cp_async_wait<kAheadTc>();
+    for (int i = -kIdxAhead; i < ntiles && ok; ++i) {
+      cp_async_wait<kIdxAhead - kAheadTc - 1>();  // the group that fetched index i+kAheadTc
+      const int tp = i + kAheadTc;
+      if (tp >= 0) {
+        const int32_t idx = idx_of(tp);
+        if (idx >= 0 && (idx >> p.log2_page) < p.stride)
+          cp_async4(smem_u32(spage + (tp % kPageRingTc) * kN + myslot), pt_row + (idx >> p.log2_page));
+      }
+      const int ti = i + kIdxAhead;
+      if (in_split(ti))
+        cp_async4(smem_u32(sidx + (ti % kIdxRing) * kN + myslot), idx_row + j0 + ti * kN + myslot);
+      cp_async_commit();
+      if (i < 0) continue;
       const int st = i % kStagesTc;
       if (!mbar_wait(bar(B_RAW_EMPTY + st), ((i / kStagesTc) & 1) ^ 1)) {
         ok = false;
@@ -284,8 +290,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
         const uint32_t kt = sb + uint32_t(kOffKtile) + uint32_t(b * kKtile);
 #pragma unroll
         for (int s = 0; s < 18; ++s) {
-          const uint32_t a = s < 16 ? kt + (s >> 2) * kPanel + (s & 3) * 32 : kt + 4 * kPanel + (s - 16) * 32;
-          tc::mma_ts(tm + kTmS, tm + kTmQ + 8 * s, tc::sdesc_sw128(a, 16, 1024), kIdQK, s > 0);
+          const uint64_t bdesc = s < 16 ? tc::sdesc_sw128(kt + (s >> 2) * kPanel + (s & 3) * 32, 16, 1024)
+                                        : tc::sdesc_sw64(kt + 4 * kPanel + (s - 16) * 32, 16, 512);
+          tc::mma_ts(tm + kTmS, tm + kTmQ + 8 * s, bdesc, kIdQK, s > 0);
         }
         tc::commit(bar(B_S_FULL));
         TRACE(3, i);
@@ -357,7 +364,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
         const int id = tid + 128 * k;
         const int rc = id >> 6, slot = id & 63;
         const uint4 v = lds128(raw + slot * kHalfRow + 272 + 16 * rc);
-        const uint32_t dst = kt + 4 * kPanel + slot * 128 + ((rc ^ (slot & 7)) << 4);
+        const uint32_t dst = kt + 4 * kPanel + slot * 64 + ((rc ^ ((slot >> 1) & 3)) << 4);
         asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
                      "r"(v.w) : "memory");
       }

@@ -20,6 +20,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr, uint32_t lbo, uin
   return d;
 }
 
+// Same with 64-byte swizzle: K-major tiles of 32-element (64 B) rows in 8-row atoms of
+// 512 B (sbo = 512); the atom base is 512-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= uint64_t((addr & 0x3FFFF) >> 4);
+  d |= uint64_t((lbo & 0x3FFFF) >> 4) << 16;
+  d |= uint64_t((sbo & 0x3FFFF) >> 4) << 32;
+  d |= uint64_t(1) << 46;  // descriptor version (tcgen05)
+  d |= uint64_t(4) << 61;  // SWIZZLE_64B
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn_major) << 15) |
