@@ -333,7 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
       if (tid == 0) TRACE(2, i);
       const uint32_t raw = sb + uint32_t(kOffRaw) + uint32_t(st * kN * kHalfRow);
       const uint32_t kt = sb + uint32_t(kOffKtile) + uint32_t(b * kKtile);
-#pragma unroll 2
+#pragma unroll 4
       for (int k = 0; k < 8; ++k) {
         const int id = tid + 128 * k;
         const int ch = id >> 6, slot = id & 63;  // 16 latent bytes [16ch, 16ch+16) of slot
