@@ -54,17 +54,25 @@ def measured_peaks() -> dict:
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the decode
 # kernel, from one ncu capture of this bench's own command on the named workload, with
-# the SHA-256 of the kernel sources at capture time. A capture of an older kernel (the
-# hash differs) is not reported.
+# the SHA-256 (first 16 hex digits) of that kernel's sources at capture time. A capture
+# of an older kernel (the hash differs) is not reported.
+# The 16k-context and 8k-16k-context captures gather exactly as many rows (tokens x
+# valid indices) as the full workloads; only the pool they are drawn from is smaller.
 TRAFFIC = {
+    ("fp8_T32_H64_K2048_ctx1k-32k", "decode_tc_kernel"): (52236288, "8f3b76f6c58a34ba"),
+    ("fp8_T128_H128_K2048_ctx64k_sink", "decode_tc_kernel"): (228855296, "8f3b76f6c58a34ba"),
+    ("fp8_T256_H16_K2048_ctx8k-128k_pad20", "decode_mma_kernel"): (329790208, "0ce18dc013986fa8"),
 }
-KERNEL_SOURCES = ("common.cuh", "kernels.h", "tcgen05.cuh", "decode_tc.cu", "decode_mma.cu")
+KERNEL_SOURCES = {
+    "decode_tc_kernel": ("common.cuh", "kernels.h", "tcgen05.cuh", "decode_tc.cu"),
+    "decode_mma_kernel": ("common.cuh", "kernels.h", "decode_mma.cu"),
+}
 
 
-def kernel_sources_sha() -> str:
+def kernel_sources_sha(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "sparse_mla_decode_smla_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -72,7 +80,7 @@ def kernel_sources_sha() -> str:
 
 def recorded_traffic(workload: str, kernel: str):
     rec = TRAFFIC.get((workload, kernel))
-    if rec is None or rec[1] != kernel_sources_sha():
+    if rec is None or rec[1] != kernel_sources_sha(kernel):
         return None
     return rec[0]
 
@@ -184,13 +192,15 @@ def barrier(world: int):
 # ------------------------------------------------------------------------------ oracle arm
 
 
-def run_oracle_sample(problem, budget_s: float, wall_limit_s: float | None = None):
+def run_oracle_sample(problem, budget_s: float, wall_limit_s: float | None = None,
+                      max_tokens: int | None = None):
     """Time the float64 oracle's decode, as it stands, on whole query tokens.
 
     The oracle's cache rows for a few requests at a time are packed first, outside the
     timed region, as the GPU side's cache is packed before its timed steps. Returns
-    (tokens, seconds of oracle decode) once the decode time reaches budget_s or the wall
-    time reaches wall_limit_s (default 4 x budget_s); at least one token is timed.
+    (tokens, seconds of oracle decode) once the decode time reaches budget_s, the wall
+    time reaches wall_limit_s (default 4 x budget_s) or max_tokens tokens are done; at
+    least one token is timed.
     """
     from oracle.workload_oracle import OracleCache, oracle_decode
     w = problem.w
@@ -207,7 +217,8 @@ def run_oracle_sample(problem, budget_s: float, wall_limit_s: float | None = Non
             oracle_decode(problem, tokens=[t], cache=cache)
             el += time.perf_counter() - t0
             done += 1
-            if el >= budget_s or time.perf_counter() - wall0 >= wall_limit:
+            if (el >= budget_s or time.perf_counter() - wall0 >= wall_limit
+                    or (max_tokens is not None and done >= max_tokens)):
                 return done, el
     return done, el
 
@@ -236,8 +247,7 @@ def reference_arm(args):
     if args.warmup > 0:  # one untimed token
         run_oracle_sample(problem, budget_s=0.0)
     n, el = run_oracle_sample(problem, budget_s=args.ref_budget_seconds,
-                              wall_limit_s=4.0 * args.ref_budget_seconds)
-    n = min(n, max(1, args.steps))
+                              wall_limit_s=4.0 * args.ref_budget_seconds, max_tokens=max(1, args.steps))
     value = n / el if el > 0 else float("nan")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "query-tokens/s",
             "n_gpus": 1, "steps": n, "steps_requested": args.steps, "warmup": args.warmup,
