@@ -41,6 +41,7 @@ DIM = LATENT + ROPE
 BLOCK = 128  # latent dims per fp32 scale
 FP8_ROW_BYTES = LATENT + 4 * 4 + ROPE * 2  # 656
 BF16_ROW_BYTES = DIM * 2  # 1152
+FP8_TENSOR_ROW_BYTES = DIM  # 576
 E4M3_MAX = 448.0
 
 SCALE_POW2 = 0
@@ -146,6 +147,22 @@ def pack_fp8_ds(latent_bits: np.ndarray, rope_bits: np.ndarray,
     return out
 
 
+def pack_fp8_tensor(latent_bits: np.ndarray, rope_bits: np.ndarray, kv_scale: float) -> np.ndarray:
+    """Quantise bf16 latent [N,512] + bf16 RoPE [N,64] into 576-byte per-tensor FP8 rows.
+
+    The contiguous FP8 cache of FlashInfer's DeepSeek-V4 path (vLLM PR #43827,
+    "实现拆解 4" and "关键源码片段": the compressor's store_full_fp8 writes a
+    per-tensor FP8 cache with one fp8 scale; _resolve_dsv4_kv_cache_dtype gives it
+    dtype float8_e4m3fn): all 576 values [latent 512 | RoPE 64] are E4M3 codes of
+    fl32(x / kv_scale), round-to-nearest-even, saturating at +-448.
+    """
+    lat = bf16_bits_to_f64(latent_bits).reshape(-1, LATENT)
+    rope = bf16_bits_to_f64(rope_bits).reshape(-1, ROPE)
+    x = np.concatenate([lat, rope], axis=1)
+    q = f32(x / float(f32(kv_scale)))
+    return e4m3_encode_rne_satfinite(q).astype(np.uint8).reshape(-1, FP8_TENSOR_ROW_BYTES)
+
+
 def pack_bf16(latent_bits: np.ndarray, rope_bits: np.ndarray) -> np.ndarray:
     """bf16 cache row: 576 bf16 values [latent 512 | rope 64] (little-endian) = 1152 bytes."""
     n = np.asarray(latent_bits).reshape(-1, LATENT).shape[0]
@@ -154,18 +171,25 @@ def pack_bf16(latent_bits: np.ndarray, rope_bits: np.ndarray) -> np.ndarray:
     return row.view(np.uint8).reshape(n, BF16_ROW_BYTES)
 
 
-def dequant_rows(rows: np.ndarray, kv_format: str) -> np.ndarray:
+def dequant_rows(rows: np.ndarray, kv_format: str, kv_scale: float | None = None) -> np.ndarray:
     """Cache rows [n, R] uint8 -> [n, 576] float64 key vectors.
 
     fp8_ds: latent element d = fl32(e4m3(code_d) * scale[d // 128]) -- the
     float64 product of a 4-bit and a 24-bit significand is exact, so rounding
     it once to fp32 is the fp32 multiply; RoPE is bf16, exact.
+    fp8_tensor: every element d = fl32(e4m3(code_d) * kv_scale), the per-tensor
+    scale of the FlashInfer path (vLLM PR #43827: bmm1_scale = scale * q_scale *
+    kv_scale, bmm2_scale = kv_scale, i.e. keys and values both carry kv_scale).
     bf16: the 576 bf16 values, exact.
     """
     rows = np.ascontiguousarray(rows, dtype=np.uint8)
     n = rows.shape[0]
     if kv_format == "bf16":
         return bf16_bits_to_f64(rows.view("<u2").reshape(n, DIM))
+    if kv_format == "fp8_tensor":
+        if kv_scale is None:
+            raise ValueError("fp8_tensor rows need kv_scale")
+        return f32(e4m3_decode(rows[:, :DIM]) * float(f32(kv_scale)))
     codes = rows[:, :LATENT]
     sc = rows[:, LATENT:LATENT + 16].copy().view("<f4").reshape(n, 4).astype(np.float64)
     lat = f32(e4m3_decode(codes) * np.repeat(sc, BLOCK, axis=1))
@@ -249,7 +273,8 @@ def attend(q: np.ndarray, keys: np.ndarray, sm_scale: float, sink: np.ndarray | 
 
 def decode(q_bits: np.ndarray, fetch_rows: Callable[[np.ndarray], np.ndarray], kv_format: str,
            page_table: np.ndarray, topk: np.ndarray, page_size: int, num_pages: int,
-           sm_scale: float, sink=None, next_n: int = 1, req_id_per_token=None, tokens=None):
+           sm_scale: float, sink=None, next_n: int = 1, req_id_per_token=None, tokens=None,
+           kv_scale: float | None = None):
     """Sparse MLA decode of the listed tokens (all by default), float64.
 
     q_bits [T, H, 576] bf16 bit patterns; fetch_rows(phys_slots) -> [n, R] uint8
@@ -264,7 +289,7 @@ def decode(q_bits: np.ndarray, fetch_rows: Callable[[np.ndarray], np.ndarray], k
         r = request_of_token(t, next_n, req_id_per_token)
         _, phys, n_invalid = physical_slots(topk[t], page_table[r], page_size, num_pages)
         rows = fetch_rows(phys) if len(phys) else np.zeros((0, 1), dtype=np.uint8)
-        keys = dequant_rows(rows, kv_format) if len(phys) else np.zeros((0, DIM))
+        keys = dequant_rows(rows, kv_format, kv_scale) if len(phys) else np.zeros((0, DIM))
         o, l, l0 = attend(bf16_bits_to_f64(q_bits[t]), keys, sm_scale, sink)
         outs.append(o)
         lses.append(l)
@@ -275,7 +300,7 @@ def decode(q_bits: np.ndarray, fetch_rows: Callable[[np.ndarray], np.ndarray], k
 
 
 def gather_dequant(fetch_rows, kv_format: str, page_table, topk, page_size: int, num_pages: int,
-                   next_n: int = 1, req_id_per_token=None) -> np.ndarray:
+                   next_n: int = 1, req_id_per_token=None, kv_scale: float | None = None) -> np.ndarray:
     """The gathered, dequantised key rows: [T, K, 576] as fp32 values (float64 array).
 
     Row (t, j) is dequant(row at the physical slot of topk[t, j]); padding and
@@ -288,5 +313,5 @@ def gather_dequant(fetch_rows, kv_format: str, page_table, topk, page_size: int,
         r = request_of_token(t, next_n, req_id_per_token)
         keep, phys, _ = physical_slots(topk[t], page_table[r], page_size, num_pages)
         if keep:
-            out[t, keep] = dequant_rows(fetch_rows(phys), kv_format)
+            out[t, keep] = dequant_rows(fetch_rows(phys), kv_format, kv_scale)
     return out

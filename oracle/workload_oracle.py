@@ -31,6 +31,9 @@ class OracleCache:
             kv = problem.kv_bf16.cpu().reshape(problem.num_pages, P, 576)
             sel = kv[pages].reshape(-1, 576)
             self.rows = O.pack_bf16(_bits(sel[:, :512]), _bits(sel[:, 512:]))
+        elif w.kv_format == "fp8_tensor":
+            lat, rope = problem.raw_pages(pages)
+            self.rows = O.pack_fp8_tensor(_bits(lat), _bits(rope), w.kv_scale)
         else:
             lat, rope = problem.raw_pages(pages)
             self.rows = O.pack_fp8_ds(_bits(lat), _bits(rope), scale_mode)
@@ -51,4 +54,5 @@ def oracle_decode(problem, tokens=None, scale_mode: int = O.SCALE_POW2, cache: O
     sink = None if problem.sink is None else problem.sink.cpu().double().numpy()
     return O.decode(_bits(problem.q), cache.fetch, w.kv_format, problem.page_table.cpu().numpy(),
                     problem.topk.cpu().numpy(), w.page_size, problem.num_pages, w.sm_scale,
-                    sink=sink, next_n=w.next_n, tokens=tokens)
+                    sink=sink, next_n=w.next_n, tokens=tokens,
+                    kv_scale=w.kv_scale if w.kv_format == "fp8_tensor" else None)

@@ -142,6 +142,43 @@ def test_pack_bf16_layout():
     assert np.array_equal(back[:, :512], _bits(lat)) and np.array_equal(back[:, 512:], _bits(rope))
 
 
+@pytest.mark.parametrize("kv_scale", [1.0, 2.0 ** -6, 0.0137])
+def test_pack_fp8_tensor_matches_torch_cast(kv_scale):
+    # codes are torch's float8_e4m3fn cast of the fp32 quotient x / kv_scale (in range)
+    g = torch.Generator().manual_seed(21)
+    lat = torch.randn(200, 512, generator=g).to(torch.bfloat16)
+    rope = torch.randn(200, 64, generator=g).to(torch.bfloat16)
+    rows = O.pack_fp8_tensor(_bits(lat), _bits(rope), kv_scale)
+    assert rows.shape == (200, 576) and rows.dtype == np.uint8
+    x = torch.cat([lat, rope], 1).to(torch.float32)
+    quot = (x / torch.tensor(kv_scale, dtype=torch.float32))
+    assert quot.abs().max() < 448
+    ref = quot.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(rows, ref)
+
+
+def test_pack_fp8_tensor_saturates_and_scales_by_powers_of_two():
+    lat = torch.full((2, 512), 3.0).to(torch.bfloat16)
+    lat[1, :] = -1000.0
+    rope = torch.zeros(2, 64).to(torch.bfloat16)
+    rows = O.pack_fp8_tensor(_bits(lat), _bits(rope), 1.0)
+    assert (rows[1, :512] == 0xFE).all() and (rows[:, 512:] == 0).all()
+    # x / s with s a power of two is exact: scaling x and s together leaves the codes
+    x = torch.randn(50, 576, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    a = O.pack_fp8_tensor(_bits(x[:, :512]), _bits(x[:, 512:]), 2.0 ** -4)
+    xb = (x.to(torch.float32) * 8).to(torch.bfloat16)
+    b = O.pack_fp8_tensor(_bits(xb[:, :512]), _bits(xb[:, 512:]), 2.0 ** -1)
+    assert np.array_equal(a, b)
+
+
+def test_dequant_fp8_tensor_matches_torch():
+    codes = np.random.default_rng(9).integers(0, 256, (300, 576), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    for s in (1.0, 0.0137, 2.0 ** -9):
+        got = O.dequant_rows(codes, "fp8_tensor", s)
+        assert np.array_equal(got, _torch_tensor_keys(codes, s).numpy())
+
+
 def test_dequant_rows_fp8_is_fp32_product():
     lat = _rand_latent(16, seed=5)
     rows = O.pack_fp8_ds(_bits(lat), _bits(torch.randn(16, 64).to(torch.bfloat16)), O.SCALE_FP32)
@@ -168,19 +205,33 @@ def test_physical_slots_invalid_entries_dropped_and_counted():
 
 # ----------------------------------------------------------------------------- attention
 
+TENSOR_SCALE = 2.0 ** -5  # per-tensor scale of the fp8_tensor pins (N(0,1) values stay in range)
+
+
+def _torch_tensor_keys(rows: np.ndarray, kv_scale: float) -> torch.Tensor:
+    """Keys of per-tensor FP8 rows through torch's own float8 decode and an fp32 multiply."""
+    codes = torch.from_numpy(np.ascontiguousarray(rows[:, :576])).view(torch.float8_e4m3fn)
+    return (codes.to(torch.float32) * torch.tensor(kv_scale, dtype=torch.float32)).to(torch.float64)
+
+
 def _problem(n_pages=3, P=64, H=4, fmt="fp8_ds", seed=0, sink=False):
     g = torch.Generator().manual_seed(seed)
     n = n_pages * P
     lat = torch.randn(n, 512, generator=g).to(torch.bfloat16)
     rope = torch.randn(n, 64, generator=g).to(torch.bfloat16)
-    rows = O.pack_fp8_ds(_bits(lat), _bits(rope)) if fmt == "fp8_ds" else O.pack_bf16(_bits(lat), _bits(rope))
+    if fmt == "fp8_ds":
+        rows = O.pack_fp8_ds(_bits(lat), _bits(rope))
+    elif fmt == "fp8_tensor":
+        rows = O.pack_fp8_tensor(_bits(lat), _bits(rope), TENSOR_SCALE)
+    else:
+        rows = O.pack_bf16(_bits(lat), _bits(rope))
     q = torch.randn(1, H, 576, generator=g).to(torch.bfloat16)
     pt = torch.randperm(n_pages, generator=g).numpy()[None, :].astype(np.int32)
     sig = torch.randn(H, generator=g, dtype=torch.float64).numpy() if sink else None
     return rows, q, pt, sig
 
 
-@pytest.mark.parametrize("fmt", ["fp8_ds", "bf16"])
+@pytest.mark.parametrize("fmt", ["fp8_ds", "bf16", "fp8_tensor"])
 @pytest.mark.parametrize("sink", [False, True])
 def test_full_context_topk_equals_dense_sdpa(fmt, sink):
     P, n_pages, H = 64, 3, 4
@@ -188,10 +239,15 @@ def test_full_context_topk_equals_dense_sdpa(fmt, sink):
     ctx = n_pages * P
     perm = np.random.default_rng(2).permutation(ctx).astype(np.int32)
     sm = 1.0 / 24
-    res = O.decode(_bits(q), lambda s: rows[s], fmt, pt, perm[None, :], P, n_pages, sm, sink=sig)
+    kvs = TENSOR_SCALE if fmt == "fp8_tensor" else None
+    res = O.decode(_bits(q), lambda s: rows[s], fmt, pt, perm[None, :], P, n_pages, sm, sink=sig,
+                   kv_scale=kvs)
     # dense reference: all keys of the request in logical order, by page table lookup
     logical_rows = np.concatenate([rows[p * P:(p + 1) * P] for p in pt[0]])
-    keys = torch.from_numpy(O.dequant_rows(logical_rows, fmt))
+    if fmt == "fp8_tensor":  # keys decoded by torch, not by the oracle
+        keys = _torch_tensor_keys(logical_rows, TENSOR_SCALE)
+    else:
+        keys = torch.from_numpy(O.dequant_rows(logical_rows, fmt))
     qf = torch.from_numpy(O.bf16_bits_to_f64(_bits(q[0])))  # [H, 576]
     if sig is None:
         out = torch.nn.functional.scaled_dot_product_attention(

@@ -51,3 +51,11 @@ def test_raw_chunk_is_reproducible():
     pages = [0, 2]
     lat, rope = a.raw_pages(pages)
     assert torch.equal(lat[64:128], la[128:192]) and torch.equal(rope[:64], ra[:64])
+
+
+def test_per_tensor_fp8_workload_shape():
+    w = W.BY_NAME["fp8tensor_T32_H64_K2048_ctx1k-32k"]
+    assert w.kv_format == "fp8_tensor" and w.row_bytes == 576 and w.kv_scale == 1.0
+    small = W.small_variant(w, num_requests=2, ctx_lo=100, ctx_hi=300, topk=128)
+    p = W.make_problem(small)
+    assert p.topk.shape == (2, 128) and p.q.shape == (2, 64, 576)

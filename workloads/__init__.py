@@ -50,7 +50,7 @@ class Workload:
     num_heads: int
     topk: int
     page_size: int
-    kv_format: str  # "bf16" (576 bf16 = 1152 B per slot) or "fp8_ds" (656 B per slot)
+    kv_format: str  # "bf16" (1152 B per slot), "fp8_ds" (656 B) or "fp8_tensor" (576 B)
     ctx_lo: int
     ctx_hi: int
     sink: bool
@@ -58,6 +58,7 @@ class Workload:
     shared_pool_pages: int = 0  # > 0: every request maps the same small pool
     sm_scale: float = SM_SCALE_576
     seed_offset: int = 0
+    kv_scale: float = 1.0  # per-tensor scale of the fp8_tensor format (unused otherwise)
 
     @property
     def num_tokens(self) -> int:
@@ -65,7 +66,7 @@ class Workload:
 
     @property
     def row_bytes(self) -> int:
-        return 656 if self.kv_format == "fp8_ds" else 2 * HEAD_DIM
+        return {"fp8_ds": 656, "fp8_tensor": HEAD_DIM}.get(self.kv_format, 2 * HEAD_DIM)
 
     @property
     def page_table_stride(self) -> int:
@@ -97,7 +98,13 @@ WORKLOADS = [
     Workload("fp8_T256_H16_K2048_ctx8k-128k_pad20", 256, 1, 16, 2048, 64, "fp8_ds", 8192,
              131072, False, tail_pad=410, seed_offset=4),
 ]
-BY_NAME = {w.name: w for w in WORKLOADS}
+# The per-tensor FP8 cache of the FlashInfer path (vLLM PR #43827): the default
+# workload's batch with that format, at the per-tensor scale 1.0 the page's code uses.
+EXTRA_WORKLOADS = [
+    Workload("fp8tensor_T32_H64_K2048_ctx1k-32k", 32, 1, 64, 2048, 64, "fp8_tensor", 1024, 32768,
+             False, seed_offset=5, kv_scale=1.0),
+]
+BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
 
 
 def _mix(seed: int, tag: int) -> int:
