@@ -412,7 +412,8 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[w.name for w in W.WORKLOADS])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[w.name for w in W.WORKLOADS + W.EXTRA_WORKLOADS])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)

@@ -46,7 +46,13 @@ enum {
   SMLA_KV_BF16 = 0,
   /* fp8_ds_mla: 656 bytes per slot = 512 E4M3FN latent codes | 4 fp32 scales
    * (little-endian; scale b covers latent dims [128b, 128b+128)) | 64 bf16 RoPE. */
-  SMLA_KV_FP8_DS = 1
+  SMLA_KV_FP8_DS = 1,
+  /* per-tensor FP8: 576 E4M3FN codes per slot, [latent 512 | RoPE 64] = 576 bytes, all
+   * dequantised with the one fp32 scale smla_desc.kv_scale (the contiguous per-tensor FP8
+   * cache of vLLM PR #43827 "实现拆解 4" / "关键源码片段": keys and values both carry
+   * kv_scale, bmm1_scale = scale * q_scale * kv_scale, bmm2_scale = kv_scale; q stays
+   * bf16, so q_scale = 1). */
+  SMLA_KV_FP8_TENSOR = 2
 };
 
 /* Block-scale rule of smla_pack_kv (amax = max |x| over the 128-dim block). */
@@ -76,13 +82,15 @@ typedef struct smla_desc {
   float sm_scale;            /* softmax scale multiplying q.k (e.g. 1/sqrt(576)) */
   int32_t num_splits;        /* 0: the library chooses; n > 0: split the top-k list
                                 into n contiguous parts merged by log-sum-exp */
-  int32_t reserved[4];       /* must be zero */
+  float kv_scale;            /* SMLA_KV_FP8_TENSOR: the cache's per-tensor scale (finite,
+                                > 0); ignored by the other formats */
+  int32_t reserved[3];       /* must be zero */
 } smla_desc;
 
 /* Human-readable name of a status (static string). */
 const char* smla_status_string(int32_t status);
 
-/* ABI version of this header (increments on any incompatible change). */
+/* ABI version of this header (increments on any incompatible change; 2 added kv_scale). */
 int32_t smla_abi_version(void);
 
 /*
@@ -151,6 +159,19 @@ smla_status smla_set_kernel_events(void* start, void* stop);
 smla_status smla_pack_kv(int32_t kv_format, int32_t scale_mode, const void* latent,
                          const void* rope, const int64_t* slot_mapping, int64_t n,
                          void* kv_cache, int64_t num_slots, void* stream);
+
+/*
+ * Write rows of a per-tensor FP8 cache (SMLA_KV_FP8_TENSOR): for each i < n with
+ * 0 <= slot_mapping[i] < num_slots, row slot_mapping[i] of kv_cache (576 bytes) receives
+ * the E4M3 codes, round-to-nearest-even and saturating at +-448, of fl32(x / kv_scale)
+ * for the 512 latent values latent[i] and the 64 RoPE values rope[i] (bf16). This is the
+ * store_full_fp8 path of the compressor in vLLM PR #43827 "实现拆解 4-5".
+ *   latent [n, 512] bf16 and rope [n, 64] bf16, 16-byte aligned; slot_mapping [n] int64;
+ *   kv_scale finite and > 0 (SMLA_ERR_SHAPE otherwise).
+ */
+smla_status smla_pack_kv_fp8_tensor(const void* latent, const void* rope,
+                                    const int64_t* slot_mapping, int64_t n, float kv_scale,
+                                    void* kv_cache, int64_t num_slots, void* stream);
 
 /*
  * Test hook exposing the gather + dequantise steps of smla_decode

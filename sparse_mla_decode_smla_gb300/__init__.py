@@ -14,6 +14,7 @@ from ._build import LIB as LIB_PATH
 
 SMLA_KV_BF16 = 0
 SMLA_KV_FP8_DS = 1
+SMLA_KV_FP8_TENSOR = 2
 SMLA_SCALE_POW2 = 0
 SMLA_SCALE_FP32 = 1
 SMLA_DEVERR_INDEX = 1
@@ -24,7 +25,7 @@ STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_NULL", 2: "SMLA_ERR_SHAPE", 3: "SMLA_ERR_AL
           7: "SMLA_ERR_INDEX_RANGE", 8: "SMLA_ERR_DEVICE"}
 EXPORTS = ["smla_status_string", "smla_abi_version", "smla_workspace_size", "smla_decode",
            "smla_pack_kv", "smla_gather_dequant", "smla_read_error", "smla_decode_noalloc",
-           "smla_set_kernel_events"]
+           "smla_set_kernel_events", "smla_pack_kv_fp8_tensor"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -40,7 +41,8 @@ class smla_desc(ctypes.Structure):
                 ("next_n", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("num_pages", ctypes.c_int64), ("page_table_stride", ctypes.c_int32),
                 ("kv_format", ctypes.c_int32), ("sm_scale", ctypes.c_float),
-                ("num_splits", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+                ("num_splits", ctypes.c_int32), ("kv_scale", ctypes.c_float),
+                ("reserved", ctypes.c_int32 * 3)]
 
 
 _lib = None
@@ -65,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.smla_decode.argtypes = [D, P, P, P, P, P, P, P, P, P, SZ, P]
         L.smla_pack_kv.restype = I32
         L.smla_pack_kv.argtypes = [I32, I32, P, P, P, I64, P, I64, P]
+        L.smla_pack_kv_fp8_tensor.restype = I32
+        L.smla_pack_kv_fp8_tensor.argtypes = [P, P, P, I64, ctypes.c_float, P, I64, P]
         L.smla_gather_dequant.restype = I32
         L.smla_gather_dequant.argtypes = [D, P, P, P, P, P, P, P]
         L.smla_decode_noalloc.restype = I32
@@ -98,12 +102,13 @@ def _check(fn: str, status: int):
 
 
 def make_desc(num_tokens, num_heads, topk, num_requests, page_size, num_pages, page_table_stride,
-              kv_format, sm_scale, next_n=1, num_splits=0) -> smla_desc:
+              kv_format, sm_scale, next_n=1, num_splits=0, kv_scale=1.0) -> smla_desc:
     d = smla_desc()
     d.num_tokens, d.num_heads, d.topk = num_tokens, num_heads, topk
     d.num_requests, d.next_n, d.page_size = num_requests, next_n, page_size
     d.num_pages, d.page_table_stride = num_pages, page_table_stride
     d.kv_format, d.sm_scale, d.num_splits = kv_format, sm_scale, num_splits
+    d.kv_scale = kv_scale
     return d
 
 
@@ -150,6 +155,12 @@ def set_kernel_events(start=None, stop=None):
 def pack_kv(kv_format, scale_mode, latent, rope, slot_mapping, kv_cache, num_slots, stream=None):
     _check("smla_pack_kv", lib().smla_pack_kv(
         kv_format, scale_mode, _ptr(latent), _ptr(rope), _ptr(slot_mapping), latent.shape[0],
+        _ptr(kv_cache), num_slots, _stream(stream)))
+
+
+def pack_kv_fp8_tensor(latent, rope, slot_mapping, kv_cache, num_slots, kv_scale, stream=None):
+    _check("smla_pack_kv_fp8_tensor", lib().smla_pack_kv_fp8_tensor(
+        _ptr(latent), _ptr(rope), _ptr(slot_mapping), latent.shape[0], float(kv_scale),
         _ptr(kv_cache), num_slots, _stream(stream)))
 
 

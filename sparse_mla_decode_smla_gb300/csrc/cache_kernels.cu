@@ -5,6 +5,8 @@
 // covers latent dims [128b, 128b+128) (vLLM PR #43477 "实现拆解 1": the fp8_ds_mla
 // cache; vLLM PR #43827 "功能与动机": the "UE8M0 paged" FlashMLA layout, i.e. power-of-
 // two block scales).
+// Per-tensor FP8 row (576 B): 576 E4M3FN codes [latent 512 | RoPE 64] of x / kv_scale,
+// one scale for the whole cache (vLLM PR #43827 "实现拆解 4": store_full_fp8).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -16,7 +18,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint4* __restrict__ lat
                                                    const uint4* __restrict__ rope,
                                                    const int64_t* __restrict__ slot_mapping,
                                                    int64_t n, uint8_t* __restrict__ kv,
-                                                   int64_t num_slots, int scale_mode) {
+                                                   int64_t num_slots, int scale_mode,
+                                                   float kv_scale) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (row >= n) return;
@@ -29,6 +32,33 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint4* __restrict__ lat
     dst[2 * lane] = x0;
     dst[2 * lane + 1] = x1;
     if (lane < 8) dst[64 + lane] = rope[row * 8 + lane];
+    return;
+  }
+  if (FMT == SMLA_KV_FP8_TENSOR) {
+    uint8_t* dst = kv + slot * kFp8TensorRowBytes;
+    const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    uint32_t codes[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[2 * i]), kv_scale), __fdiv_rn(bf16_hi(w[2 * i]), kv_scale));
+      const uint16_t hi =
+          f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[2 * i + 1]), kv_scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), kv_scale));
+      codes[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+    *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+    if (lane < 8) {  // RoPE values [8 lane, 8 lane + 8)
+      const uint4 r = rope[row * 8 + lane];
+      const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+      uint32_t rc[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(rw[2 * i]), kv_scale), __fdiv_rn(bf16_hi(rw[2 * i]), kv_scale));
+        const uint16_t hi =
+            f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(rw[2 * i + 1]), kv_scale), __fdiv_rn(bf16_hi(rw[2 * i + 1]), kv_scale));
+        rc[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      }
+      *reinterpret_cast<uint2*>(dst + kLatent + 8 * lane) = make_uint2(rc[0], rc[1]);
+    }
     return;
   }
   const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
@@ -72,7 +102,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint4* __restrict__ lat
   if (lane < 8) *reinterpret_cast<uint4*>(dst + kRopeOffFp8 + 16 * lane) = rope[row * 8 + lane];
 }
 
-cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, const void* latent,
+cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, float kv_scale, const void* latent,
                         const void* rope, const int64_t* slot_mapping, int64_t n, void* kv,
                         int64_t num_slots, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
@@ -82,10 +112,13 @@ cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, const void* laten
   auto* K = static_cast<uint8_t*>(kv);
   if (kv_format == SMLA_KV_FP8_DS)
     pack_kernel<SMLA_KV_FP8_DS><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        L, R, slot_mapping, n, K, num_slots, scale_mode);
+        L, R, slot_mapping, n, K, num_slots, scale_mode, kv_scale);
+  else if (kv_format == SMLA_KV_FP8_TENSOR)
+    pack_kernel<SMLA_KV_FP8_TENSOR><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        L, R, slot_mapping, n, K, num_slots, scale_mode, kv_scale);
   else
     pack_kernel<SMLA_KV_BF16><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        L, R, slot_mapping, n, K, num_slots, scale_mode);
+        L, R, slot_mapping, n, K, num_slots, scale_mode, kv_scale);
   return cudaGetLastError();
 }
 
@@ -129,6 +162,29 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(DecodeArgs a, float
     const uint32_t rw = reinterpret_cast<const uint32_t*>(src + kRopeOffFp8)[lane];
     rp0 = bf16_lo(rw);
     rp1 = bf16_hi(rw);
+  } else if (a.kv_format == SMLA_KV_FP8_TENSOR) {
+    const uint8_t* src = a.kv + slot * kFp8TensorRowBytes;
+    const uint4 c = *reinterpret_cast<const uint4*>(src + 16 * lane);
+    const float scale = a.kv_scale;
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t lo, hi;
+      e4m3x4_to_f16x4(w[i], lo, hi);
+      const float2 f0 = __half22float2(*reinterpret_cast<__half2*>(&lo));
+      const float2 f1 = __half22float2(*reinterpret_cast<__half2*>(&hi));
+      v[4 * i] = __fmul_rn(f0.x, scale);
+      v[4 * i + 1] = __fmul_rn(f0.y, scale);
+      v[4 * i + 2] = __fmul_rn(f1.x, scale);
+      v[4 * i + 3] = __fmul_rn(f1.y, scale);
+    }
+    // RoPE dims [2 lane, 2 lane + 2): two codes
+    const uint32_t rc = reinterpret_cast<const uint16_t*>(src + kLatent)[lane];
+    uint32_t lo, hi;
+    e4m3x4_to_f16x4(rc, lo, hi);
+    const float2 rf = __half22float2(*reinterpret_cast<__half2*>(&lo));
+    rp0 = __fmul_rn(rf.x, scale);
+    rp1 = __fmul_rn(rf.y, scale);
   } else {
     const uint8_t* src = a.kv + slot * kBf16RowBytes;
     const uint4 c0 = *reinterpret_cast<const uint4*>(src + 32 * lane);

@@ -15,6 +15,7 @@ constexpr int kRope = 64;
 constexpr int kDim = kLatent + kRope;
 constexpr int kFp8RowBytes = 656;   // 512 e4m3 | 4 fp32 scales | 64 bf16
 constexpr int kBf16RowBytes = 1152; // 576 bf16
+constexpr int kFp8TensorRowBytes = 576;  // 576 e4m3, one per-tensor scale
 constexpr int kScaleOff = 512;      // byte offset of the scales in an fp8_ds row
 constexpr int kRopeOffFp8 = 528;    // byte offset of the RoPE part in an fp8_ds row
 constexpr float kLog2e = 1.4426950408889634f;
@@ -128,6 +129,11 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ float lds_f32(uint32_t addr) {

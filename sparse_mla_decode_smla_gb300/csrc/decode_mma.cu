@@ -61,8 +61,10 @@ constexpr int kPageRing = 8;
 
 template <int FMT>
 struct Cfg {
-  static constexpr bool kFp8 = FMT == SMLA_KV_FP8_DS;
-  static constexpr int kRowBytes = kFp8 ? kFp8RowBytes : kBf16RowBytes;
+  static constexpr bool kFp8 = FMT != SMLA_KV_BF16;          // e4m3 latent codes
+  static constexpr bool kTensor = FMT == SMLA_KV_FP8_TENSOR;  // one scale, e4m3 RoPE too
+  static constexpr int kRowBytes =
+      kTensor ? kFp8TensorRowBytes : (kFp8 ? kFp8RowBytes : kBf16RowBytes);
   static constexpr int kStages = kFp8 ? SMLA_MMA_STAGES_FP8 : 3;
   static constexpr size_t kRing = size_t(kStages) * kSlots * kRowBytes;
   static constexpr size_t kRed = 2 * 4 * 4 * 32 * 16;  // partial scores [2][warp][nt][lane] float4
@@ -230,6 +232,9 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
     const uint2 rv8 =
         __ldg(reinterpret_cast<const uint2*>(qt + (g + 8) * kDim + kLatent + 16 * w + 4 * c));
     qr[0] = rv.x; qr[1] = rv8.x; qr[2] = rv.y; qr[3] = rv8.y;
+    if (C::kTensor)  // the RoPE codes become f16 B fragments: q's RoPE part goes f16 too
+#pragma unroll
+      for (int e = 0; e < 4; ++e) qr[e] = bf16x2_to_f16x2(qr[e]);
   }
 
   float O[8][2][4];
@@ -282,12 +287,22 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
           const uint4 v0 = lds128(rb), v1 = lds128(rb + 16);
           wd[nt][0] = v0.x; wd[nt][1] = v0.y; wd[nt][2] = v0.z; wd[nt][3] = v0.w;
           wd[nt][4] = v1.x; wd[nt][5] = v1.y; wd[nt][6] = v1.z; wd[nt][7] = v1.w;
-          const uint2 rv = lds64(sb + (8 * nt + g) * RB + kRopeOffFp8 + 2 * (16 * w + 4 * c));
 #pragma unroll
           for (int e = 0; e < 4; ++e) accr[nt][e] = 0.f;
-          mma_bf16(accr[nt], qr, rv.x, rv.y);
-          sc[nt][0] = lds_f32(sb + (8 * nt + 2 * c) * RB + kScaleOff + 4 * w);
-          sc[nt][1] = lds_f32(sb + (8 * nt + 2 * c + 1) * RB + kScaleOff + 4 * w);
+          if (C::kTensor) {
+            // RoPE codes of dims [16w + 4c, +4), one scale for everything
+            const uint32_t rc = lds_u32(sb + (8 * nt + g) * RB + kLatent + 16 * w + 4 * c);
+            uint32_t r0, r1;
+            e4m3x4_to_f16x4(rc, r0, r1);
+            mma_f16(accr[nt], qr, r0, r1);
+            sc[nt][0] = p.kv_scale;
+            sc[nt][1] = p.kv_scale;
+          } else {
+            const uint2 rv = lds64(sb + (8 * nt + g) * RB + kRopeOffFp8 + 2 * (16 * w + 4 * c));
+            mma_bf16(accr[nt], qr, rv.x, rv.y);
+            sc[nt][0] = lds_f32(sb + (8 * nt + 2 * c) * RB + kScaleOff + 4 * w);
+            sc[nt][1] = lds_f32(sb + (8 * nt + 2 * c + 1) * RB + kScaleOff + 4 * w);
+          }
         }
 #pragma unroll
         for (int s = 0; s < 8; ++s)
@@ -299,6 +314,10 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
           }
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
+          if (C::kTensor) {  // the RoPE part carries the scale too
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accr[nt][e] *= p.kv_scale;
+          }
           acc[nt][0] = fmaf(acc[nt][0], sc[nt][0], accr[nt][0]);
           acc[nt][1] = fmaf(acc[nt][1], sc[nt][1], accr[nt][1]);
           acc[nt][2] = fmaf(acc[nt][2], sc[nt][0], accr[nt][2]);
@@ -596,8 +615,9 @@ cudaError_t launch_fmt(const DecodeArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, int /*num_sms*/, cudaStream_t s) {
-  return a.kv_format == SMLA_KV_FP8_DS ? launch_fmt<SMLA_KV_FP8_DS>(a, s)
-                                       : launch_fmt<SMLA_KV_BF16>(a, s);
+  if (a.kv_format == SMLA_KV_FP8_DS) return launch_fmt<SMLA_KV_FP8_DS>(a, s);
+  if (a.kv_format == SMLA_KV_FP8_TENSOR) return launch_fmt<SMLA_KV_FP8_TENSOR>(a, s);
+  return launch_fmt<SMLA_KV_BF16>(a, s);
 }
 
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {

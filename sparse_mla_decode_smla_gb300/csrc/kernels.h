@@ -28,6 +28,7 @@ struct DecodeArgs {
   int64_t num_pages;
   int32_t num_splits, split_len;
   float c2;  // sm_scale * log2(e)
+  float kv_scale;  // per-tensor scale (SMLA_KV_FP8_TENSOR)
 };
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t s);
@@ -36,7 +37,7 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);
 
 // The tensor-core pair kernel serves the fp8_ds cache with at least this many heads.
 constexpr int kTcMinHeads = 64;
-cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, const void* latent,
+cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, float kv_scale, const void* latent,
                         const void* rope, const int64_t* slot_mapping, int64_t n, void* kv,
                         int64_t num_slots, cudaStream_t s);
 cudaError_t launch_gather_dequant(const DecodeArgs& a, float* rows, cudaStream_t s);

@@ -60,11 +60,15 @@ smla_status check_desc(const smla_desc* d) {
   if (!is_pow2(d->page_size) || d->page_size > 4096) return SMLA_ERR_SHAPE;
   if (d->num_pages < 1 || d->page_table_stride < 1) return SMLA_ERR_SHAPE;
   if (d->num_pages > (int64_t(1) << 31)) return SMLA_ERR_SHAPE;
-  if (d->kv_format != SMLA_KV_BF16 && d->kv_format != SMLA_KV_FP8_DS) return SMLA_ERR_UNSUPPORTED;
+  if (d->kv_format != SMLA_KV_BF16 && d->kv_format != SMLA_KV_FP8_DS &&
+      d->kv_format != SMLA_KV_FP8_TENSOR)
+    return SMLA_ERR_UNSUPPORTED;
   if (!isfinite(d->sm_scale)) return SMLA_ERR_SHAPE;
+  if (d->kv_format == SMLA_KV_FP8_TENSOR && !(isfinite(d->kv_scale) && d->kv_scale > 0.f))
+    return SMLA_ERR_SHAPE;
   if (d->num_splits < 0 || d->num_splits > smla::kMaxSplits) return SMLA_ERR_SHAPE;
   if (d->topk > smla::kMaxSplits * smla::kMaxSplitLen) return SMLA_ERR_SHAPE;
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 3; ++i)
     if (d->reserved[i] != 0) return SMLA_ERR_SHAPE;
   return SMLA_OK;
 }
@@ -144,6 +148,7 @@ smla::DecodeArgs make_args(const smla_desc* d, const void* q, const void* kv,
   a.kv_format = d->kv_format;
   a.num_pages = d->num_pages;
   a.c2 = d->sm_scale * 1.4426950408889634f;
+  a.kv_scale = d->kv_format == SMLA_KV_FP8_TENSOR ? d->kv_scale : 1.f;
   return a;
 }
 
@@ -166,7 +171,7 @@ const char* smla_status_string(int32_t s) {
   }
 }
 
-int32_t smla_abi_version(void) { return 1; }
+int32_t smla_abi_version(void) { return 2; }
 
 smla_status smla_workspace_size(const smla_desc* d, size_t* bytes) {
   if (!bytes) return SMLA_ERR_NULL;
@@ -239,8 +244,28 @@ smla_status smla_pack_kv(int32_t kv_format, int32_t scale_mode, const void* late
   int sms = 0;
   smla_status st = current_device(&sms);
   if (st != SMLA_OK) return st;
-  if (smla::launch_pack(kv_format, scale_mode, latent, rope, slot_mapping, n, kv_cache, num_slots,
+  if (smla::launch_pack(kv_format, scale_mode, 1.f, latent, rope, slot_mapping, n, kv_cache, num_slots,
                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+smla_status smla_pack_kv_fp8_tensor(const void* latent, const void* rope,
+                                    const int64_t* slot_mapping, int64_t n, float kv_scale,
+                                    void* kv_cache, int64_t num_slots, void* stream) {
+  if (!(isfinite(kv_scale) && kv_scale > 0.f)) return SMLA_ERR_SHAPE;
+  if (n < 0 || num_slots < 0) return SMLA_ERR_SHAPE;
+  if (n == 0) return SMLA_OK;
+  if (!latent || !rope || !slot_mapping || !kv_cache) return SMLA_ERR_NULL;
+  if (!aligned(latent, 16) || !aligned(rope, 16) || !aligned(kv_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return SMLA_ERR_ALIGN;
+  if (n > (int64_t(1) << 36)) return SMLA_ERR_SHAPE;
+  int sms = 0;
+  smla_status st = current_device(&sms);
+  if (st != SMLA_OK) return st;
+  if (smla::launch_pack(SMLA_KV_FP8_TENSOR, SMLA_SCALE_FP32, kv_scale, latent, rope, slot_mapping, n,
+                        kv_cache, num_slots, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return SMLA_ERR_CUDA;
   return SMLA_OK;
 }

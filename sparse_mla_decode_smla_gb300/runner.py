@@ -7,10 +7,10 @@ from __future__ import annotations
 
 import torch
 
-from . import (SMLA_KV_BF16, SMLA_KV_FP8_DS, SMLA_SCALE_POW2, decode, make_desc, pack_kv,
-               workspace_size)
+from . import (SMLA_KV_BF16, SMLA_KV_FP8_DS, SMLA_KV_FP8_TENSOR, SMLA_SCALE_POW2, decode,
+               make_desc, pack_kv, pack_kv_fp8_tensor, workspace_size)
 
-FMT = {"bf16": SMLA_KV_BF16, "fp8_ds": SMLA_KV_FP8_DS}
+FMT = {"bf16": SMLA_KV_BF16, "fp8_ds": SMLA_KV_FP8_DS, "fp8_tensor": SMLA_KV_FP8_TENSOR}
 
 
 def pack_problem_cache(problem, scale_mode: int = SMLA_SCALE_POW2, device="cuda") -> torch.Tensor:
@@ -30,7 +30,10 @@ def pack_problem_cache(problem, scale_mode: int = SMLA_SCALE_POW2, device="cuda"
         lat, rope = lat.to(device), rope.to(device)
         lo = c * CHUNK_SLOTS
         slots = torch.arange(lo, lo + lat.shape[0], dtype=torch.int64, device=device)
-        pack_kv(SMLA_KV_FP8_DS, scale_mode, lat, rope, slots, kv, problem.num_slots)
+        if w.kv_format == "fp8_tensor":
+            pack_kv_fp8_tensor(lat, rope, slots, kv, problem.num_slots, w.kv_scale)
+        else:
+            pack_kv(SMLA_KV_FP8_DS, scale_mode, lat, rope, slots, kv, problem.num_slots)
         del lat, rope, slots
     return kv
 
@@ -51,7 +54,7 @@ class DeviceDecode:
         T, H = w.num_tokens, w.num_heads
         self.desc = make_desc(T, H, w.topk, w.num_requests, w.page_size, problem.num_pages,
                               w.page_table_stride, FMT[w.kv_format], w.sm_scale, next_n=w.next_n,
-                              num_splits=num_splits)
+                              num_splits=num_splits, kv_scale=w.kv_scale)
         ws = workspace_size(self.desc)
         self.workspace = torch.zeros((ws + 255) // 256 * 256 // 4, dtype=torch.int32, device=device)
         self.out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=device)

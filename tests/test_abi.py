@@ -38,17 +38,18 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.smla_abi_version() == 1
+    assert L.smla_abi_version() == 2
     for s in range(9):
         assert smla.status_string(s)
     assert smla.status_string(99) == "unknown status"
 
 
 def test_desc_layout_matches_header():
-    # int32 x6, int64, int32 x2, float, int32, int32[4]; natural alignment
+    # int32 x6, int64, int32 x2, float, int32, float, int32[3]; natural alignment
     assert ctypes.sizeof(smla.smla_desc) == 64
     assert smla.smla_desc.num_pages.offset == 24
-    assert smla.smla_desc.reserved.offset == 48
+    assert smla.smla_desc.kv_scale.offset == 48
+    assert smla.smla_desc.reserved.offset == 52
 
 
 def _desc(**kw):
@@ -114,3 +115,12 @@ def test_kernel_events_hook_needs_both_or_neither(L):
     assert L.smla_set_kernel_events(P(16), None) == 1
     assert L.smla_set_kernel_events(None, P(16)) == 1
     assert L.smla_set_kernel_events(None, None) == 0
+
+
+@pytest.mark.parametrize("kv_scale", [0.0, -1.0, float("nan"), float("inf")])
+def test_per_tensor_fp8_needs_a_positive_finite_scale(L, kv_scale):
+    d = _desc(kv_format=smla.SMLA_KV_FP8_TENSOR)
+    d.kv_scale = kv_scale
+    assert _decode_status(L, d) == 2
+    P = ctypes.c_void_p
+    assert L.smla_pack_kv_fp8_tensor(P(16), P(16), P(16), 4, ctypes.c_float(kv_scale), P(16), 8, None) == 2

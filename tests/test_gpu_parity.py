@@ -131,6 +131,52 @@ def test_gather_dequant_bit_exact(wi):
     assert err.item() == smla.SMLA_DEVERR_INDEX
 
 
+# ------------------------------------------------------------------ per-tensor FP8 cache
+
+TENSOR = W.EXTRA_WORKLOADS[0]  # fp8tensor_T32_H64_K2048_ctx1k-32k
+
+
+@pytest.mark.parametrize("kv_scale", [1.0, 2.0 ** -6, 0.0137])
+def test_pack_fp8_tensor_bit_exact(kv_scale):
+    n, slots = 2000, 2500
+    g = torch.Generator().manual_seed(5)
+    lat = (torch.randn(n, 512, generator=g) * 4).to(torch.bfloat16)
+    rope = (torch.randn(n, 64, generator=g) * 4).to(torch.bfloat16)
+    lat[0, :8] = 1e4  # saturates at +-448
+    mapping = torch.randperm(slots, generator=g)[:n].to(torch.int64)
+    mapping[3] = -1
+    kv = torch.full((slots, 576), 0xAB, dtype=torch.uint8, device="cuda")
+    smla.pack_kv_fp8_tensor(lat.cuda(), rope.cuda(), mapping.cuda(), kv, slots, kv_scale)
+    ref = O.pack_fp8_tensor(_bits(lat), _bits(rope), kv_scale)
+    m = mapping.numpy()
+    ok = m >= 0
+    assert np.array_equal(kv.cpu().numpy()[m[ok]], ref[ok])
+
+
+def test_gather_dequant_fp8_tensor_bit_exact():
+    w = W.small_variant(TENSOR, num_requests=3, ctx_lo=100, ctx_hi=900, topk=320).replace(kv_scale=0.0137)
+    p = W.make_problem(w)
+    kv = pack_problem_cache(p)
+    d = smla.make_desc(w.num_tokens, w.num_heads, w.topk, w.num_requests, w.page_size, p.num_pages,
+                       w.page_table_stride, smla.SMLA_KV_FP8_TENSOR, w.sm_scale, kv_scale=w.kv_scale)
+    rows = torch.full((w.num_tokens, w.topk, 576), 7.0, device="cuda")
+    smla.gather_dequant(d, kv, p.page_table.cuda(), p.topk.cuda(), None, rows)
+    ref = O.gather_dequant(OracleCache(p).fetch, "fp8_tensor", p.page_table.numpy(), p.topk.numpy(),
+                           w.page_size, p.num_pages, kv_scale=w.kv_scale)
+    assert np.array_equal(rows.cpu().double().numpy(), ref)
+
+
+@pytest.mark.parametrize("heads,sink,kv_scale", [(16, False, 1.0), (64, False, 1.0), (128, True, 2.0 ** -6),
+                                                 (64, True, 0.0137)])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_decode_fp8_tensor_matches_oracle(heads, sink, kv_scale, splits):
+    w = W.small_variant(TENSOR, num_requests=3, ctx_lo=200, ctx_hi=800, topk=448).replace(
+        num_heads=heads, sink=sink, kv_scale=kv_scale, name=f"fp8tensor_H{heads}")
+    p = W.make_problem(w)
+    out, lse = DeviceDecode(p, num_splits=splits).run()
+    assert_parity(out, lse, oracle_decode(p))
+
+
 # ------------------------------------------------------------------ decode parity
 
 
