@@ -1,6 +1,7 @@
 // Sparse MLA decode on the 5th-generation tensor cores (tcgen05, TMEM accumulators),
-// for the fp8_ds cache and 64..128 heads. One CTA pair (cluster of 2) per (query token,
-// top-k split).
+// for the FP8 caches (fp8_ds: 656-byte rows with per-128 scales and bf16 RoPE; per-tensor
+// FP8: 576 E4M3 codes with one scale, vLLM PR #43827) and 64..128 heads. One CTA pair
+// (cluster of 2) per (query token, top-k split).
 //
 // What it computes is the sparse decode of vLLM PR #43477 "关键源码片段" (forward_mqa)
 // with the sink and split merge of SGLang PR #24692 "关键文件": out_h = softmax over the
@@ -108,6 +109,9 @@ static_assert(128 * kQRow <= kOffRaw, "q staging fits below the raw ring");
 
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
+// TENS: per-tensor FP8 rows (576 B, one scale) instead of fp8_ds rows (656 B, 4 block
+// scales).
+template <bool TENS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
     decode_tc_kernel(const DecodeArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -121,6 +125,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
 #ifdef SMLA_TRACE
   if (threadIdx.x == 0 && blockIdx.x < 4096) g_span[blockIdx.x][0] = globaltimer_ns();
 #endif
+  // Per-tensor FP8 codes go into the K tile unscaled (exact in bf16) and kv_scale is
+  // applied in fp32 to the scores (bmm1_scale = sm_scale * kv_scale) and to O (bmm2_scale =
+  // kv_scale), the scale algebra of vLLM PR #43827 "关键源码片段".
+  constexpr bool tens = TENS;
+  const float c2 = tens ? p.c2 * p.kv_scale : p.c2;
   const int item = blockIdx.x >> 1;
   const int split = item % p.num_splits;
   const int t = item / p.num_splits;
@@ -257,10 +266,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
       const uint32_t vm = __ballot_sync(0xffffffffu, phys >= 0);
       if (lane == 0) {
         meta[(i % kMetaRing) * kProducersTc + pw] = uint16_t(vm);
-        mbar_arrive_expect_tx(bar(B_RAW_FULL + st), uint32_t(__popc(vm)) * kHalfRow);
+        mbar_arrive_expect_tx(bar(B_RAW_FULL + st), uint32_t(__popc(vm)) * (tens ? 288u : uint32_t(kHalfRow)));
       }
       __syncwarp();
-      if (phys >= 0) {
+      if (tens && phys >= 0) {
+        // latent [256c, 256c+256) and the RoPE codes [32c, 32c+32)
+        const uint8_t* src = p.kv + phys * kFp8TensorRowBytes;
+        const uint32_t dst = sb + uint32_t(kOffRaw) + uint32_t((st * kN + myslot) * kHalfRow);
+        bulk_g2s(dst, src + 256 * crank, 256, bar(B_RAW_FULL + st));
+        bulk_g2s(dst + 256, src + kLatent + 32 * crank, 32, bar(B_RAW_FULL + st));
+      } else if (phys >= 0) {
         const uint8_t* src = p.kv + phys * kFp8RowBytes;
         const uint32_t dst = sb + uint32_t(kOffRaw) + uint32_t((st * kN + myslot) * kHalfRow);
         if (crank == 0) {
@@ -339,7 +354,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
         const int ch = id >> 6, slot = id & 63;  // 16 latent bytes [16ch, 16ch+16) of slot
         const uint32_t rrow = raw + slot * kHalfRow;
         const uint4 v = lds128(rrow + 16 * ch);
-        const float sc = lds_f32(rrow + 256 + 4 * (2 * crank + (ch >> 3)));
+        const float sc = tens ? 1.f : lds_f32(rrow + 256 + 4 * (2 * crank + (ch >> 3)));
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[8];
 #pragma unroll
@@ -362,8 +377,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int id = tid + 128 * k;
-        const int rc = id >> 6, slot = id & 63;
-        const uint4 v = lds128(raw + slot * kHalfRow + 272 + 16 * rc);
+        const int rc = id >> 6, slot = id & 63;  // RoPE dims [8rc, 8rc+8) of slot
+        uint4 v;
+        if constexpr (tens) {  // eight E4M3 codes -> bf16 (exact; the scale comes later in fp32)
+          const uint2 cw = lds64(raw + slot * kHalfRow + 256 + 8 * rc);
+          uint32_t h[4];
+          e4m3x4_to_f16x4(cw.x, h[0], h[1]);
+          e4m3x4_to_f16x4(cw.y, h[2], h[3]);
+          uint32_t o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[q]));
+            o[q] = pack_bf16x2(f.x, f.y);
+          }
+          v = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+          v = lds128(raw + slot * kHalfRow + 272 + 16 * rc);
+        }
         const uint32_t dst = kt + 4 * kPanel + slot * 64 + ((rc ^ ((slot >> 1) & 3)) << 4);
         asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
                      "r"(v.w) : "memory");
@@ -374,7 +404,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
         mbar_arrive(bar(B_K_FULL + b));
         mbar_arrive(bar(B_RAW_EMPTY + st));
       }
-    }    // all K tiles are dequantised: the split merge, if one follows, may start launching
+    }
+    // all K tiles are dequantised: the split merge, if one follows, may start launching
     if (tid == 0) pdl_trigger();
   }
   // ------------------------------------------------------------------ softmax + epilogue
@@ -454,7 +485,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j = 4 * k + e;
-            const float v = ((msk >> j) & 1ull) ? (s[j] + xs4[e]) * p.c2 : -CUDART_INF_F;
+            const float v = ((msk >> j) & 1ull) ? (s[j] + xs4[e]) * c2 : -CUDART_INF_F;
             s[j] = v;
             mx = fmaxf(mx, v);
           }
@@ -503,7 +534,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
       if (owner) {
         const float lse0 = l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
         float lse_out = lse0;
-        f = l > 0.f ? 1.f / l : 0.f;
+        f = l > 0.f ? (tens ? p.kv_scale : 1.f) / l : 0.f;
         if (S == 1 && p.sink && h < p.H) {
           const float sg = __ldg(p.sink + h);
           lse_out = fmaxf(lse0, sg) + log1pf(expf(-fabsf(lse0 - sg)));
@@ -591,13 +622,18 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemTc));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemTc));
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
   const int64_t grid = int64_t(a.T) * a.num_splits * 2;
-  decode_tc_kernel<<<static_cast<unsigned>(grid), kThreadsTc, kSmemTc, s>>>(a);
+  if (a.kv_format == SMLA_KV_FP8_TENSOR)
+    decode_tc_kernel<true><<<static_cast<unsigned>(grid), kThreadsTc, kSmemTc, s>>>(a);
+  else
+    decode_tc_kernel<false><<<static_cast<unsigned>(grid), kThreadsTc, kSmemTc, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -35,7 +35,7 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);
 
-// The tensor-core pair kernel serves the fp8_ds cache with at least this many heads.
+// The tensor-core pair kernel serves the FP8 caches with at least this many heads.
 constexpr int kTcMinHeads = 64;
 cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, float kv_scale, const void* latent,
                         const void* rope, const int64_t* slot_mapping, int64_t n, void* kv,

@@ -80,7 +80,8 @@ struct Plan {
 };
 
 bool use_tc(const smla_desc* d) {
-  return d->kv_format == SMLA_KV_FP8_DS && d->num_heads >= smla::kTcMinHeads;
+  return (d->kv_format == SMLA_KV_FP8_DS || d->kv_format == SMLA_KV_FP8_TENSOR) &&
+         d->num_heads >= smla::kTcMinHeads;
 }
 
 Plan make_plan(const smla_desc* d, int num_sms) {

@@ -61,7 +61,7 @@ class DeviceDecode:
         self.lse = torch.empty((T, H), dtype=torch.float32, device=device) if with_lse else None
         # the decode kernel the library dispatches to for this batch (the fp8_ds cache with
         # 64 or more heads takes the tensor-core pair kernel)
-        self.kernel_name = ("decode_tc_kernel" if w.kv_format == "fp8_ds" and H >= 64
+        self.kernel_name = ("decode_tc_kernel" if w.kv_format in ("fp8_ds", "fp8_tensor") and H >= 64
                             else "decode_mma_kernel")
 
     def run(self, stream=None):
