@@ -12,7 +12,13 @@
 // [32c, 32c+32): it gathers only those bytes of each row, scores all 128 heads over its 288
 // dims, and accumulates its 256 output dims. The two partial score rows of a head are
 // summed by the CTA that owns the head (heads [64c, 64c+64)), which runs the softmax and
-// sends the bf16 probabilities back, so both halves of PV use identical P.
+// sends the probabilities back, so both halves of PV use identical P.
+//
+// The MMAs run on f16 operands with fp32 accumulation. An E4M3 code converts to f16
+// exactly in one instruction, and the block scale applies with one f16 multiply: exact for
+// power-of-two scales and within 2^-11 otherwise, finer than bf16's 2^-8. q converts from
+// bf16 exactly. The price is f16's range: dequantised keys and q must stay within
+// +-65504 (for power-of-two block scales, a block's largest magnitude within 57344).
 //
 // Per CTA (416 threads):
 //  * warps 8-11, producers (16 slots of every tile each): the split's index list by one
@@ -20,11 +26,11 @@
 //    half of each valid row (256 latent bytes, the 4 scales, 32 RoPE values = 336 bytes)
 //    as two bulk copies into a 3-stage ring. Bulk copies issued by one warp serialise on
 //    the TMA engine; four issuing warps keep the gather near the per-SM limit.
-//  * warps 0-3, dequant: e4m3 * scale -> bf16, written as the swizzled K tile [64 slots x
+//  * warps 0-3, dequant: e4m3 * scale -> f16, written as the swizzled K tile [64 slots x
 //    288 dims]: four 128-byte-swizzled latent panels and a 64-byte-swizzled RoPE panel
 //    (two buffers). The same bytes serve as B of QK (K-major) and
 //    as B of PV (MN-major view of the 256 latent dims).
-//  * warp 12, MMA issuer (one thread): QK = 18 x tcgen05.mma M128 N64 K16 with q (bf16) as
+//  * warp 12, MMA issuer (one thread): QK = 18 x tcgen05.mma M128 N64 K16 with q (f16) as
 //    the A operand in TMEM; PV = 4 x tcgen05.mma M128 N256 K16 with P from shared memory.
 //    QK of tile i+1 is issued before PV of tile i, so scores are ready when softmax needs them.
 //  * warps 4-7, softmax: thread h owns TMEM lane h (head h). Non-owners send their partial
@@ -69,7 +75,7 @@ constexpr int kHalfRow = 336;      // 256 latent + 16 scales + 64 RoPE bytes
 constexpr int kPanel = kN * 128;   // one 64-dim 128-byte-swizzled panel of a tile: 8 KB
 constexpr int kRopePanel = kN * 64;  // the CTA's 32 RoPE dims, 64-byte swizzle: 4 KB
 constexpr int kKtile = 4 * kPanel + kRopePanel;  // 4 latent panels + the RoPE panel
-constexpr int kPtile = 128 * 128;  // P [128 heads x 64 slots] bf16
+constexpr int kPtile = 128 * 128;  // P [128 heads x 64 slots] f16
 constexpr int kXsRow = 272;        // 64 fp32 + padding (conflict-free row reads)
 constexpr int kXs = 64 * kXsRow;
 constexpr int kMetaRing = 8;
@@ -81,7 +87,7 @@ constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 // TMEM columns (512 allocated)
 constexpr uint32_t kTmO = 0;    // O_c [128 x 256] fp32
-constexpr uint32_t kTmQ = 256;  // q_c [128 x 288] bf16: 144 columns
+constexpr uint32_t kTmQ = 256;  // q_c [128 x 288] f16: 144 columns
 constexpr uint32_t kTmS = 448;  // S [128 x 64] fp32
 
 constexpr size_t kOffKtile = 0;
@@ -125,7 +131,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
 #ifdef SMLA_TRACE
   if (threadIdx.x == 0 && blockIdx.x < 4096) g_span[blockIdx.x][0] = globaltimer_ns();
 #endif
-  // Per-tensor FP8 codes go into the K tile unscaled (exact in bf16) and kv_scale is
+  // Per-tensor FP8 codes go into the K tile unscaled (exact in f16) and kv_scale is
   // applied in fp32 to the scores (bmm1_scale = sm_scale * kv_scale) and to O (bmm2_scale =
   // kv_scale), the scale algebra of vLLM PR #43827 "关键源码片段".
   constexpr bool tens = TENS;
@@ -200,7 +206,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
       for (int k = 0; k < 4; ++k) {
         uint4 v = make_uint4(0, 0, 0, 0);
         if (have && got) v = lds128(qs + 16 * (4 * ch + k));
-        wv[4 * k] = v.x; wv[4 * k + 1] = v.y; wv[4 * k + 2] = v.z; wv[4 * k + 3] = v.w;
+        // the MMAs run on f16 operands: bf16 -> f16 (exact within f16's range)
+        wv[4 * k] = bf16x2_to_f16x2(v.x); wv[4 * k + 1] = bf16x2_to_f16x2(v.y);
+        wv[4 * k + 2] = bf16x2_to_f16x2(v.z); wv[4 * k + 3] = bf16x2_to_f16x2(v.w);
       }
       tc::st16(lrow + 16 * ch, wv);
     }
@@ -295,8 +303,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
   // ------------------------------------------------------------------ MMA issuer
   else if (warp == kMmaWarp) {
     if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t kIdQK = tc::idesc_bf16_f32(128, kN, false, false);
-      constexpr uint32_t kIdPV = tc::idesc_bf16_f32(128, 256, false, true);
+      constexpr uint32_t kIdQK = tc::idesc_f16_f32(128, kN, false, false);
+      constexpr uint32_t kIdPV = tc::idesc_f16_f32(128, 256, false, true);
       auto qk = [&](int i) -> bool {
         const int b = i & 1;
         if (!mbar_wait(bar(B_K_FULL + b), (i >> 1) & 1)) return false;
@@ -357,14 +365,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
         const float sc = tens ? 1.f : lds_f32(rrow + 256 + 4 * (2 * crank + (ch >> 3)));
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[8];
+        const __half2 s2 = __float2half2_rn(sc);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t lo, hi;
-          e4m3x4_to_f16x4(wv[q], lo, hi);
-          const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&lo));
-          const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-          o[2 * q] = pack_bf16x2(f0.x * sc, f0.y * sc);
-          o[2 * q + 1] = pack_bf16x2(f1.x * sc, f1.y * sc);
+          e4m3x4_to_f16x4(wv[q], lo, hi);  // exact
+          if constexpr (tens) {  // the scale comes later, in fp32
+            o[2 * q] = lo;
+            o[2 * q + 1] = hi;
+          } else {  // code * scale in f16 (exact for power-of-two scales in f16's range)
+            __half2 a = __hmul2(*reinterpret_cast<const __half2*>(&lo), s2);
+            __half2 b = __hmul2(*reinterpret_cast<const __half2*>(&hi), s2);
+            o[2 * q] = *reinterpret_cast<uint32_t*>(&a);
+            o[2 * q + 1] = *reinterpret_cast<uint32_t*>(&b);
+          }
         }
         const uint32_t row = kt + (ch >> 2) * kPanel + slot * 128;
         const int c0 = 2 * (ch & 3);
@@ -379,20 +393,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
         const int id = tid + 128 * k;
         const int rc = id >> 6, slot = id & 63;  // RoPE dims [8rc, 8rc+8) of slot
         uint4 v;
-        if constexpr (tens) {  // eight E4M3 codes -> bf16 (exact; the scale comes later in fp32)
+        if constexpr (tens) {  // eight E4M3 codes -> f16 (exact; the scale comes later in fp32)
           const uint2 cw = lds64(raw + slot * kHalfRow + 256 + 8 * rc);
           uint32_t h[4];
           e4m3x4_to_f16x4(cw.x, h[0], h[1]);
           e4m3x4_to_f16x4(cw.y, h[2], h[3]);
-          uint32_t o[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[q]));
-            o[q] = pack_bf16x2(f.x, f.y);
-          }
-          v = make_uint4(o[0], o[1], o[2], o[3]);
-        } else {
-          v = lds128(raw + slot * kHalfRow + 272 + 16 * rc);
+          v = make_uint4(h[0], h[1], h[2], h[3]);
+        } else {  // bf16 RoPE -> f16
+          const uint4 r = lds128(raw + slot * kHalfRow + 272 + 16 * rc);
+          v = make_uint4(bf16x2_to_f16x2(r.x), bf16x2_to_f16x2(r.y), bf16x2_to_f16x2(r.z),
+                         bf16x2_to_f16x2(r.w));
         }
         const uint32_t dst = kt + 4 * kPanel + slot * 64 + ((rc ^ ((slot >> 1) & 3)) << 4);
         asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
@@ -503,7 +513,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
         for (int j = 0; j < 32; ++j) {
           const float p0 = exp2f(s[2 * j] - base), p1 = exp2f(s[2 * j + 1] - base);
           sum += p0 + p1;
-          pw[j] = pack_bf16x2(p0, p1);
+          pw[j] = pack_f16x2(p0, p1);
         }
         l = l * a + sum;
         const uint32_t prow_l = sb + uint32_t(kOffPtile + b * kPtile + h * 128);

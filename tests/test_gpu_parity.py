@@ -134,18 +134,14 @@ def test_gather_dequant_bit_exact(wi):
 @pytest.mark.parametrize("wi", [2, 4])
 def test_decode_fp32_block_scales(wi):
     # fp8_ds rows packed with fp32 block scales (amax / 448, not powers of two). The
-    # 16-head path folds the scale into fp32 partial scores and meets every tolerance. The
-    # tensor-core path rounds code * scale to the bf16 MMA operand: exact for
-    # power-of-two scales, up to 2^-9 relative otherwise, which moves the LSE by a few
-    # 1e-4 to 1e-3. There the output tolerances stand and the LSE bound is 4e-3.
+    # 16-head path folds the scale into fp32 partial scores; the tensor-core path rounds
+    # code * scale to its f16 MMA operand (within 2^-11 relative). Both meet every
+    # tolerance.
     w = SMALL[wi]
     p = W.make_problem(w)
     out, lse = DeviceDecode(p, scale_mode=smla.SMLA_SCALE_FP32).run()
     ref = oracle_decode(p, scale_mode=O.SCALE_FP32)
-    if w.num_heads >= 64:
-        assert_parity(out, lse, ref, lse_atol=4e-3)
-    else:
-        assert_parity(out, lse, ref)
+    assert_parity(out, lse, ref)
 
 
 # ------------------------------------------------------------------ per-tensor FP8 cache
