@@ -360,6 +360,38 @@ def test_mixed_batch_one_call(wi):
     assert_parity(out, lse, ref)
 
 
+@pytest.mark.parametrize("page_size", [1, 16, 256])
+def test_decode_other_page_sizes(page_size):
+    w = W.small_variant(W.WORKLOADS[2], num_requests=2, ctx_lo=600, ctx_hi=900, topk=320).replace(
+        page_size=page_size, name=f"fp8_P{page_size}")
+    p = W.make_problem(w)
+    assert_parity(*DeviceDecode(p).run(), oracle_decode(p))
+
+
+@pytest.mark.parametrize("wi,splits", [(1, 0), (1, 8), (4, 0), (2, 5)])
+def test_decode_long_index_rows(wi, splits):
+    # 8192 entries per row: more than one split's 2048-entry index list, so at least 4 splits
+    w = W.small_variant(W.WORKLOADS[wi], num_requests=1, ctx_lo=9000, ctx_hi=9000, topk=8192,
+                        tail_pad=1000 if wi == 4 else 0)
+    p = W.make_problem(w)
+    assert_parity(*DeviceDecode(p, num_splits=splits).run(), oracle_decode(p))
+
+
+@pytest.mark.parametrize("heads", [64, 128])
+def test_decode_bf16_cache_many_heads(heads):
+    w = W.WORKLOADS[0].replace(num_heads=heads, name=f"bf16_H{heads}")
+    p = W.make_problem(w)
+    for splits in (1, 2):
+        assert_parity(*DeviceDecode(p, num_splits=splits).run(), oracle_decode(p))
+
+
+@pytest.mark.parametrize("wi", [1, 2])
+def test_decode_two_tokens_per_request(wi):
+    w = W.small_variant(W.WORKLOADS[wi], num_requests=2, ctx_lo=300, ctx_hi=700, topk=256).replace(next_n=2)
+    p = W.make_problem(w)
+    assert_parity(*DeviceDecode(p).run(), oracle_decode(p))
+
+
 # ------------------------------------------------------------------ full-size, sampled
 
 
