@@ -187,6 +187,15 @@ smla_status smla_gather_dequant(const smla_desc* d, const void* kv_cache,
                                 int32_t* error_word, void* stream);
 
 /*
+ * Self-test of the failure path (the pages have no counterpart): launches one warp that
+ * waits, with the same bounded mbarrier wait every pipeline stage of smla_decode uses, on
+ * a barrier that nothing will complete. After limit_us microseconds (1..100000) the wait
+ * gives up, sets SMLA_DEVERR_TIMEOUT in *error_word (a device int32) and the kernel returns,
+ * as a stalled decode CTA would; the GPU context stays usable. Nothing faults or hangs.
+ */
+smla_status smla_selftest_wait_timeout(int32_t* error_word, uint32_t limit_us, void* stream);
+
+/*
  * Synchronises `stream`, copies the device error word of `workspace` into
  * *error_word and clears it. Returns SMLA_ERR_INDEX_RANGE when any bit was set.
  */

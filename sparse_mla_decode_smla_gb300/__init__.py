@@ -19,13 +19,14 @@ SMLA_SCALE_POW2 = 0
 SMLA_SCALE_FP32 = 1
 SMLA_DEVERR_INDEX = 1
 SMLA_DEVERR_PAGE = 2
+SMLA_DEVERR_TIMEOUT = 4
 
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_NULL", 2: "SMLA_ERR_SHAPE", 3: "SMLA_ERR_ALIGN",
           4: "SMLA_ERR_UNSUPPORTED", 5: "SMLA_ERR_WORKSPACE", 6: "SMLA_ERR_CUDA",
           7: "SMLA_ERR_INDEX_RANGE", 8: "SMLA_ERR_DEVICE"}
 EXPORTS = ["smla_status_string", "smla_abi_version", "smla_workspace_size", "smla_decode",
            "smla_pack_kv", "smla_gather_dequant", "smla_read_error", "smla_decode_noalloc",
-           "smla_set_kernel_events", "smla_pack_kv_fp8_tensor"]
+           "smla_set_kernel_events", "smla_pack_kv_fp8_tensor", "smla_selftest_wait_timeout"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -75,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.smla_decode_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P]
         L.smla_set_kernel_events.restype = I32
         L.smla_set_kernel_events.argtypes = [P, P]
+        L.smla_selftest_wait_timeout.restype = I32
+        L.smla_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P]
         L.smla_read_error.restype = I32
         L.smla_read_error.argtypes = [D, P, SZ, ctypes.POINTER(I32), P]
         _lib = L
@@ -169,6 +172,12 @@ def gather_dequant(desc, kv_cache, page_table, topk, req_id_per_token, rows, err
     _check("smla_gather_dequant", lib().smla_gather_dequant(
         ctypes.byref(desc), _ptr(kv_cache), _ptr(page_table), _ptr(topk), _ptr(req_id_per_token),
         _ptr(rows), _ptr(error_word), _stream(stream)))
+
+
+def selftest_wait_timeout(error_word, limit_us: int, stream=None):
+    """Run the bounded-wait self-test: error_word (device int32) gets SMLA_DEVERR_TIMEOUT."""
+    _check("smla_selftest_wait_timeout", lib().smla_selftest_wait_timeout(
+        _ptr(error_word), int(limit_us), _stream(stream)))
 
 
 def read_error(desc, workspace, stream=None) -> int:

@@ -205,6 +205,22 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(DecodeArgs a, float
   *reinterpret_cast<float2*>(dst + kLatent + 2 * lane) = make_float2(rp0, rp1);
 }
 
+// One warp waits, with the kernels' own bounded wait, on an mbarrier that nothing will
+// complete; when the limit runs out it sets SMLA_DEVERR_TIMEOUT and returns, as a pipeline
+// CTA does. Tests the timeout path without faulting or hanging anything.
+__global__ void __launch_bounds__(32) selftest_wait_kernel(int32_t* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) mbar_init(b, 1);  // one arrival expected, none will come
+  __syncwarp();
+  if (!mbar_wait_for(b, 0, limit_ns) && threadIdx.x == 0) atomicOr(err, SMLA_DEVERR_TIMEOUT);
+}
+
+cudaError_t launch_selftest_wait(int32_t* err, uint64_t limit_ns, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather_dequant(const DecodeArgs& a, float* rows, cudaStream_t s) {
   const int64_t items = static_cast<int64_t>(a.T) * a.K;
   const int64_t blocks = (items * 32 + 255) / 256;

@@ -179,14 +179,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Every pipeline wait gives up after this long and reports SMLA_DEVERR_TIMEOUT.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-// Bounded wait for the phase of `bar` with the given parity; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Bounded wait for the phase of `bar` with the given parity; false once `limit_ns` passed.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+// The pipeline wait of every kernel: bounded by kWaitLimitNs; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 // Untiled bulk copy global -> shared (TMA engine), completing `bytes` on `bar`.

@@ -41,5 +41,6 @@ cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, float kv_scale, c
                         const void* rope, const int64_t* slot_mapping, int64_t n, void* kv,
                         int64_t num_slots, cudaStream_t s);
 cudaError_t launch_gather_dequant(const DecodeArgs& a, float* rows, cudaStream_t s);
+cudaError_t launch_selftest_wait(int32_t* err, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace smla

@@ -293,6 +293,19 @@ smla_status smla_gather_dequant(const smla_desc* d, const void* kv_cache,
   return SMLA_OK;
 }
 
+smla_status smla_selftest_wait_timeout(int32_t* error_word, uint32_t limit_us, void* stream) {
+  if (!error_word) return SMLA_ERR_NULL;
+  if (!aligned(error_word, 4)) return SMLA_ERR_ALIGN;
+  if (limit_us < 1 || limit_us > 100000) return SMLA_ERR_SHAPE;
+  int sms = 0;
+  smla_status st = current_device(&sms);
+  if (st != SMLA_OK) return st;
+  if (smla::launch_selftest_wait(error_word, uint64_t(limit_us) * 1000u, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
 smla_status smla_read_error(const smla_desc* d, void* workspace, size_t workspace_bytes,
                             int32_t* error_word, void* stream) {
   (void)d;

@@ -124,3 +124,10 @@ def test_per_tensor_fp8_needs_a_positive_finite_scale(L, kv_scale):
     assert _decode_status(L, d) == 2
     P = ctypes.c_void_p
     assert L.smla_pack_kv_fp8_tensor(P(16), P(16), P(16), 4, ctypes.c_float(kv_scale), P(16), 8, None) == 2
+
+
+def test_selftest_wait_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    assert L.smla_selftest_wait_timeout(None, 10, None) == 1
+    assert L.smla_selftest_wait_timeout(P(16), 0, None) == 2
+    assert L.smla_selftest_wait_timeout(P(16), 200000, None) == 2

@@ -392,6 +392,22 @@ def test_decode_two_tokens_per_request(wi):
     assert_parity(*DeviceDecode(p).run(), oracle_decode(p))
 
 
+def test_bounded_wait_runs_out_and_reports():
+    # a wait that nothing completes gives up after its limit, sets the timeout bit and
+    # returns; the context stays usable for the next decode
+    import time
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    smla.selftest_wait_timeout(err, 2000)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert err.item() == smla.SMLA_DEVERR_TIMEOUT
+    assert 0.002 <= dt < 1.0
+    p = W.make_problem(SMALL[1])
+    assert_parity(*DeviceDecode(p).run(), oracle_decode(p))
+
+
 # ------------------------------------------------------------------ full-size, sampled
 
 
