@@ -148,6 +148,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
   const int nidx = max(0, j1 - j0);
   const int ntiles = req_ok ? (nidx + kN - 1) / kN : 0;
 
+  // Producer lanes (warps 8..11, slots [16 pw, 16 pw + 16) of every tile) fetch their slot's
+  // index kIdxAhead tiles ahead and, once that has landed, its page-table entry kAheadTc
+  // tiles ahead, both by 4-byte cp.async. Every ring step commits one group {index of tile
+  // i+kIdxAhead, page entry of tile i+kAheadTc}; the steps before tile 0 only prime the two
+  // rings, and they run first thing, so the first dependent round trips overlap the set-up.
+  const bool producer = warp >= 8 && warp < kMmaWarp;
+  const int pw = warp - 8;
+  const bool act = lane < kN / kProducersTc;
+  const int myslot = (kN / kProducersTc) * pw + lane;
+  int32_t* sidx = reinterpret_cast<int32_t*>(sm + kOffIdx);    // index ring
+  int32_t* spage = reinterpret_cast<int32_t*>(sm + kOffPages);  // page-table entry ring
+  auto in_split = [&](int tile) { return act && tile < ntiles && tile * kN + myslot < nidx; };
+  auto idx_of = [&](int tile) -> int32_t {
+    return in_split(tile) ? sidx[(tile % kIdxRing) * kN + myslot] : -1;
+  };
+  auto ring_step = [&](int i) {
+    cp_async_wait<kIdxAhead - kAheadTc - 1>();  // the group that fetched index i+kAheadTc
+    const int tp = i + kAheadTc;
+    if (tp >= 0) {
+      const int32_t idx = idx_of(tp);
+      if (idx >= 0 && (idx >> p.log2_page) < p.stride)
+        cp_async4(smem_u32(spage + (tp % kPageRingTc) * kN + myslot), pt_row + (idx >> p.log2_page));
+    }
+    const int ti = i + kIdxAhead;
+    if (in_split(ti))
+      cp_async4(smem_u32(sidx + (ti % kIdxRing) * kN + myslot), idx_row + j0 + ti * kN + myslot);
+    cp_async_commit();
+  };
+  if (producer)
+    for (int i = -kIdxAhead; i < 0; ++i) ring_step(i);
+
   // ------------------------------------------------------------------ set-up
   {
     uint4* z = reinterpret_cast<uint4*>(sm + kOffRaw);
@@ -223,35 +254,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1)
 
   bool ok = true;
   // ------------------------------------------------------------------ producer
-  if (warp >= 8 && warp < kMmaWarp) {
-    const int pw = warp - 8;                 // slots [16 pw, 16 pw + 16) of every tile
-    const bool act = lane < kN / kProducersTc;
-    const int myslot = (kN / kProducersTc) * pw + lane;
-    int32_t* sidx = reinterpret_cast<int32_t*>(sm + kOffIdx);    // index ring
-    int32_t* spage = reinterpret_cast<int32_t*>(sm + kOffPages);  // page-table entry ring
+  if (producer) {
     uint16_t* meta = reinterpret_cast<uint16_t*>(sm + kOffMeta);
-    // Each lane fetches its own slot's index kIdxAhead tiles ahead and, once that has
-    // landed, its page-table entry kAheadTc tiles ahead, both by 4-byte cp.async. Every
-    // iteration commits one group {index of tile i+kIdxAhead, page entry of tile
-    // i+kAheadTc}; iterations before tile 0 only prime the two rings.
-    auto in_split = [&](int tile) { return act && tile < ntiles && tile * kN + myslot < nidx; };
-    auto idx_of = [&](int tile) -> int32_t {
-      return in_split(tile) ? sidx[(tile % kIdxRing) * kN + myslot] : -1;
-    };
     int issued = 0;
-    for (int i = -kIdxAhead; i < ntiles && ok; ++i) {
-      cp_async_wait<kIdxAhead - kAheadTc - 1>();  // the group that fetched index i+kAheadTc
-      const int tp = i + kAheadTc;
-      if (tp >= 0) {
-        const int32_t idx = idx_of(tp);
-        if (idx >= 0 && (idx >> p.log2_page) < p.stride)
-          cp_async4(smem_u32(spage + (tp % kPageRingTc) * kN + myslot), pt_row + (idx >> p.log2_page));
-      }
-      const int ti = i + kIdxAhead;
-      if (in_split(ti))
-        cp_async4(smem_u32(sidx + (ti % kIdxRing) * kN + myslot), idx_row + j0 + ti * kN + myslot);
-      cp_async_commit();
-      if (i < 0) continue;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      ring_step(i);
       const int st = i % kStagesTc;
       if (!mbar_wait(bar(B_RAW_EMPTY + st), ((i / kStagesTc) & 1) ^ 1)) {
         ok = false;
