@@ -65,6 +65,7 @@ TRAFFIC = {
 }
 KERNEL_SOURCES = {
     "decode_tc_kernel": ("common.cuh", "kernels.h", "tcgen05.cuh", "decode_tc.cu"),
+    "decode_hg_kernel": ("common.cuh", "kernels.h", "tcgen05.cuh", "decode_hg.cu"),
     "decode_mma_kernel": ("common.cuh", "kernels.h", "decode_mma.cu"),
 }
 

@@ -209,6 +209,23 @@ __device__ __forceinline__ void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
+// Named barrier over `count` threads that also ANDs a predicate across them: every
+// participant gets true only if all passed true.
+__device__ __forceinline__ bool named_bar_and(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+// Arrive on a named barrier without waiting (the waiting side uses named_bar).
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+
 // Physical slot of a request-local index, or -1 (padding / invalid; invalid entries
 // also set a bit of *err when err != nullptr).
 __device__ __forceinline__ int64_t translate_index(int32_t idx, const int32_t* __restrict__ pt_row,

@@ -1,0 +1,683 @@
+// Sparse MLA decode on the 5th-generation tensor cores (tcgen05, TMEM accumulators) for the
+// FP8 caches (fp8_ds: 656-byte rows with per-128 scales and bf16 RoPE; per-tensor FP8: 576
+// E4M3 codes with one scale, vLLM PR #43827), one CTA per (query token, top-k split, group
+// of 64 heads).
+//
+// What it computes is the sparse decode of vLLM PR #43477 "关键源码片段" (forward_mqa) with
+// the sink and split merge of SGLang PR #24692 "关键文件": out_h = softmax over the selected
+// slots of sm_scale * <q_h, k_j>, applied to v_j = k_j[0:512].
+//
+// Why one CTA holds a whole head group: the fp32 output of 64 heads x 512 dims is 128 KB,
+// half of an SM's tensor memory, if the two halves of each head's 512 dims are stacked on
+// the 128 TMEM lanes: lane l < 64 holds head l's dims [0, 256), lane 64 + l its dims
+// [256, 512), in 256 columns. q is stacked the same way (lane l < 64: dims [0, 256) of
+// head l; lane 64 + l: dims [256, 512)), so QK needs no exchange between SMs:
+//  * QK of a 32-slot tile: B stacks the same slots twice, rows 0-31 with dims [0, 256) and
+//    rows 32-63 with dims [256, 512). Lane l < 64, columns 0-31 of the M128 N64 result are
+//    the low partial scores of head l; lane 64 + l, columns 32-63, the high ones (the other
+//    two quadrants are unused). The 64 RoPE dims are split the same way, with q's RoPE part
+//    as an A operand in shared memory. 18 x M128 N64 K16 per tile.
+//  * The two partial rows of a head meet in shared memory: the warp of lane quarter w and
+//    the warp of quarter w ^ 2 hold heads 32(w & 1) .. 32(w & 1) + 31, low and high. Both
+//    add the two rows in the same order, so both see bit-identical scores, maxima and
+//    rescale factors; each writes the probabilities of 16 of the 32 slots.
+//  * PV: A = [P; 0] against the latent dims [0, 256) of the tile and A = [0; P] against dims
+//    [256, 512), both into the same 256 TMEM columns, so lanes 0-63 accumulate the low
+//    output dims and lanes 64-127 the high ones. 4 x M128 N256 K16 per tile.
+// Half of each MMA's rows or columns are unused: 64 heads fill only half of an M = 128
+// tile. In exchange the head group needs one SM, not two, and no traffic between SMs.
+//
+// The MMAs run on f16 operands with fp32 accumulation: an E4M3 code converts to f16 exactly,
+// and the block scale applies with one f16 multiply (exact for power-of-two scales, within
+// 2^-11 otherwise); q converts from bf16 exactly. Dequantised keys and q must stay within
+// f16's range (+-65504).
+//
+// Per CTA (480 threads):
+//  * warps 12-13, producers (16 slots of every tile each): index entries twelve tiles ahead
+//    and page-table entries six tiles ahead by 4-byte cp.async, then each valid row by one
+//    bulk copy (TMA engine) into a 3-stage ring.
+//  * warps 4-11, dequant: e4m3 (* scale) -> f16 into the K tile: four 128-byte-swizzled
+//    blocks of [32 slots x 64 low dims | 32 slots x 64 high dims] and a 64-byte-swizzled
+//    RoPE block (3 buffers). The same bytes are B of QK (K-major) and B of PV (MN-major).
+//  * warp 14, MMA issuer (one thread). QK of tile i+2 follows PV of tile i; two score
+//    buffers let QK run while the softmax of the previous tile does.
+//  * warps 0-3, softmax and epilogue: base-2 online softmax with lazy rescaling (the running
+//    max moves only when it grows by more than 8, as in FlashAttention-4).
+// Every wait is bounded in time; a wait that gives up sets SMLA_DEVERR_TIMEOUT. The two
+// warps of a head pair meet at named barriers that also AND their status, so both leave the
+// tile loop at the same barrier and neither waits for a partner that has left.
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+// Optional timeline of the first CTA's pipeline events (compiled in with -DSMLA_TRACE; read
+// back with smla_hgtrace_read). Off in normal builds: the macro expands to nothing.
+#ifdef SMLA_TRACE
+__device__ unsigned long long g_hgtrace[128][12];
+__device__ unsigned long long g_hgspan[4096][2];
+#define HTRACE(ev, tile)                                                                    \
+  do {                                                                                      \
+    if (blockIdx.x == 0 && (tile) < 128) g_hgtrace[(tile)][(ev)] = globaltimer_ns();        \
+  } while (0)
+#else
+#define HTRACE(ev, tile) \
+  do {                   \
+  } while (0)
+#endif
+
+namespace smla {
+namespace {
+
+constexpr int kHgN = 32;                 // slots per tile
+constexpr int kHgFirstDequant = 4;       // warps 0..3: softmax
+constexpr int kHgDequantWarps = 8;
+constexpr int kHgFirstProducer = kHgFirstDequant + kHgDequantWarps;
+constexpr int kHgProducers = 2;
+constexpr int kHgMmaWarp = kHgFirstProducer + kHgProducers;
+constexpr int kHgThreads = 32 * (kHgMmaWarp + 1);
+constexpr int kHgDequantThreads = 32 * kHgDequantWarps;
+constexpr int kHgStages = 3;             // raw-row ring and K tiles
+constexpr int kHgRawRow = kFp8RowBytes;  // a per-tensor row uses its first 576 bytes
+constexpr int kHgRawStage = kHgN * kHgRawRow;
+constexpr int kHgPairBlk = 2 * kHgN * 128;  // [32 slots x 64 low dims | same slots, high dims]
+constexpr int kHgRopeBlk = 2 * kHgN * 64;   // [32 slots x RoPE 0..31 | same slots, 32..63]
+constexpr int kHgKtile = 4 * kHgPairBlk + kHgRopeBlk;
+constexpr int kHgPBlk = 64 * kHgN * 2;      // 64 rows x 32 slots f16, 64-byte swizzle
+constexpr int kHgQrope = 128 * 64;          // q RoPE, [128 rows x 32 dims] f16
+constexpr int kHgXRow = 144;                // 32 fp32 + padding (conflict-free rows)
+constexpr int kHgIdxAhead = 12, kHgIdxRing = 16;
+constexpr int kHgAhead = 6, kHgPageRing = 8;
+constexpr int kHgMetaRing = 16;
+constexpr float kHgRescaleThreshold = 8.f;  // log2 units
+static_assert(kHgIdxAhead <= 2 * kHgAhead && kHgIdxRing > kHgIdxAhead && kHgPageRing > kHgAhead,
+              "index and page rings");
+
+// TMEM columns (512 allocated)
+constexpr uint32_t kHgTmO = 0;    // O [128 lanes x 256] fp32, lanes 64.. = high dims
+constexpr uint32_t kHgTmQ = 256;  // q latent [128 lanes x 256 dims] f16: 128 columns
+constexpr uint32_t kHgTmS = 384;  // two score buffers of 64 columns
+
+constexpr size_t kHgOffK = 0;
+constexpr size_t kHgOffRaw = kHgOffK + size_t(kHgStages) * kHgKtile;
+constexpr size_t kHgOffP = kHgOffRaw + size_t(kHgStages) * kHgRawStage;  // [0 | P0 | 0 | P1 | 0]
+constexpr size_t kHgOffQr = kHgOffP + 5 * size_t(kHgPBlk);
+constexpr size_t kHgOffXs = kHgOffQr + kHgQrope;
+constexpr size_t kHgOffIdx = kHgOffXs + 128 * size_t(kHgXRow);
+constexpr size_t kHgOffPages = kHgOffIdx + size_t(kHgIdxRing) * kHgN * 4;
+constexpr size_t kHgOffMeta = kHgOffPages + size_t(kHgPageRing) * kHgN * 4;
+constexpr size_t kHgOffTmem = kHgOffMeta + kHgMetaRing * 4;
+constexpr size_t kHgOffBars = kHgOffTmem + 16;
+enum {
+  H_RAW_FULL = 0, H_RAW_EMPTY = 3, H_K_FULL = 6, H_K_FREE = 9, H_S_FULL = 12, H_S_FREE = 14,
+  H_P_READY = 16, H_PV_DONE = 18, H_Q = 20, H_DRAIN = 21, H_COUNT = 22
+};
+constexpr size_t kSmemHg = kHgOffBars + H_COUNT * 8 + 1024;  // + alignment slack
+static_assert(kSmemHg <= 232448, "shared memory budget");
+static_assert(kHgOffP % 512 == 0 && kHgOffQr % 512 == 0 && kHgKtile % 1024 == 0 && kHgOffRaw % 1024 == 0,
+              "swizzle atoms: 512-byte (64-byte swizzle) and 1024-byte (128-byte swizzle) aligned");
+// q staging at start-up: 64 rows of 1152 bytes (+16 for conflict-free 16-byte reads) in the
+// K-tile area, which the pipeline first writes after the start-up barrier
+constexpr uint32_t kHgQRow = 1168;
+static_assert(64 * kHgQRow <= kHgOffRaw, "q staging fits in the K-tile area");
+
+template <bool TENS>
+__global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  auto bar = [&](int k) -> uint32_t { return sb + uint32_t(kHgOffBars) + 8u * k; };
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#ifdef SMLA_TRACE
+  if (tid == 0 && blockIdx.x < 4096) g_hgspan[blockIdx.x][0] = globaltimer_ns();
+#endif
+
+  // Per-tensor FP8 codes go into the K tile unscaled (exact in f16); kv_scale is applied in
+  // fp32 to the scores (bmm1_scale = sm_scale * kv_scale) and to O (bmm2_scale = kv_scale),
+  // the scale algebra of vLLM PR #43827 "关键源码片段".
+  constexpr bool tens = TENS;
+  const float c2 = tens ? p.c2 * p.kv_scale : p.c2;
+  const int G = (p.H + 63) >> 6;
+  const int g = blockIdx.x % G;
+  const int item = blockIdx.x / G;
+  const int split = item % p.num_splits;
+  const int t = item / p.num_splits;
+  const int r = p.req_id ? __ldg(p.req_id + t) : t / p.next_n;
+  const bool req_ok = r >= 0 && r < p.B;
+  const int32_t* pt_row = p.page_table + int64_t(req_ok ? r : 0) * p.stride;
+  const int32_t* idx_row = p.topk + int64_t(t) * p.K;
+  const int j0 = split * p.split_len;
+  const int j1 = min(p.K, j0 + p.split_len);
+  const int nidx = max(0, j1 - j0);
+  const int ntiles = req_ok ? (nidx + kHgN - 1) / kHgN : 0;
+  const int h0 = 64 * g;
+  const int gheads = min(64, p.H - h0);  // heads of this group
+  const int nq = req_ok ? gheads : 0;     // q rows to load
+
+  // Producer lanes (slots [16 pw, 16 pw + 16) of every tile) fetch their slot's index
+  // kHgIdxAhead tiles ahead and, once it has landed, its page-table entry kHgAhead tiles
+  // ahead. Every ring step commits one cp.async group {index of tile i + kHgIdxAhead, page
+  // entry of tile i + kHgAhead}; the steps before tile 0 prime the rings before the set-up.
+  const bool producer = warp >= kHgFirstProducer && warp < kHgMmaWarp;
+  const int pw = warp - kHgFirstProducer;
+  const bool act = lane < kHgN / kHgProducers;
+  const int myslot = (kHgN / kHgProducers) * pw + lane;
+  int32_t* sidx = reinterpret_cast<int32_t*>(sm + kHgOffIdx);
+  int32_t* spage = reinterpret_cast<int32_t*>(sm + kHgOffPages);
+  auto in_split = [&](int tile) { return act && tile < ntiles && tile * kHgN + myslot < nidx; };
+  auto idx_of = [&](int tile) -> int32_t {
+    return in_split(tile) ? sidx[(tile % kHgIdxRing) * kHgN + myslot] : -1;
+  };
+  auto ring_step = [&](int i) {
+    cp_async_wait<kHgIdxAhead - kHgAhead - 1>();  // the group that fetched index i + kHgAhead
+    const int tp = i + kHgAhead;
+    if (tp >= 0) {
+      const int32_t idx = idx_of(tp);
+      if (idx >= 0 && (idx >> p.log2_page) < p.stride)
+        cp_async4(smem_u32(spage + (tp % kHgPageRing) * kHgN + myslot), pt_row + (idx >> p.log2_page));
+    }
+    const int ti = i + kHgIdxAhead;
+    if (in_split(ti))
+      cp_async4(smem_u32(sidx + (ti % kHgIdxRing) * kHgN + myslot), idx_row + j0 + ti * kHgN + myslot);
+    cp_async_commit();
+  };
+  if (producer)
+    for (int i = -kHgIdxAhead; i < 0; ++i) ring_step(i);
+
+  // ------------------------------------------------------------------ set-up
+  {
+    // masked slots of the first tiles dequantise zeros, and the P buffer's zero blocks stay 0
+    uint4* z = reinterpret_cast<uint4*>(sm + kHgOffRaw);
+    for (int k = tid; k < kHgStages * kHgRawStage / 16; k += kHgThreads) z[k] = make_uint4(0, 0, 0, 0);
+    uint4* zp = reinterpret_cast<uint4*>(sm + kHgOffP);
+    for (int k = tid; k < 5 * kHgPBlk / 16; k += kHgThreads) zp[k] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (tid == 0) {
+      for (int s = 0; s < kHgStages; ++s) {
+        mbar_init(bar(H_RAW_FULL + s), kHgProducers);  // one expect_tx arrival per producer warp
+        mbar_init(bar(H_RAW_EMPTY + s), kHgDequantWarps);
+        mbar_init(bar(H_K_FULL + s), kHgDequantWarps);
+        mbar_init(bar(H_K_FREE + s), 1);
+      }
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(bar(H_S_FULL + b), 1);
+        mbar_init(bar(H_S_FREE + b), 4);
+        mbar_init(bar(H_P_READY + b), 4);
+        mbar_init(bar(H_PV_DONE + b), 1);
+      }
+      mbar_init(bar(H_Q), 1);
+      mbar_init(bar(H_DRAIN), 1);
+      tc::fence_mbarrier_init_cluster();
+      if (!req_ok && split == 0 && g == 0) atomicOr(p.err, SMLA_DEVERR_INDEX);
+    }
+    if (warp == kHgMmaWarp) tc::alloc(sb + uint32_t(kHgOffTmem), 512);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+  }
+  const uint32_t tm = *reinterpret_cast<volatile uint32_t*>(sm + kHgOffTmem);
+
+  // Softmax warps place q: lane l < 64 gets dims [0, 256) of head h0 + l, lane 64 + l dims
+  // [256, 512), as f16 in TMEM (A of QK); the RoPE dims go to shared memory, rows 0-63 dims
+  // 512..543 and rows 64-127 dims 544..575 (64-byte swizzle). The group's q rows arrive by
+  // one bulk copy per head into the still idle K-tile area.
+  if (warp < 4) {
+    const int half = warp >> 1;
+    const int hl = 32 * (warp & 1) + lane;
+    const uint32_t lrow = tm + (uint32_t(32 * warp) << 16);
+    const uint32_t qs = sb + uint32_t(kHgOffK) + uint32_t(hl) * kHgQRow;
+    if (tid == 0 && nq > 0) mbar_arrive_expect_tx(bar(H_Q), uint32_t(nq) * (2 * kDim));
+    if (half == 0 && hl < nq)
+      bulk_g2s(qs, reinterpret_cast<const uint8_t*>(p.q) + (int64_t(t) * p.H + h0 + hl) * (2 * kDim), 2 * kDim,
+               bar(H_Q));
+    const bool got = nq == 0 || mbar_wait(bar(H_Q), 0);
+    if (!got && lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
+    const bool have = got && hl < nq;
+#pragma unroll 1
+    for (int ch = 0; ch < 8; ++ch) {
+      uint32_t wv[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (have) v = lds128(qs + 512 * half + 64 * ch + 16 * k);
+        wv[4 * k] = bf16x2_to_f16x2(v.x); wv[4 * k + 1] = bf16x2_to_f16x2(v.y);
+        wv[4 * k + 2] = bf16x2_to_f16x2(v.z); wv[4 * k + 3] = bf16x2_to_f16x2(v.w);
+      }
+      tc::st16(lrow + kHgTmQ + 16 * ch, wv);
+    }
+    tc::wait_st();
+    const int row = 32 * warp + lane;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (have) v = lds128(qs + 2 * kLatent + 64 * half + 16 * c);
+      const uint32_t dst = sb + uint32_t(kHgOffQr) + row * 64 + ((c ^ ((row >> 1) & 3)) << 4);
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(bf16x2_to_f16x2(v.x)),
+                   "r"(bf16x2_to_f16x2(v.y)), "r"(bf16x2_to_f16x2(v.z)), "r"(bf16x2_to_f16x2(v.w))
+                   : "memory");
+    }
+    fence_proxy_async_smem();  // read by the tensor core
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+
+  bool ok = true;
+  // ------------------------------------------------------------------ producer
+  if (producer) {
+    uint16_t* meta = reinterpret_cast<uint16_t*>(sm + kHgOffMeta);
+    const uint32_t rowbytes = tens ? uint32_t(kFp8TensorRowBytes) : uint32_t(kFp8RowBytes);
+    int issued = 0;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      ring_step(i);
+      const int st = i % kHgStages;
+      if (!mbar_wait(bar(H_RAW_EMPTY + st), ((i / kHgStages) & 1) ^ 1)) {
+        ok = false;
+        break;
+      }
+      const int32_t idx = idx_of(i);
+      int64_t phys = -1;
+      if (idx != -1) {
+        if (idx < 0 || (idx >> p.log2_page) >= p.stride) {
+          atomicOr(p.err, SMLA_DEVERR_INDEX);
+        } else {
+          const int32_t pg = spage[(i % kHgPageRing) * kHgN + myslot];
+          if (pg < 0 || pg >= p.num_pages)
+            atomicOr(p.err, SMLA_DEVERR_PAGE);
+          else
+            phys = (int64_t(pg) << p.log2_page) + (idx & ((1 << p.log2_page) - 1));
+        }
+      }
+      const uint32_t vm = __ballot_sync(0xffffffffu, phys >= 0);
+      if (lane == 0 && pw == 0) HTRACE(0, i);
+      if (lane == 0) {
+        meta[(i % kHgMetaRing) * kHgProducers + pw] = uint16_t(vm);
+        mbar_arrive_expect_tx(bar(H_RAW_FULL + st), uint32_t(__popc(vm)) * rowbytes);
+      }
+      __syncwarp();
+      if (phys >= 0)
+        bulk_g2s(sb + uint32_t(kHgOffRaw) + uint32_t(st * kHgRawStage + myslot * kHgRawRow),
+                 p.kv + phys * rowbytes, rowbytes, bar(H_RAW_FULL + st));
+      issued = i + 1;
+    }
+    cp_async_wait<0>();
+    // no bulk copy may land after the CTA has left
+    for (int i = max(0, issued - kHgStages); i < issued; ++i)
+      if (!mbar_wait(bar(H_RAW_FULL + i % kHgStages), (i / kHgStages) & 1)) break;
+  }
+  // ------------------------------------------------------------------ MMA issuer
+  else if (warp == kHgMmaWarp) {
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t kIdQK = tc::idesc_f16_f32(128, 64, false, false);
+      constexpr uint32_t kIdPV = tc::idesc_f16_f32(128, 256, false, true);
+      const uint32_t qr = sb + uint32_t(kHgOffQr);
+      auto qk = [&](int i) -> bool {
+        const int st = i % kHgStages, b = i & 1;
+        if (!mbar_wait(bar(H_K_FULL + st), (i / kHgStages) & 1)) return false;
+        if (i >= 2 && !mbar_wait(bar(H_S_FREE + b), ((i - 2) >> 1) & 1)) return false;
+        HTRACE(4, i);
+        tc::fence_after();
+        const uint32_t kt = sb + uint32_t(kHgOffK) + uint32_t(st * kHgKtile);
+        const uint32_t d = tm + kHgTmS + 64 * b;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          tc::mma_ts(d, tm + kHgTmQ + 8 * j, tc::sdesc_sw128(kt + (j >> 2) * kHgPairBlk + (j & 3) * 32, 16, 1024),
+                     kIdQK, j > 0);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          tc::mma_ss(d, tc::sdesc_sw64(qr + 32 * j, 16, 512), tc::sdesc_sw64(kt + 4 * kHgPairBlk + 32 * j, 16, 512),
+                     kIdQK, 1);
+        tc::commit(bar(H_S_FULL + b));
+        return true;
+      };
+      auto pv = [&](int i) -> bool {
+        const int st = i % kHgStages, b = i & 1;
+        if (!mbar_wait(bar(H_P_READY + b), (i >> 1) & 1)) return false;
+        HTRACE(5, i);
+        tc::fence_after();
+        const uint32_t kt = sb + uint32_t(kHgOffK) + uint32_t(st * kHgKtile);
+        const uint32_t pa = sb + uint32_t(kHgOffP) + uint32_t((1 + 2 * b) * kHgPBlk);  // P rows
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {  // 16 slots per MMA
+          // [P; 0] x latent dims [0, 256) -> lanes 0-63; [0; P] x dims [256, 512) -> lanes 64-127
+          tc::mma_ss(tm + kHgTmO, tc::sdesc_sw64(pa + 32 * s, 16, 512),
+                     tc::sdesc_sw128(kt + 2048 * s, kHgPairBlk, 1024), kIdPV, (i > 0 || s > 0));
+          tc::mma_ss(tm + kHgTmO, tc::sdesc_sw64(pa - kHgPBlk + 32 * s, 16, 512),
+                     tc::sdesc_sw128(kt + 4096 + 2048 * s, kHgPairBlk, 1024), kIdPV, 1);
+        }
+        tc::commit(bar(H_K_FREE + st));
+        tc::commit(bar(H_PV_DONE + b));
+        return true;
+      };
+      ok = qk(0);
+      if (ok && ntiles > 1) ok = qk(1);
+      for (int i = 0; i < ntiles && ok; ++i) {
+        ok = pv(i);
+        if (ok && i + 2 < ntiles) ok = qk(i + 2);
+      }
+      // every MMA issued has completed before the tensor memory is released
+      tc::commit(bar(H_DRAIN));
+      if (!mbar_wait(bar(H_DRAIN), 0)) ok = false;
+    }
+    __syncwarp();
+  }
+  // ------------------------------------------------------------------ dequant
+  else if (warp >= kHgFirstDequant) {
+    const int dtid = tid - 32 * kHgFirstDequant;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      const int st = i % kHgStages;
+      if (!mbar_wait(bar(H_RAW_FULL + st), (i / kHgStages) & 1)) { ok = false; break; }
+      if (dtid == 0) HTRACE(1, i);
+      if (i >= kHgStages && !mbar_wait(bar(H_K_FREE + st), ((i - kHgStages) / kHgStages) & 1)) {
+        ok = false;
+        break;
+      }
+      if (dtid == 0) HTRACE(2, i);
+      const uint32_t raw = sb + uint32_t(kHgOffRaw) + uint32_t(st * kHgRawStage);
+      const uint32_t kt = sb + uint32_t(kHgOffK) + uint32_t(st * kHgKtile);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int id = dtid + kHgDequantThreads * k;
+        const int slot = id & 31, ch = id >> 5;  // latent bytes [16ch, 16ch+16) of slot
+        const uint32_t rrow = raw + slot * kHgRawRow;
+        const uint4 v = lds128(rrow + 16 * ch);
+        const float sc = tens ? 1.f : lds_f32(rrow + kScaleOff + 4 * (ch >> 3));
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[8];
+        const __half2 s2 = __float2half2_rn(sc);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t lo, hi;
+          e4m3x4_to_f16x4(wv[q], lo, hi);  // exact
+          if constexpr (tens) {  // the scale comes later, in fp32
+            o[2 * q] = lo;
+            o[2 * q + 1] = hi;
+          } else {  // code * scale in f16 (exact for power-of-two scales in f16's range)
+            __half2 a = __hmul2(*reinterpret_cast<const __half2*>(&lo), s2);
+            __half2 b = __hmul2(*reinterpret_cast<const __half2*>(&hi), s2);
+            o[2 * q] = *reinterpret_cast<uint32_t*>(&a);
+            o[2 * q + 1] = *reinterpret_cast<uint32_t*>(&b);
+          }
+        }
+        // dims [16ch, 16ch+16): block ch/4 mod 4, low rows for ch < 16, high rows after
+        const int rr = 32 * (ch >> 4) + slot;
+        const uint32_t row = kt + ((ch >> 2) & 3) * kHgPairBlk + rr * 128;
+        const int c0 = 2 * (ch & 3);
+        const uint32_t sw = rr & 7;
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + ((c0 ^ sw) << 4)), "r"(o[0]),
+                     "r"(o[1]), "r"(o[2]), "r"(o[3]) : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + (((c0 + 1) ^ sw) << 4)), "r"(o[4]),
+                     "r"(o[5]), "r"(o[6]), "r"(o[7]) : "memory");
+      }
+      {
+        const int slot = dtid & 31, rc = dtid >> 5;  // RoPE dims [8rc, 8rc+8) of slot
+        uint4 v;
+        if constexpr (tens) {  // eight E4M3 codes -> f16 (exact; the scale comes later in fp32)
+          const uint2 cw = lds64(raw + slot * kHgRawRow + kLatent + 8 * rc);
+          uint32_t hh[4];
+          e4m3x4_to_f16x4(cw.x, hh[0], hh[1]);
+          e4m3x4_to_f16x4(cw.y, hh[2], hh[3]);
+          v = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+        } else {  // bf16 RoPE -> f16
+          const uint4 rv = lds128(raw + slot * kHgRawRow + kRopeOffFp8 + 16 * rc);
+          v = make_uint4(bf16x2_to_f16x2(rv.x), bf16x2_to_f16x2(rv.y), bf16x2_to_f16x2(rv.z),
+                         bf16x2_to_f16x2(rv.w));
+        }
+        const int rr = 32 * (rc >> 2) + slot, c = rc & 3;
+        const uint32_t dst = kt + 4 * kHgPairBlk + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4);
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
+                     "r"(v.w) : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(H_K_FULL + st));
+        mbar_arrive(bar(H_RAW_EMPTY + st));
+      }
+      if (dtid == 0) HTRACE(3, i);
+    }
+    // all K tiles are dequantised: the split merge, if one follows, may start launching
+    if (dtid == 0) pdl_trigger();
+  }
+  // ------------------------------------------------------------------ softmax + epilogue
+  else {
+    const int half = warp >> 1;  // 0: lanes 0-63 (low dims), 1: lanes 64-127 (high dims)
+    const int pr = warp & 1;     // head pair: warps pr (low) and pr + 2 (high)
+    const int hl = 32 * pr + lane;
+    const int h = h0 + hl;
+    const uint32_t lrow = tm + (uint32_t(32 * warp) << 16);
+    const uint32_t* meta = reinterpret_cast<const uint32_t*>(sm + kHgOffMeta);  // 32 slot bits per tile
+    const uint32_t xmine = sb + uint32_t(kHgOffXs) + uint32_t(32 * warp + lane) * kHgXRow;
+    const uint32_t xpart = sb + uint32_t(kHgOffXs) + uint32_t(32 * (warp ^ 2) + lane) * kHgXRow;
+    const int bar_x = 1 + pr;                     // both rows of the pair are written
+    const int bar_mine = 3 + 2 * pr + half;       // the partner has read my row
+    const int bar_part = 3 + 2 * pr + (half ^ 1); // I have read the partner's row
+    float m = -CUDART_INF_F, l = 0.f;
+    bool good = true;
+
+    // rescale this thread's O lane (256 columns) by a once PV(i-1) is complete; the TMEM
+    // loads and stores are warp-wide, so the whole warp calls this when any lane needs it
+    auto correct_o = [&](int i, float a) -> bool {
+      if (i > 0 && !mbar_wait(bar(H_PV_DONE + ((i - 1) & 1)), ((i - 1) >> 1) & 1)) return false;
+      tc::fence_after();
+#pragma unroll 1
+      for (int k = 0; k < 16; ++k) {
+        uint32_t v[16];
+        tc::ld16(lrow + kHgTmO + 16 * k, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
+        tc::st16(lrow + kHgTmO + 16 * k, v);
+      }
+      tc::wait_st();
+      return true;
+    };
+
+    bool loop_ok = true;
+    for (int i = 0; i < ntiles; ++i) {
+      const int b = i & 1;
+      float s[32];
+      const bool got = good && mbar_wait(bar(H_S_FULL + b), (i >> 1) & 1);
+      if (got) {
+        tc::fence_after();
+        uint32_t v[32];
+        tc::ld32(lrow + kHgTmS + 64 * b + 32 * half, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(v[e]);
+        tc::fence_before();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[e] = 0.f;
+      }
+      __syncwarp();
+      if (lane == 0 && got) mbar_arrive(bar(H_S_FREE + b));
+      if (lane == 0 && (warp == 0 || warp == 2)) HTRACE(6 + warp / 2, i);
+      if (i > 0) named_bar(bar_mine, 64);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(xmine + 16 * k), "r"(__float_as_uint(s[4 * k])),
+                     "r"(__float_as_uint(s[4 * k + 1])), "r"(__float_as_uint(s[4 * k + 2])),
+                     "r"(__float_as_uint(s[4 * k + 3])) : "memory");
+      if (!named_bar_and(bar_x, 64, got)) {
+        loop_ok = false;
+        break;
+      }
+      float x[32];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 xv = lds128(xpart + 16 * k);
+        x[4 * k] = __uint_as_float(xv.x); x[4 * k + 1] = __uint_as_float(xv.y);
+        x[4 * k + 2] = __uint_as_float(xv.z); x[4 * k + 3] = __uint_as_float(xv.w);
+      }
+      named_bar_arrive(bar_part, 64);
+      if (lane == 0 && warp == 0) HTRACE(8, i);
+
+      // both warps of the pair add the same two rows (fp32 addition commutes bitwise), so
+      // both get identical scores, maxima and rescale factors
+      const uint32_t msk = meta[i % kHgMetaRing];
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float v = ((msk >> j) & 1u) ? (s[j] + x[j]) * c2 : -CUDART_INF_F;
+        s[j] = v;
+        mx = fmaxf(mx, v);
+      }
+      float a = 1.f;
+      const float mn = fmaxf(m, mx);
+      if (m == -CUDART_INF_F ? mn != -CUDART_INF_F : mn > m + kHgRescaleThreshold) {
+        a = exp2f(m - mn);  // 0 when m was -inf
+        m = mn;
+      }
+      const float base = m == -CUDART_INF_F ? 0.f : m;
+      // this warp's 16 of the 32 slots
+      float sh[16];  // (selects keep the scores in registers)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) sh[j] = half ? s[16 + j] : s[j];
+      float sum = 0.f;
+      uint32_t pw2[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float p0 = exp2f(sh[2 * j] - base), p1 = exp2f(sh[2 * j + 1] - base);
+        sum += p0 + p1;
+        pw2[j] = pack_f16x2(p0, p1);
+      }
+      l = l * a + sum;
+      // P buffer b is free once PV(i-2) is complete
+      if (i >= 2 && !mbar_wait(bar(H_PV_DONE + b), ((i - 2) >> 1) & 1)) good = false;
+      if (good && i > 0 && __any_sync(0xffffffffu, a != 1.f) && !correct_o(i, a)) good = false;
+      if (good) {
+        const uint32_t prow = sb + uint32_t(kHgOffP) + uint32_t((1 + 2 * b) * kHgPBlk) + uint32_t(hl) * 64;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int c = 2 * half + k;
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((c ^ ((hl >> 1) & 3)) << 4)),
+                       "r"(pw2[4 * k]), "r"(pw2[4 * k + 1]), "r"(pw2[4 * k + 2]), "r"(pw2[4 * k + 3])
+                       : "memory");
+        }
+        fence_proxy_async_smem();  // read by the tensor core
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0 && good) mbar_arrive(bar(H_P_READY + b));
+      if (lane == 0 && (warp == 0 || warp == 2)) HTRACE(9 + warp / 2, i);
+    }
+
+    // ---- epilogue: both row halves' sums, final row factor, then O lane -> output
+    ok = loop_ok;
+    if (ok) {
+      if (ntiles > 0) named_bar(bar_mine, 64);  // the partner has read my last row
+      bool fin = good;
+      if (fin && ntiles > 0) {
+        const int last = ntiles - 1;
+        fin = mbar_wait(bar(H_PV_DONE + (last & 1)), (last >> 1) & 1);
+        tc::fence_after();
+      }
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(xmine), "f"(l) : "memory");
+      ok = named_bar_and(bar_x, 64, fin);
+      if (ok) l += lds_f32(xpart);  // low half + high half in the other warp: same sum order
+    }
+    if (ok) {
+      const int S = p.num_splits;
+      const bool real = hl < gheads;
+      const float lse0 = l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
+      float lse_out = lse0;
+      float f = l > 0.f ? (tens ? p.kv_scale : 1.f) / l : 0.f;
+      if (S == 1 && p.sink && real) {
+        const float sg = __ldg(p.sink + h);
+        lse_out = fmaxf(lse0, sg) + log1pf(expf(-fabsf(lse0 - sg)));
+        f *= expf(lse0 - lse_out);
+      }
+      if (real && half == 0) {
+        if (S == 1) {
+          if (p.lse) p.lse[int64_t(t) * p.H + h] = lse_out;
+        } else {
+          p.lse_part[(int64_t(t) * S + split) * p.H + h] = lse0;
+        }
+      }
+      const int64_t orow_g = S == 1 ? int64_t(t) * p.H + h : (int64_t(t) * S + split) * p.H + h;
+      // four 16-column loads in flight per wait; every lane loads, only real heads store
+#pragma unroll 1
+      for (int k4 = 0; k4 < 4; ++k4) {
+        uint32_t v4[4][16];
+        if (ntiles > 0) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tc::ld16(lrow + kHgTmO + 64 * k4 + 16 * j, v4[j]);
+          tc::wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v4[j][e] = 0u;
+        }
+        if (!real) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t* v = v4[j];
+          const int col = 256 * half + 64 * k4 + 16 * j;
+          if (S == 1) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow_g * kLatent + col);
+            uint32_t o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              o[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * f, __uint_as_float(v[2 * e + 1]) * f);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+          } else {
+            float4* dst = reinterpret_cast<float4*>(p.o_part + orow_g * kLatent + col);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_float4(__uint_as_float(v[4 * e]) * f, __uint_as_float(v[4 * e + 1]) * f,
+                                   __uint_as_float(v[4 * e + 2]) * f, __uint_as_float(v[4 * e + 3]) * f);
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  if (!ok && lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
+  tc::fence_before();
+  __syncthreads();
+  if (warp == kHgMmaWarp) {
+    tc::fence_after();
+    tc::dealloc(tm, 512);
+  }
+#ifdef SMLA_TRACE
+  if (tid == 0 && blockIdx.x < 4096) g_hgspan[blockIdx.x][1] = globaltimer_ns();
+#endif
+}
+
+}  // namespace
+
+cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s) {
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(decode_hg_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemHg));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_hg_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemHg));
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  const int64_t grid = int64_t(a.T) * a.num_splits * ((a.H + 63) / 64);
+  if (a.kv_format == SMLA_KV_FP8_TENSOR)
+    decode_hg_kernel<true><<<static_cast<unsigned>(grid), kHgThreads, kSmemHg, s>>>(a);
+  else
+    decode_hg_kernel<false><<<static_cast<unsigned>(grid), kHgThreads, kSmemHg, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace smla
+
+#ifdef SMLA_TRACE
+extern "C" int smla_hgtrace_read(unsigned long long* host) {
+  return int(cudaMemcpyFromSymbol(host, g_hgtrace, sizeof(g_hgtrace)));
+}
+extern "C" int smla_hgspan_read(unsigned long long* host) {
+  return int(cudaMemcpyFromSymbol(host, g_hgspan, sizeof(g_hgspan)));
+}
+#endif

@@ -83,12 +83,17 @@ bool use_tc(const smla_desc* d) {
   return (d->kv_format == SMLA_KV_FP8_DS || d->kv_format == SMLA_KV_FP8_TENSOR) &&
          d->num_heads >= smla::kTcMinHeads;
 }
+// 64 heads fit one SM (the head-group kernel); 80..128 heads take a CTA pair.
+bool use_hg(const smla_desc* d) { return use_tc(d) && d->num_heads <= smla::kHgMaxHeads; }
 
 Plan make_plan(const smla_desc* d, int num_sms) {
   int S = d->num_splits;
   if (S == 0) {
     S = 1;
-    if (use_tc(d)) {
+    if (use_hg(d)) {
+      // one CTA per (token, split), one per SM: fill one wave at most
+      if (d->num_tokens < num_sms) S = num_sms / d->num_tokens;
+    } else if (use_tc(d)) {
       // one CTA pair per (token, split), one pair per two SMs: fill one wave at most
       const int pairs = num_sms / 2;
       if (d->num_tokens < pairs) S = pairs / d->num_tokens;
@@ -216,7 +221,9 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
   a.split_len = plan.split_len;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (t_ev_start && cudaEventRecord(t_ev_start, s) != cudaSuccess) return SMLA_ERR_CUDA;
-  const cudaError_t e = use_tc(d) ? smla::launch_decode_tc(a, s) : smla::launch_decode_mma(a, sms, s);
+  const cudaError_t e = use_hg(d)   ? smla::launch_decode_hg(a, s)
+                            : use_tc(d) ? smla::launch_decode_tc(a, s)
+                                        : smla::launch_decode_mma(a, sms, s);
   if (e != cudaSuccess) return SMLA_ERR_CUDA;
   if (t_ev_stop && cudaEventRecord(t_ev_stop, s) != cudaSuccess) return SMLA_ERR_CUDA;
   if (plan.num_splits > 1 && smla::launch_merge(a, s) != cudaSuccess) return SMLA_ERR_CUDA;
