@@ -1,31 +1,32 @@
 // Sparse MLA decode on the 5th-generation tensor cores (tcgen05, TMEM accumulators) for the
 // FP8 caches (fp8_ds: 656-byte rows with per-128 scales and bf16 RoPE; per-tensor FP8: 576
-// E4M3 codes with one scale, vLLM PR #43827), one CTA per (query token, top-k split, group
-// of 64 heads).
+// E4M3 codes with one scale, vLLM PR #43827), one CTA per (query token, top-k split, group of
+// 64 heads).
 //
 // What it computes is the sparse decode of vLLM PR #43477 "关键源码片段" (forward_mqa) with
 // the sink and split merge of SGLang PR #24692 "关键文件": out_h = softmax over the selected
 // slots of sm_scale * <q_h, k_j>, applied to v_j = k_j[0:512].
 //
-// Why one CTA holds a whole head group: the fp32 output of 64 heads x 512 dims is 128 KB,
-// half of an SM's tensor memory, if the two halves of each head's 512 dims are stacked on
-// the 128 TMEM lanes: lane l < 64 holds head l's dims [0, 256), lane 64 + l its dims
-// [256, 512), in 256 columns. q is stacked the same way (lane l < 64: dims [0, 256) of
-// head l; lane 64 + l: dims [256, 512)), so QK needs no exchange between SMs:
-//  * QK of a 32-slot tile: B stacks the same slots twice, rows 0-31 with dims [0, 256) and
-//    rows 32-63 with dims [256, 512). Lane l < 64, columns 0-31 of the M128 N64 result are
-//    the low partial scores of head l; lane 64 + l, columns 32-63, the high ones (the other
+// Why one CTA holds 64 heads: the fp32 output of 64 heads x 512 dims is 128 KB, half of
+// an SM's tensor memory, if the two halves of each head's 512 dims are stacked on the 128
+// TMEM lanes: lane l < 64 holds head l's dims [0, 256), lane 64 + l its dims [256, 512), in
+// 256 columns. q is stacked the same way (lane l < 64: dims [0, 256) of head l; lane 64 + l:
+// dims [256, 512)), so QK needs no exchange between SMs:
+//  * QK of a 64-slot tile: B stacks the same slots twice, rows 0-63 with dims [0, 256) and
+//    rows 64-127 with dims [256, 512). Lane l < 64, columns 0-63 of the M128 N128 result are
+//    the low partial scores of head l; lane 64 + l, columns 64-127, the high ones (the other
 //    two quadrants are unused). The 64 RoPE dims are split the same way, with q's RoPE part
-//    as an A operand in shared memory. 18 x M128 N64 K16 per tile.
+//    as an A operand in shared memory. 18 x M128 N128 K16 per tile: the cost of these MMAs
+//    barely depends on N, so a wide tile halves the QK cost per slot.
 //  * The two partial rows of a head meet in shared memory: the warp of lane quarter w and
-//    the warp of quarter w ^ 2 hold heads 32(w & 1) .. 32(w & 1) + 31, low and high. Both
-//    add the two rows in the same order, so both see bit-identical scores, maxima and
-//    rescale factors; each writes the probabilities of 16 of the 32 slots.
+//    the warp of quarter w ^ 2 hold heads 32(w & 1) .. 32(w & 1) + 31, low and high. The low
+//    warp finishes slots 0-31 and the high warp slots 32-63; they swap their maxima, so both
+//    take the same running max and rescale factor.
 //  * PV: A = [P; 0] against the latent dims [0, 256) of the tile and A = [0; P] against dims
 //    [256, 512), both into the same 256 TMEM columns, so lanes 0-63 accumulate the low
-//    output dims and lanes 64-127 the high ones. 4 x M128 N256 K16 per tile.
+//    output dims and lanes 64-127 the high ones. 8 x M128 N256 K16 per tile.
 // Half of each MMA's rows or columns are unused: 64 heads fill only half of an M = 128
-// tile. In exchange the head group needs one SM, not two, and no traffic between SMs.
+// tile. In exchange a group of 64 heads needs one SM, not two, and no traffic between SMs.
 //
 // The MMAs run on f16 operands with fp32 accumulation: an E4M3 code converts to f16 exactly,
 // and the block scale applies with one f16 multiply (exact for power-of-two scales, within
@@ -33,19 +34,27 @@
 // f16's range (+-65504).
 //
 // Per CTA (480 threads):
-//  * warps 12-13, producers (16 slots of every tile each): index entries twelve tiles ahead
-//    and page-table entries six tiles ahead by 4-byte cp.async, then each valid row by one
-//    bulk copy (TMA engine) into a 3-stage ring.
-//  * warps 4-11, dequant: e4m3 (* scale) -> f16 into the K tile: four 128-byte-swizzled
-//    blocks of [32 slots x 64 low dims | 32 slots x 64 high dims] and a 64-byte-swizzled
-//    RoPE block (3 buffers). The same bytes are B of QK (K-major) and B of PV (MN-major).
-//  * warp 14, MMA issuer (one thread). QK of tile i+2 follows PV of tile i; two score
-//    buffers let QK run while the softmax of the previous tile does.
+//  * warps 12-13, producers: index entries six tiles ahead and page-table entries three
+//    tiles ahead by 4-byte cp.async, then the selected rows by TMA gathers of four rows each
+//    (tile::gather4 on a tensor map of the cache) into a 3-stage ring of 16-row stages; a
+//    masked slot gets a row outside the tensor, which the TMA fills with zeros without
+//    reading memory. One gather per four rows keeps the TMA engine, which serialises its
+//    operations, off the critical path. Warp 12 fills stages 0 and 2 of every tile, warp 13
+//    stages 1 and 3.
+//  * warps 4-11, dequant: e4m3 (* scale) -> f16 into the latent K tile (two buffers): four
+//    128-byte-swizzled blocks of [64 slots x 64 low dims | 64 slots x 64 high dims], which
+//    are B of QK (K-major) and B of PV (MN-major). A 16-row quarter of a buffer is rewritten
+//    as soon as PV has finished reading it. The RoPE dims go to one 64-byte-swizzled block
+//    once QK of the previous tile has completed.
+//  * warp 14, MMA issuer (one thread): QK of tile i+1 runs while the softmax of tile i does;
+//    of the two, whichever is ready is issued first (PV of tile i when its P is written).
 //  * warps 0-3, softmax and epilogue: base-2 online softmax with lazy rescaling (the running
 //    max moves only when it grows by more than 8, as in FlashAttention-4).
 // Every wait is bounded in time; a wait that gives up sets SMLA_DEVERR_TIMEOUT. The two
 // warps of a head pair meet at named barriers that also AND their status, so both leave the
 // tile loop at the same barrier and neither waits for a partner that has left.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -70,7 +79,8 @@ __device__ unsigned long long g_hgspan[4096][2];
 namespace smla {
 namespace {
 
-constexpr int kHgN = 32;                 // slots per tile
+constexpr int kHgN = 64;                 // slots per tile
+constexpr int kHgSub = 16;               // rows per raw-ring stage (a quarter tile)
 constexpr int kHgFirstDequant = 4;       // warps 0..3: softmax
 constexpr int kHgDequantWarps = 8;
 constexpr int kHgFirstProducer = kHgFirstDequant + kHgDequantWarps;
@@ -78,18 +88,18 @@ constexpr int kHgProducers = 2;
 constexpr int kHgMmaWarp = kHgFirstProducer + kHgProducers;
 constexpr int kHgThreads = 32 * (kHgMmaWarp + 1);
 constexpr int kHgDequantThreads = 32 * kHgDequantWarps;
-constexpr int kHgStages = 3;             // raw-row ring and K tiles
-constexpr int kHgRawRow = kFp8RowBytes;  // a per-tensor row uses its first 576 bytes
-constexpr int kHgRawStage = kHgN * kHgRawRow;
-constexpr int kHgPairBlk = 2 * kHgN * 128;  // [32 slots x 64 low dims | same slots, high dims]
-constexpr int kHgRopeBlk = 2 * kHgN * 64;   // [32 slots x RoPE 0..31 | same slots, 32..63]
-constexpr int kHgKtile = 4 * kHgPairBlk + kHgRopeBlk;
-constexpr int kHgPBlk = 64 * kHgN * 2;      // 64 rows x 32 slots f16, 64-byte swizzle
+constexpr int kHgRawStages = 4;  // a whole tile
+constexpr int kHgGroup = 2688;              // four gathered rows (<= 4 x 656 B), 128-byte aligned
+constexpr int kHgRawStage = 4 * kHgGroup;   // 16 rows
+constexpr int kHgPairBlk = 2 * kHgN * 128;  // [64 slots x 64 low dims | same slots, high dims]
+constexpr int kHgKLat = 4 * kHgPairBlk;     // latent K tile (two buffers)
+constexpr int kHgRopeBlk = 2 * kHgN * 64;   // [64 slots x RoPE 0..31 | same slots, 32..63]
+constexpr int kHgPBlk = 64 * kHgN * 2;      // 64 rows x 64 slots f16, 128-byte swizzle
 constexpr int kHgQrope = 128 * 64;          // q RoPE, [128 rows x 32 dims] f16
-constexpr int kHgXRow = 144;                // 32 fp32 + padding (conflict-free rows)
-constexpr int kHgIdxAhead = 12, kHgIdxRing = 16;
-constexpr int kHgAhead = 6, kHgPageRing = 8;
-constexpr int kHgMetaRing = 16;
+constexpr int kHgXRow = 80;                 // 16 fp32 + padding (conflict-free rows)
+constexpr int kHgIdxAhead = 5, kHgIdxRing = 6;
+constexpr int kHgAhead = 3, kHgPageRing = 4;
+constexpr int kHgMetaRing = 8;
 constexpr float kHgRescaleThreshold = 8.f;  // log2 units
 static_assert(kHgIdxAhead <= 2 * kHgAhead && kHgIdxRing > kHgIdxAhead && kHgPageRing > kHgAhead,
               "index and page rings");
@@ -97,33 +107,45 @@ static_assert(kHgIdxAhead <= 2 * kHgAhead && kHgIdxRing > kHgIdxAhead && kHgPage
 // TMEM columns (512 allocated)
 constexpr uint32_t kHgTmO = 0;    // O [128 lanes x 256] fp32, lanes 64.. = high dims
 constexpr uint32_t kHgTmQ = 256;  // q latent [128 lanes x 256 dims] f16: 128 columns
-constexpr uint32_t kHgTmS = 384;  // two score buffers of 64 columns
+constexpr uint32_t kHgTmS = 384;  // scores [128 lanes x 128] fp32
 
 constexpr size_t kHgOffK = 0;
-constexpr size_t kHgOffRaw = kHgOffK + size_t(kHgStages) * kHgKtile;
-constexpr size_t kHgOffP = kHgOffRaw + size_t(kHgStages) * kHgRawStage;  // [0 | P0 | 0 | P1 | 0]
-constexpr size_t kHgOffQr = kHgOffP + 5 * size_t(kHgPBlk);
-constexpr size_t kHgOffXs = kHgOffQr + kHgQrope;
-constexpr size_t kHgOffIdx = kHgOffXs + 128 * size_t(kHgXRow);
+constexpr size_t kHgOffRope = kHgOffK + 2 * size_t(kHgKLat);
+constexpr size_t kHgOffP = kHgOffRope + kHgRopeBlk;  // [0 | P | 0]
+constexpr size_t kHgOffQr = kHgOffP + 3 * size_t(kHgPBlk);
+constexpr size_t kHgOffRaw = kHgOffQr + kHgQrope;
+constexpr size_t kHgOffXs = kHgOffRaw + size_t(kHgRawStages) * kHgRawStage;
+constexpr size_t kHgOffXm = kHgOffXs + 128 * size_t(kHgXRow);
+constexpr size_t kHgOffIdx = kHgOffXm + 128 * 4;
 constexpr size_t kHgOffPages = kHgOffIdx + size_t(kHgIdxRing) * kHgN * 4;
 constexpr size_t kHgOffMeta = kHgOffPages + size_t(kHgPageRing) * kHgN * 4;
-constexpr size_t kHgOffTmem = kHgOffMeta + kHgMetaRing * 4;
+constexpr size_t kHgOffTmem = kHgOffMeta + kHgMetaRing * 8;
 constexpr size_t kHgOffBars = kHgOffTmem + 16;
+// mbarrier indices, laid out from the raw ring's stage count
 enum {
-  H_RAW_FULL = 0, H_RAW_EMPTY = 3, H_K_FULL = 6, H_K_FREE = 9, H_S_FULL = 12, H_S_FREE = 14,
-  H_P_READY = 16, H_PV_DONE = 18, H_Q = 20, H_DRAIN = 21, H_COUNT = 22
+  H_RAW_FULL = 0,
+  H_RAW_EMPTY = H_RAW_FULL + kHgRawStages,
+  H_K_FULL = H_RAW_EMPTY + kHgRawStages,  // [buffer]
+  H_K_FREE = H_K_FULL + 2,                 // [buffer][16-slot chunk]
+  H_ROPE_FULL = H_K_FREE + 8,
+  H_S_FULL, H_S_FREE, H_P_READY, H_PV_DONE, H_Q, H_DRAIN, H_COUNT
 };
+static_assert(H_RAW_EMPTY == kHgRawStages && H_K_FULL == 2 * kHgRawStages && H_COUNT == 2 * kHgRawStages + 17,
+              "one mbarrier per ring stage and buffer, none shared");
 constexpr size_t kSmemHg = kHgOffBars + H_COUNT * 8 + 1024;  // + alignment slack
 static_assert(kSmemHg <= 232448, "shared memory budget");
-static_assert(kHgOffP % 512 == 0 && kHgOffQr % 512 == 0 && kHgKtile % 1024 == 0 && kHgOffRaw % 1024 == 0,
-              "swizzle atoms: 512-byte (64-byte swizzle) and 1024-byte (128-byte swizzle) aligned");
+static_assert(kHgOffK % 1024 == 0 && kHgKLat % 1024 == 0 && kHgOffP % 1024 == 0 && kHgOffRope % 512 == 0 &&
+                  kHgOffQr % 512 == 0 && kHgOffRaw % 128 == 0 && kHgOffBars % 8 == 0 && kHgGroup % 128 == 0 &&
+                  kHgGroup >= 4 * kFp8RowBytes,
+              "swizzle atoms: 1024-byte (128-byte swizzle) and 512-byte (64-byte swizzle) aligned");
 // q staging at start-up: 64 rows of 1152 bytes (+16 for conflict-free 16-byte reads) in the
 // K-tile area, which the pipeline first writes after the start-up barrier
 constexpr uint32_t kHgQRow = 1168;
-static_assert(64 * kHgQRow <= kHgOffRaw, "q staging fits in the K-tile area");
+static_assert(64 * kHgQRow <= kHgOffRope, "q staging fits in the K-tile area");
 
 template <bool TENS>
-__global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeArgs p) {
+__global__ void __launch_bounds__(kHgThreads, 1)
+    decode_hg_kernel(const DecodeArgs p, const __grid_constant__ CUtensorMap kv_map) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
@@ -138,7 +160,7 @@ __global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeAr
   // the scale algebra of vLLM PR #43827 "关键源码片段".
   constexpr bool tens = TENS;
   const float c2 = tens ? p.c2 * p.kv_scale : p.c2;
-  const int G = (p.H + 63) >> 6;
+  const int G = (p.H + 63) >> 6;  // groups of 64 heads, one CTA each
   const int g = blockIdx.x % G;
   const int item = blockIdx.x / G;
   const int split = item % p.num_splits;
@@ -155,31 +177,38 @@ __global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeAr
   const int gheads = min(64, p.H - h0);  // heads of this group
   const int nq = req_ok ? gheads : 0;     // q rows to load
 
-  // Producer lanes (slots [16 pw, 16 pw + 16) of every tile) fetch their slot's index
-  // kHgIdxAhead tiles ahead and, once it has landed, its page-table entry kHgAhead tiles
-  // ahead. Every ring step commits one cp.async group {index of tile i + kHgIdxAhead, page
-  // entry of tile i + kHgAhead}; the steps before tile 0 prime the rings before the set-up.
+  // Producer lanes 0-15 of warp 12 + pw own slots 16q + lane for q in {pw, pw + 2} of every
+  // tile. They fetch each slot's index kHgIdxAhead tiles ahead and, once it has landed, its
+  // page-table entry kHgAhead tiles ahead. Every ring step commits one cp.async group
+  // {indices of tile i + kHgIdxAhead, page entries of tile i + kHgAhead}; the steps before
+  // tile 0 prime the rings before the set-up.
   const bool producer = warp >= kHgFirstProducer && warp < kHgMmaWarp;
   const int pw = warp - kHgFirstProducer;
-  const bool act = lane < kHgN / kHgProducers;
-  const int myslot = (kHgN / kHgProducers) * pw + lane;
+  const bool act = lane < kHgSub;
   int32_t* sidx = reinterpret_cast<int32_t*>(sm + kHgOffIdx);
   int32_t* spage = reinterpret_cast<int32_t*>(sm + kHgOffPages);
-  auto in_split = [&](int tile) { return act && tile < ntiles && tile * kHgN + myslot < nidx; };
-  auto idx_of = [&](int tile) -> int32_t {
-    return in_split(tile) ? sidx[(tile % kHgIdxRing) * kHgN + myslot] : -1;
+  auto in_split = [&](int tile, int q) {
+    return act && tile < ntiles && tile * kHgN + kHgSub * q + lane < nidx;
+  };
+  auto idx_of = [&](int tile, int q) -> int32_t {
+    return in_split(tile, q) ? sidx[(tile % kHgIdxRing) * kHgN + kHgSub * q + lane] : -1;
   };
   auto ring_step = [&](int i) {
-    cp_async_wait<kHgIdxAhead - kHgAhead - 1>();  // the group that fetched index i + kHgAhead
+    cp_async_wait<kHgIdxAhead - kHgAhead - 1>();  // the group that fetched indices i + kHgAhead
     const int tp = i + kHgAhead;
-    if (tp >= 0) {
-      const int32_t idx = idx_of(tp);
-      if (idx >= 0 && (idx >> p.log2_page) < p.stride)
-        cp_async4(smem_u32(spage + (tp % kHgPageRing) * kHgN + myslot), pt_row + (idx >> p.log2_page));
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int q = pw + 2 * k;
+      if (tp >= 0) {
+        const int32_t idx = idx_of(tp, q);
+        if (idx >= 0 && (idx >> p.log2_page) < p.stride)
+          cp_async4(smem_u32(spage + (tp % kHgPageRing) * kHgN + kHgSub * q + lane), pt_row + (idx >> p.log2_page));
+      }
+      const int ti = i + kHgIdxAhead;
+      if (in_split(ti, q))
+        cp_async4(smem_u32(sidx + (ti % kHgIdxRing) * kHgN + kHgSub * q + lane),
+                  idx_row + j0 + ti * kHgN + kHgSub * q + lane);
     }
-    const int ti = i + kHgIdxAhead;
-    if (in_split(ti))
-      cp_async4(smem_u32(sidx + (ti % kHgIdxRing) * kHgN + myslot), idx_row + j0 + ti * kHgN + myslot);
     cp_async_commit();
   };
   if (producer)
@@ -189,23 +218,22 @@ __global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeAr
   {
     // masked slots of the first tiles dequantise zeros, and the P buffer's zero blocks stay 0
     uint4* z = reinterpret_cast<uint4*>(sm + kHgOffRaw);
-    for (int k = tid; k < kHgStages * kHgRawStage / 16; k += kHgThreads) z[k] = make_uint4(0, 0, 0, 0);
+    for (int k = tid; k < kHgRawStages * kHgRawStage / 16; k += kHgThreads) z[k] = make_uint4(0, 0, 0, 0);
     uint4* zp = reinterpret_cast<uint4*>(sm + kHgOffP);
-    for (int k = tid; k < 5 * kHgPBlk / 16; k += kHgThreads) zp[k] = make_uint4(0, 0, 0, 0);
+    for (int k = tid; k < 3 * kHgPBlk / 16; k += kHgThreads) zp[k] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (tid == 0) {
-      for (int s = 0; s < kHgStages; ++s) {
-        mbar_init(bar(H_RAW_FULL + s), kHgProducers);  // one expect_tx arrival per producer warp
+      for (int s = 0; s < kHgRawStages; ++s) {
+        mbar_init(bar(H_RAW_FULL + s), 1);  // the expect_tx arrival of the stage's producer warp
         mbar_init(bar(H_RAW_EMPTY + s), kHgDequantWarps);
-        mbar_init(bar(H_K_FULL + s), kHgDequantWarps);
-        mbar_init(bar(H_K_FREE + s), 1);
       }
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(bar(H_S_FULL + b), 1);
-        mbar_init(bar(H_S_FREE + b), 4);
-        mbar_init(bar(H_P_READY + b), 4);
-        mbar_init(bar(H_PV_DONE + b), 1);
-      }
+      for (int b = 0; b < 2; ++b) mbar_init(bar(H_K_FULL + b), kHgDequantWarps);
+      for (int c = 0; c < 8; ++c) mbar_init(bar(H_K_FREE + c), 1);
+      mbar_init(bar(H_ROPE_FULL), kHgDequantWarps);
+      mbar_init(bar(H_S_FULL), 1);
+      mbar_init(bar(H_S_FREE), 4);
+      mbar_init(bar(H_P_READY), 4);
+      mbar_init(bar(H_PV_DONE), 1);
       mbar_init(bar(H_Q), 1);
       mbar_init(bar(H_DRAIN), 1);
       tc::fence_mbarrier_init_cluster();
@@ -220,8 +248,8 @@ __global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeAr
 
   // Softmax warps place q: lane l < 64 gets dims [0, 256) of head h0 + l, lane 64 + l dims
   // [256, 512), as f16 in TMEM (A of QK); the RoPE dims go to shared memory, rows 0-63 dims
-  // 512..543 and rows 64-127 dims 544..575 (64-byte swizzle). The group's q rows arrive by
-  // one bulk copy per head into the still idle K-tile area.
+  // 512..543 and rows 64-127 dims 544..575 (64-byte swizzle). The q rows arrive by one bulk
+  // copy per head into the still idle K-tile area.
   if (warp < 4) {
     const int half = warp >> 1;
     const int hl = 32 * (warp & 1) + lane;
@@ -268,93 +296,120 @@ __global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeAr
   if (producer) {
     uint16_t* meta = reinterpret_cast<uint16_t*>(sm + kHgOffMeta);
     const uint32_t rowbytes = tens ? uint32_t(kFp8TensorRowBytes) : uint32_t(kFp8RowBytes);
-    int issued = 0;
+    // a row the tensor map does not hold: its gather reads nothing and fills zeros
+    const int32_t oob_row = int32_t(p.num_pages << p.log2_page);
     for (int i = 0; i < ntiles && ok; ++i) {
       ring_step(i);
-      const int st = i % kHgStages;
-      if (!mbar_wait(bar(H_RAW_EMPTY + st), ((i / kHgStages) & 1) ^ 1)) {
-        ok = false;
-        break;
-      }
-      const int32_t idx = idx_of(i);
-      int64_t phys = -1;
-      if (idx != -1) {
-        if (idx < 0 || (idx >> p.log2_page) >= p.stride) {
-          atomicOr(p.err, SMLA_DEVERR_INDEX);
-        } else {
-          const int32_t pg = spage[(i % kHgPageRing) * kHgN + myslot];
-          if (pg < 0 || pg >= p.num_pages)
-            atomicOr(p.err, SMLA_DEVERR_PAGE);
-          else
-            phys = (int64_t(pg) << p.log2_page) + (idx & ((1 << p.log2_page) - 1));
+#pragma unroll 1
+      for (int k = 0; k < 2 && ok; ++k) {
+        const int q = pw + 2 * k;
+        const int u = 4 * i + q, st = u % kHgRawStages;
+        if (!mbar_wait(bar(H_RAW_EMPTY + st), ((u / kHgRawStages) & 1) ^ 1)) {
+          ok = false;
+          break;
         }
+        const int32_t idx = idx_of(i, q);
+        int64_t phys = -1;
+        if (idx != -1) {
+          if (idx < 0 || (idx >> p.log2_page) >= p.stride) {
+            atomicOr(p.err, SMLA_DEVERR_INDEX);
+          } else {
+            const int32_t pg = spage[(i % kHgPageRing) * kHgN + kHgSub * q + lane];
+            if (pg < 0 || pg >= p.num_pages)
+              atomicOr(p.err, SMLA_DEVERR_PAGE);
+            else
+              phys = (int64_t(pg) << p.log2_page) + (idx & ((1 << p.log2_page) - 1));
+          }
+        }
+        const uint32_t vm = __ballot_sync(0xffffffffu, phys >= 0);
+        // lane g < 4 gathers rows 4g..4g+3 of the stage, unless none of them is selected
+        const int32_t y = phys >= 0 ? int32_t(phys) : oob_row;
+        const int32_t y0 = __shfl_sync(0xffffffffu, y, 4 * (lane & 3));
+        const int32_t y1 = __shfl_sync(0xffffffffu, y, 4 * (lane & 3) + 1);
+        const int32_t y2 = __shfl_sync(0xffffffffu, y, 4 * (lane & 3) + 2);
+        const int32_t y3 = __shfl_sync(0xffffffffu, y, 4 * (lane & 3) + 3);
+        uint32_t groups = 0;
+#pragma unroll
+        for (int gq = 0; gq < 4; ++gq) groups |= ((vm >> (4 * gq)) & 15u) ? (1u << gq) : 0u;
+        if (lane == 0 && pw == 0 && k == 0) HTRACE(0, i);
+        if (lane == 0) {
+          meta[(i % kHgMetaRing) * 4 + q] = uint16_t(vm);
+          mbar_arrive_expect_tx(bar(H_RAW_FULL + st), uint32_t(__popc(groups)) * 4u * rowbytes);
+        }
+        __syncwarp();
+        if (lane < 4 && ((groups >> lane) & 1u))
+          tma_gather4(sb + uint32_t(kHgOffRaw) + uint32_t(st * kHgRawStage + lane * kHgGroup), &kv_map, 0, y0, y1,
+                      y2, y3, bar(H_RAW_FULL + st));
       }
-      const uint32_t vm = __ballot_sync(0xffffffffu, phys >= 0);
-      if (lane == 0 && pw == 0) HTRACE(0, i);
-      if (lane == 0) {
-        meta[(i % kHgMetaRing) * kHgProducers + pw] = uint16_t(vm);
-        mbar_arrive_expect_tx(bar(H_RAW_FULL + st), uint32_t(__popc(vm)) * rowbytes);
-      }
-      __syncwarp();
-      if (phys >= 0)
-        bulk_g2s(sb + uint32_t(kHgOffRaw) + uint32_t(st * kHgRawStage + myslot * kHgRawRow),
-                 p.kv + phys * rowbytes, rowbytes, bar(H_RAW_FULL + st));
-      issued = i + 1;
     }
     cp_async_wait<0>();
-    // no bulk copy may land after the CTA has left
-    for (int i = max(0, issued - kHgStages); i < issued; ++i)
-      if (!mbar_wait(bar(H_RAW_FULL + i % kHgStages), (i / kHgStages) & 1)) break;
+    // no copy may land after the CTA has left: wait for this warp's stages among the last
+    // ring's worth
+    const int total = 4 * ntiles;
+    for (int u = max(0, total - kHgRawStages); u < total; ++u)
+      if ((u & 1) == pw && !mbar_wait(bar(H_RAW_FULL + u % kHgRawStages), (u / kHgRawStages) & 1)) break;
   }
   // ------------------------------------------------------------------ MMA issuer
   else if (warp == kHgMmaWarp) {
     if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t kIdQK = tc::idesc_f16_f32(128, 64, false, false);
+      constexpr uint32_t kIdQK = tc::idesc_f16_f32(128, 128, false, false);
       constexpr uint32_t kIdPV = tc::idesc_f16_f32(128, 256, false, true);
       const uint32_t qr = sb + uint32_t(kHgOffQr);
-      auto qk = [&](int i) -> bool {
-        const int st = i % kHgStages, b = i & 1;
-        if (!mbar_wait(bar(H_K_FULL + st), (i / kHgStages) & 1)) return false;
-        if (i >= 2 && !mbar_wait(bar(H_S_FREE + b), ((i - 2) >> 1) & 1)) return false;
+      const uint32_t rope = sb + uint32_t(kHgOffRope);
+      const uint32_t d = tm + kHgTmS;
+      // QK of tile i once its K tile and RoPE block are written and the scores of tile i-1
+      // have been read
+      auto qk_ready = [&](int i) {
+        return mbar_test_wait(bar(H_K_FULL + (i & 1)), (i >> 1) & 1) &&
+               (i == 0 || mbar_test_wait(bar(H_S_FREE), (i - 1) & 1)) && mbar_test_wait(bar(H_ROPE_FULL), i & 1);
+      };
+      auto qk = [&](int i) {
         HTRACE(4, i);
         tc::fence_after();
-        const uint32_t kt = sb + uint32_t(kHgOffK) + uint32_t(st * kHgKtile);
-        const uint32_t d = tm + kHgTmS + 64 * b;
+        const uint32_t kt = sb + uint32_t(kHgOffK) + uint32_t((i & 1) * kHgKLat);
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           tc::mma_ts(d, tm + kHgTmQ + 8 * j, tc::sdesc_sw128(kt + (j >> 2) * kHgPairBlk + (j & 3) * 32, 16, 1024),
                      kIdQK, j > 0);
 #pragma unroll
         for (int j = 0; j < 2; ++j)
-          tc::mma_ss(d, tc::sdesc_sw64(qr + 32 * j, 16, 512), tc::sdesc_sw64(kt + 4 * kHgPairBlk + 32 * j, 16, 512),
-                     kIdQK, 1);
-        tc::commit(bar(H_S_FULL + b));
-        return true;
+          tc::mma_ss(d, tc::sdesc_sw64(qr + 32 * j, 16, 512), tc::sdesc_sw64(rope + 32 * j, 16, 512), kIdQK, 1);
+        tc::commit(bar(H_S_FULL));
       };
-      auto pv = [&](int i) -> bool {
-        const int st = i % kHgStages, b = i & 1;
-        if (!mbar_wait(bar(H_P_READY + b), (i >> 1) & 1)) return false;
+      auto pv = [&](int i) {
         HTRACE(5, i);
         tc::fence_after();
-        const uint32_t kt = sb + uint32_t(kHgOffK) + uint32_t(st * kHgKtile);
-        const uint32_t pa = sb + uint32_t(kHgOffP) + uint32_t((1 + 2 * b) * kHgPBlk);  // P rows
+        const uint32_t kt = sb + uint32_t(kHgOffK) + uint32_t((i & 1) * kHgKLat);
+        const uint32_t pa = sb + uint32_t(kHgOffP) + uint32_t(kHgPBlk);  // P rows
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {  // 16 slots per MMA
+        for (int s = 0; s < 4; ++s) {  // 16 slots per MMA
           // [P; 0] x latent dims [0, 256) -> lanes 0-63; [0; P] x dims [256, 512) -> lanes 64-127
-          tc::mma_ss(tm + kHgTmO, tc::sdesc_sw64(pa + 32 * s, 16, 512),
+          tc::mma_ss(tm + kHgTmO, tc::sdesc_sw128(pa + 32 * s, 16, 1024),
                      tc::sdesc_sw128(kt + 2048 * s, kHgPairBlk, 1024), kIdPV, (i > 0 || s > 0));
-          tc::mma_ss(tm + kHgTmO, tc::sdesc_sw64(pa - kHgPBlk + 32 * s, 16, 512),
-                     tc::sdesc_sw128(kt + 4096 + 2048 * s, kHgPairBlk, 1024), kIdPV, 1);
+          tc::mma_ss(tm + kHgTmO, tc::sdesc_sw128(pa - kHgPBlk + 32 * s, 16, 1024),
+                     tc::sdesc_sw128(kt + 8192 + 2048 * s, kHgPairBlk, 1024), kIdPV, 1);
+          tc::commit(bar(H_K_FREE + 4 * (i & 1) + s));  // rows [16s, 16s+16) of the K tile are free
         }
-        tc::commit(bar(H_K_FREE + st));
-        tc::commit(bar(H_PV_DONE + b));
-        return true;
+        tc::commit(bar(H_PV_DONE));
       };
-      ok = qk(0);
-      if (ok && ntiles > 1) ok = qk(1);
-      for (int i = 0; i < ntiles && ok; ++i) {
-        ok = pv(i);
-        if (ok && i + 2 < ntiles) ok = qk(i + 2);
+      // Issue whichever is ready first: PV of the oldest scored tile, or QK of the next one
+      // (the barriers allow QK at most one tile ahead of PV). PV goes first, so a K buffer
+      // never waits behind a QK whose tile is still being dequantised.
+      int nqk = 0, npv = 0;
+      uint64_t t0 = globaltimer_ns();
+      for (uint32_t it = 0; npv < ntiles; ++it) {
+        if (npv < nqk && mbar_test_wait(bar(H_P_READY), npv & 1)) {
+          pv(npv++);
+        } else if (nqk < ntiles && nqk <= npv + 1 && qk_ready(nqk)) {
+          qk(nqk++);
+        } else {
+          if ((it & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+            ok = false;
+            break;
+          }
+          continue;
+        }
+        t0 = globaltimer_ns();
       }
       // every MMA issued has completed before the tensor memory is released
       tc::commit(bar(H_DRAIN));
@@ -365,77 +420,97 @@ __global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeAr
   // ------------------------------------------------------------------ dequant
   else if (warp >= kHgFirstDequant) {
     const int dtid = tid - 32 * kHgFirstDequant;
+    constexpr int rstride = tens ? kFp8TensorRowBytes : kFp8RowBytes;  // gathered rows, 4 per group
+    auto raw_row = [&](uint32_t stage, int slot) -> uint32_t {
+      return stage + uint32_t((slot >> 2) * kHgGroup + (slot & 3) * rstride);
+    };
+    // RoPE jobs: dims [8rc, 8rc+8) of slot 16q + rslot, q = rq0 + k for k = 0, 1
+    const int rslot = dtid & 15, rc = (dtid >> 4) & 7, rq0 = 2 * (dtid >> 7);
     for (int i = 0; i < ntiles && ok; ++i) {
-      const int st = i % kHgStages;
-      if (!mbar_wait(bar(H_RAW_FULL + st), (i / kHgStages) & 1)) { ok = false; break; }
-      if (dtid == 0) HTRACE(1, i);
-      if (i >= kHgStages && !mbar_wait(bar(H_K_FREE + st), ((i - kHgStages) / kHgStages) & 1)) {
-        ok = false;
-        break;
-      }
-      if (dtid == 0) HTRACE(2, i);
-      const uint32_t raw = sb + uint32_t(kHgOffRaw) + uint32_t(st * kHgRawStage);
-      const uint32_t kt = sb + uint32_t(kHgOffK) + uint32_t(st * kHgKtile);
+      const int b = i & 1;
+      const uint32_t kt = sb + uint32_t(kHgOffK) + uint32_t(b * kHgKLat);
+      uint4 rv0 = make_uint4(0, 0, 0, 0), rv1 = rv0;  // (two names keep them in registers)
+#pragma unroll 1
+      for (int q = 0; q < 4 && ok; ++q) {
+        const int u = 4 * i + q, st = u % kHgRawStages;
+        if (!mbar_wait(bar(H_RAW_FULL + st), (u / kHgRawStages) & 1)) { ok = false; break; }
+        if (dtid == 0 && q == 0) HTRACE(1, i);
+        // rows [16q, 16q+16) of the K buffer are free once that chunk of PV(i-2) is done
+        if (i >= 2 && !mbar_wait(bar(H_K_FREE + 4 * b + q), ((i - 2) >> 1) & 1)) { ok = false; break; }
+        const uint32_t raw = sb + uint32_t(kHgOffRaw) + uint32_t(st * kHgRawStage);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int id = dtid + kHgDequantThreads * k;
-        const int slot = id & 31, ch = id >> 5;  // latent bytes [16ch, 16ch+16) of slot
-        const uint32_t rrow = raw + slot * kHgRawRow;
-        const uint4 v = lds128(rrow + 16 * ch);
-        const float sc = tens ? 1.f : lds_f32(rrow + kScaleOff + 4 * (ch >> 3));
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[8];
-        const __half2 s2 = __float2half2_rn(sc);
+        for (int k = 0; k < 2; ++k) {
+          const int id = dtid + kHgDequantThreads * k;
+          const int slot = id & 15, ch = id >> 4;  // latent bytes [16ch, 16ch+16) of the stage's row
+          const uint32_t rrow = raw_row(raw, slot);
+          const uint4 v = lds128(rrow + 16 * ch);
+          const float sc = tens ? 1.f : lds_f32(rrow + kScaleOff + 4 * (ch >> 3));
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[8];
+          const __half2 s2 = __float2half2_rn(sc);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t lo, hi;
-          e4m3x4_to_f16x4(wv[q], lo, hi);  // exact
-          if constexpr (tens) {  // the scale comes later, in fp32
-            o[2 * q] = lo;
-            o[2 * q + 1] = hi;
-          } else {  // code * scale in f16 (exact for power-of-two scales in f16's range)
-            __half2 a = __hmul2(*reinterpret_cast<const __half2*>(&lo), s2);
-            __half2 b = __hmul2(*reinterpret_cast<const __half2*>(&hi), s2);
-            o[2 * q] = *reinterpret_cast<uint32_t*>(&a);
-            o[2 * q + 1] = *reinterpret_cast<uint32_t*>(&b);
+          for (int e = 0; e < 4; ++e) {
+            uint32_t lo, hi;
+            e4m3x4_to_f16x4(wv[e], lo, hi);  // exact
+            if constexpr (tens) {  // the scale comes later, in fp32
+              o[2 * e] = lo;
+              o[2 * e + 1] = hi;
+            } else {  // code * scale in f16 (exact for power-of-two scales in f16's range)
+              __half2 x = __hmul2(*reinterpret_cast<const __half2*>(&lo), s2);
+              __half2 y = __hmul2(*reinterpret_cast<const __half2*>(&hi), s2);
+              o[2 * e] = *reinterpret_cast<uint32_t*>(&x);
+              o[2 * e + 1] = *reinterpret_cast<uint32_t*>(&y);
+            }
           }
+          // dims [16ch, 16ch+16): block ch/4 mod 4, low rows for ch < 16, high rows after
+          const int rr = kHgN * (ch >> 4) + kHgSub * q + slot;
+          const uint32_t row = kt + ((ch >> 2) & 3) * kHgPairBlk + rr * 128;
+          const int c0 = 2 * (ch & 3);
+          const uint32_t sw = rr & 7;
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + ((c0 ^ sw) << 4)), "r"(o[0]),
+                       "r"(o[1]), "r"(o[2]), "r"(o[3]) : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + (((c0 + 1) ^ sw) << 4)), "r"(o[4]),
+                       "r"(o[5]), "r"(o[6]), "r"(o[7]) : "memory");
         }
-        // dims [16ch, 16ch+16): block ch/4 mod 4, low rows for ch < 16, high rows after
-        const int rr = 32 * (ch >> 4) + slot;
-        const uint32_t row = kt + ((ch >> 2) & 3) * kHgPairBlk + rr * 128;
-        const int c0 = 2 * (ch & 3);
-        const uint32_t sw = rr & 7;
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + ((c0 ^ sw) << 4)), "r"(o[0]),
-                     "r"(o[1]), "r"(o[2]), "r"(o[3]) : "memory");
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + (((c0 + 1) ^ sw) << 4)), "r"(o[4]),
-                     "r"(o[5]), "r"(o[6]), "r"(o[7]) : "memory");
+        if ((q & ~1) == rq0) {  // this thread's RoPE chunk of the stage, kept in registers
+          uint4 v;
+          if constexpr (tens) {  // eight E4M3 codes -> f16 (exact; the scale comes later in fp32)
+            const uint2 cw = lds64(raw_row(raw, rslot) + kLatent + 8 * rc);
+            uint32_t hh[4];
+            e4m3x4_to_f16x4(cw.x, hh[0], hh[1]);
+            e4m3x4_to_f16x4(cw.y, hh[2], hh[3]);
+            v = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+          } else {  // bf16 RoPE -> f16
+            const uint4 x = lds128(raw_row(raw, rslot) + kRopeOffFp8 + 16 * rc);
+            v = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                           bf16x2_to_f16x2(x.w));
+          }
+          if (q & 1)
+            rv1 = v;
+          else
+            rv0 = v;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(H_RAW_EMPTY + st));
       }
-      {
-        const int slot = dtid & 31, rc = dtid >> 5;  // RoPE dims [8rc, 8rc+8) of slot
-        uint4 v;
-        if constexpr (tens) {  // eight E4M3 codes -> f16 (exact; the scale comes later in fp32)
-          const uint2 cw = lds64(raw + slot * kHgRawRow + kLatent + 8 * rc);
-          uint32_t hh[4];
-          e4m3x4_to_f16x4(cw.x, hh[0], hh[1]);
-          e4m3x4_to_f16x4(cw.y, hh[2], hh[3]);
-          v = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-        } else {  // bf16 RoPE -> f16
-          const uint4 rv = lds128(raw + slot * kHgRawRow + kRopeOffFp8 + 16 * rc);
-          v = make_uint4(bf16x2_to_f16x2(rv.x), bf16x2_to_f16x2(rv.y), bf16x2_to_f16x2(rv.z),
-                         bf16x2_to_f16x2(rv.w));
-        }
-        const int rr = 32 * (rc >> 2) + slot, c = rc & 3;
-        const uint32_t dst = kt + 4 * kHgPairBlk + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4);
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
-                     "r"(v.w) : "memory");
+      if (!ok) break;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(H_K_FULL + b));
+      if (dtid == 0) HTRACE(3, i);
+      // the single RoPE block is free once QK of the previous tile has completed
+      if (i >= 1 && !mbar_wait(bar(H_S_FULL), (i - 1) & 1)) { ok = false; break; }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int rr = kHgN * (rc >> 2) + kHgSub * (rq0 + k) + rslot, c = rc & 3;
+        const uint32_t dst = sb + uint32_t(kHgOffRope) + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4);
+        const uint4 v = k ? rv1 : rv0;
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                     : "memory");
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(H_K_FULL + st));
-        mbar_arrive(bar(H_RAW_EMPTY + st));
-      }
-      if (dtid == 0) HTRACE(3, i);
+      if (lane == 0) mbar_arrive(bar(H_ROPE_FULL));
     }
     // all K tiles are dequantised: the split merge, if one follows, may start launching
     if (dtid == 0) pdl_trigger();
@@ -447,20 +522,23 @@ __global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeAr
     const int hl = 32 * pr + lane;
     const int h = h0 + hl;
     const uint32_t lrow = tm + (uint32_t(32 * warp) << 16);
-    const uint32_t* meta = reinterpret_cast<const uint32_t*>(sm + kHgOffMeta);  // 32 slot bits per tile
+    const uint64_t* meta = reinterpret_cast<const uint64_t*>(sm + kHgOffMeta);  // 64 slot bits per tile
     const uint32_t xmine = sb + uint32_t(kHgOffXs) + uint32_t(32 * warp + lane) * kHgXRow;
     const uint32_t xpart = sb + uint32_t(kHgOffXs) + uint32_t(32 * (warp ^ 2) + lane) * kHgXRow;
-    const int bar_x = 1 + pr;                     // both rows of the pair are written
+    const uint32_t mmine = sb + uint32_t(kHgOffXm) + uint32_t(32 * warp + lane) * 4;
+    const uint32_t mpart = sb + uint32_t(kHgOffXm) + uint32_t(32 * (warp ^ 2) + lane) * 4;
+    const int bar_x = 1 + pr;                     // both warps of the pair have written
     const int bar_mine = 3 + 2 * pr + half;       // the partner has read my row
     const int bar_part = 3 + 2 * pr + (half ^ 1); // I have read the partner's row
+    const int bar_max = 7 + pr;                   // both maxima are written
+    const int bar_x2 = 9 + pr;                    // both second halves are written
     float m = -CUDART_INF_F, l = 0.f;
     bool good = true;
 
-    // rescale this thread's O lane (256 columns) by a once PV(i-1) is complete; the TMEM
-    // loads and stores are warp-wide, so the whole warp calls this when any lane needs it
-    auto correct_o = [&](int i, float a) -> bool {
-      if (i > 0 && !mbar_wait(bar(H_PV_DONE + ((i - 1) & 1)), ((i - 1) >> 1) & 1)) return false;
-      tc::fence_after();
+    // rescale this thread's O lane (256 columns) by a; PV of the previous tile is complete.
+    // The TMEM loads and stores are warp-wide: the whole warp calls this when any lane
+    // needs it.
+    auto correct_o = [&](float a) {
 #pragma unroll 1
       for (int k = 0; k < 16; ++k) {
         uint32_t v[16];
@@ -471,59 +549,88 @@ __global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeAr
         tc::st16(lrow + kHgTmO + 16 * k, v);
       }
       tc::wait_st();
-      return true;
     };
 
     bool loop_ok = true;
     for (int i = 0; i < ntiles; ++i) {
-      const int b = i & 1;
-      float s[32];
-      const bool got = good && mbar_wait(bar(H_S_FULL + b), (i >> 1) & 1);
+      // my partial scores of all 64 slots: columns 64 * half of the score block
+      float v[64];
+      const bool got = good && mbar_wait(bar(H_S_FULL), i & 1);
       if (got) {
         tc::fence_after();
-        uint32_t v[32];
-        tc::ld32(lrow + kHgTmS + 64 * b + 32 * half, v);
+        uint32_t w0[32], w1[32];
+        tc::ld32(lrow + kHgTmS + 64 * half, w0);
+        tc::ld32(lrow + kHgTmS + 64 * half + 32, w1);
         tc::wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(v[e]);
+        for (int e = 0; e < 32; ++e) {
+          v[e] = __uint_as_float(w0[e]);
+          v[32 + e] = __uint_as_float(w1[e]);
+        }
         tc::fence_before();
       } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[e] = 0.f;
+        for (int e = 0; e < 64; ++e) v[e] = 0.f;
       }
       __syncwarp();
-      if (lane == 0 && got) mbar_arrive(bar(H_S_FREE + b));
+      if (lane == 0 && got) mbar_arrive(bar(H_S_FREE));
       if (lane == 0 && (warp == 0 || warp == 2)) HTRACE(6 + warp / 2, i);
-      if (i > 0) named_bar(bar_mine, 64);
+      // the low warp finishes slots 0-31 and sends its partials of slots 32-63; the high warp
+      // the other way round (selects keep the arrays in registers)
+      float own[32], send[32];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(xmine + 16 * k), "r"(__float_as_uint(s[4 * k])),
-                     "r"(__float_as_uint(s[4 * k + 1])), "r"(__float_as_uint(s[4 * k + 2])),
-                     "r"(__float_as_uint(s[4 * k + 3])) : "memory");
+      for (int e = 0; e < 32; ++e) {
+        own[e] = half ? v[32 + e] : v[e];
+        send[e] = half ? v[e] : v[32 + e];
+      }
+      // the partner's partials of my 32 slots, in two rounds of 16 through one row each
+      if (i > 0) named_bar(bar_mine, 64);  // the partner has read my previous row
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(xmine + 16 * k), "r"(__float_as_uint(send[4 * k])),
+                     "r"(__float_as_uint(send[4 * k + 1])), "r"(__float_as_uint(send[4 * k + 2])),
+                     "r"(__float_as_uint(send[4 * k + 3])) : "memory");
       if (!named_bar_and(bar_x, 64, got)) {
         loop_ok = false;
         break;
       }
       float x[32];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < 4; ++k) {
         const uint4 xv = lds128(xpart + 16 * k);
         x[4 * k] = __uint_as_float(xv.x); x[4 * k + 1] = __uint_as_float(xv.y);
         x[4 * k + 2] = __uint_as_float(xv.z); x[4 * k + 3] = __uint_as_float(xv.w);
       }
       named_bar_arrive(bar_part, 64);
-      if (lane == 0 && warp == 0) HTRACE(8, i);
-
-      // both warps of the pair add the same two rows (fp32 addition commutes bitwise), so
-      // both get identical scores, maxima and rescale factors
-      const uint32_t msk = meta[i % kHgMetaRing];
+      named_bar(bar_mine, 64);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(xmine + 16 * k),
+                     "r"(__float_as_uint(send[16 + 4 * k])), "r"(__float_as_uint(send[16 + 4 * k + 1])),
+                     "r"(__float_as_uint(send[16 + 4 * k + 2])), "r"(__float_as_uint(send[16 + 4 * k + 3]))
+                     : "memory");
+      named_bar(bar_x2, 64);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 xv = lds128(xpart + 16 * k);
+        x[16 + 4 * k] = __uint_as_float(xv.x); x[16 + 4 * k + 1] = __uint_as_float(xv.y);
+        x[16 + 4 * k + 2] = __uint_as_float(xv.z); x[16 + 4 * k + 3] = __uint_as_float(xv.w);
+      }
+      const uint32_t msk = uint32_t(meta[i % kHgMetaRing] >> (32 * half));
+      float s[32];
       float mx = -CUDART_INF_F;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float v = ((msk >> j) & 1u) ? (s[j] + x[j]) * c2 : -CUDART_INF_F;
-        s[j] = v;
-        mx = fmaxf(mx, v);
+        const float sv = ((msk >> j) & 1u) ? (own[j] + x[j]) * c2 : -CUDART_INF_F;
+        s[j] = sv;
+        mx = fmaxf(mx, sv);
       }
+      named_bar_arrive(bar_part, 64);
+      if (lane == 0 && warp == 0) HTRACE(8, i);
+      // both warps of the pair take the max over all 64 slots
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(mmine), "f"(mx) : "memory");
+      named_bar(bar_max, 64);
+      mx = fmaxf(mx, lds_f32(mpart));
       float a = 1.f;
       const float mn = fmaxf(m, mx);
       if (m == -CUDART_INF_F ? mn != -CUDART_INF_F : mn > m + kHgRescaleThreshold) {
@@ -531,28 +638,25 @@ __global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeAr
         m = mn;
       }
       const float base = m == -CUDART_INF_F ? 0.f : m;
-      // this warp's 16 of the 32 slots
-      float sh[16];  // (selects keep the scores in registers)
-#pragma unroll
-      for (int j = 0; j < 16; ++j) sh[j] = half ? s[16 + j] : s[j];
       float sum = 0.f;
-      uint32_t pw2[8];
+      uint32_t pw2[16];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float p0 = exp2f(sh[2 * j] - base), p1 = exp2f(sh[2 * j + 1] - base);
+      for (int j = 0; j < 16; ++j) {
+        const float p0 = exp2f(s[2 * j] - base), p1 = exp2f(s[2 * j + 1] - base);
         sum += p0 + p1;
         pw2[j] = pack_f16x2(p0, p1);
       }
       l = l * a + sum;
-      // P buffer b is free once PV(i-2) is complete
-      if (i >= 2 && !mbar_wait(bar(H_PV_DONE + b), ((i - 2) >> 1) & 1)) good = false;
-      if (good && i > 0 && __any_sync(0xffffffffu, a != 1.f) && !correct_o(i, a)) good = false;
+      // the P block and O are free once PV of the previous tile is complete
+      if (i >= 1 && !mbar_wait(bar(H_PV_DONE), (i - 1) & 1)) good = false;
+      tc::fence_after();
+      if (good && i > 0 && __any_sync(0xffffffffu, a != 1.f)) correct_o(a);
       if (good) {
-        const uint32_t prow = sb + uint32_t(kHgOffP) + uint32_t((1 + 2 * b) * kHgPBlk) + uint32_t(hl) * 64;
+        const uint32_t prow = sb + uint32_t(kHgOffP) + uint32_t(kHgPBlk) + uint32_t(hl) * 128;
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const int c = 2 * half + k;
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((c ^ ((hl >> 1) & 3)) << 4)),
+        for (int k = 0; k < 4; ++k) {
+          const int c = 4 * half + k;
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((c ^ (hl & 7)) << 4)),
                        "r"(pw2[4 * k]), "r"(pw2[4 * k + 1]), "r"(pw2[4 * k + 2]), "r"(pw2[4 * k + 3])
                        : "memory");
         }
@@ -560,7 +664,7 @@ __global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeAr
       }
       tc::fence_before();
       __syncwarp();
-      if (lane == 0 && good) mbar_arrive(bar(H_P_READY + b));
+      if (lane == 0 && good) mbar_arrive(bar(H_P_READY));
       if (lane == 0 && (warp == 0 || warp == 2)) HTRACE(9 + warp / 2, i);
     }
 
@@ -570,13 +674,12 @@ __global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeAr
       if (ntiles > 0) named_bar(bar_mine, 64);  // the partner has read my last row
       bool fin = good;
       if (fin && ntiles > 0) {
-        const int last = ntiles - 1;
-        fin = mbar_wait(bar(H_PV_DONE + (last & 1)), (last >> 1) & 1);
+        fin = mbar_wait(bar(H_PV_DONE), (ntiles - 1) & 1);
         tc::fence_after();
       }
       asm volatile("st.shared.f32 [%0], %1;" ::"r"(xmine), "f"(l) : "memory");
       ok = named_bar_and(bar_x, 64, fin);
-      if (ok) l += lds_f32(xpart);  // low half + high half in the other warp: same sum order
+      if (ok) l += lds_f32(xpart);  // my half's sum + the other half's: same value in both warps
     }
     if (ok) {
       const int S = p.num_splits;
@@ -614,22 +717,22 @@ __global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeAr
         if (!real) continue;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint32_t* v = v4[j];
+          const uint32_t* vv = v4[j];
           const int col = 256 * half + 64 * k4 + 16 * j;
           if (S == 1) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow_g * kLatent + col);
             uint32_t o[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              o[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * f, __uint_as_float(v[2 * e + 1]) * f);
+              o[e] = pack_bf16x2(__uint_as_float(vv[2 * e]) * f, __uint_as_float(vv[2 * e + 1]) * f);
             dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
           } else {
             float4* dst = reinterpret_cast<float4*>(p.o_part + orow_g * kLatent + col);
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              dst[e] = make_float4(__uint_as_float(v[4 * e]) * f, __uint_as_float(v[4 * e + 1]) * f,
-                                   __uint_as_float(v[4 * e + 2]) * f, __uint_as_float(v[4 * e + 3]) * f);
+              dst[e] = make_float4(__uint_as_float(vv[4 * e]) * f, __uint_as_float(vv[4 * e + 1]) * f,
+                                   __uint_as_float(vv[4 * e + 2]) * f, __uint_as_float(vv[4 * e + 3]) * f);
           }
         }
       }
@@ -651,6 +754,47 @@ __global__ void __launch_bounds__(kHgThreads, 1) decode_hg_kernel(const DecodeAr
 
 }  // namespace
 
+namespace {
+// Tensor map of the cache as [slots, row bytes / 4] 32-bit words, one row per box, for the
+// producers' row gathers. Encoded on the host through the driver entry point; the last one
+// is reused while the cache and its shape stay the same.
+cudaError_t kv_tensor_map(const DecodeArgs& a, CUtensorMap* out) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  thread_local const void* last_kv = nullptr;
+  thread_local int64_t last_slots = -1;
+  thread_local int32_t last_fmt = -1;
+  thread_local CUtensorMap last_map;
+  const int64_t slots = a.num_pages << a.log2_page;
+  if (last_kv == a.kv && last_slots == slots && last_fmt == a.kv_format) {
+    *out = last_map;
+    return cudaSuccess;
+  }
+  const cuuint64_t row = a.kv_format == SMLA_KV_FP8_TENSOR ? kFp8TensorRowBytes : kFp8RowBytes;
+  const cuuint64_t dims[2] = {row / 4, cuuint64_t(slots)};
+  const cuuint64_t strides[1] = {row};
+  const cuuint32_t box[2] = {cuuint32_t(row / 4), 1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(a.kv), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  last_kv = a.kv;
+  last_slots = slots;
+  last_fmt = a.kv_format;
+  last_map = *out;
+  return cudaSuccess;
+}
+}  // namespace
+
 cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s) {
   static int configured_dev = -1;
   int dev = 0;
@@ -663,11 +807,16 @@ cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
+  // row coordinates of the gathers are 32-bit, and one past the last slot marks a masked row
+  if ((a.num_pages << a.log2_page) >= (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
+  alignas(64) CUtensorMap map;
+  const cudaError_t e = kv_tensor_map(a, &map);
+  if (e != cudaSuccess) return e;
   const int64_t grid = int64_t(a.T) * a.num_splits * ((a.H + 63) / 64);
   if (a.kv_format == SMLA_KV_FP8_TENSOR)
-    decode_hg_kernel<true><<<static_cast<unsigned>(grid), kHgThreads, kSmemHg, s>>>(a);
+    decode_hg_kernel<true><<<static_cast<unsigned>(grid), kHgThreads, kSmemHg, s>>>(a, map);
   else
-    decode_hg_kernel<false><<<static_cast<unsigned>(grid), kHgThreads, kSmemHg, s>>>(a);
+    decode_hg_kernel<false><<<static_cast<unsigned>(grid), kHgThreads, kSmemHg, s>>>(a, map);
   return cudaGetLastError();
 }
 

@@ -32,15 +32,12 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t s);
-cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
 // One CTA per (token, split, group of 64 heads); FP8 caches.
 cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);
 
-// The tensor-core kernels serve the FP8 caches with at least kTcMinHeads heads: the
-// head-group kernel up to kHgMaxHeads, the pair kernel above.
-constexpr int kTcMinHeads = 64;
-constexpr int kHgMaxHeads = 64;
+// The tensor-core head-group kernel serves the FP8 caches with at least this many heads.
+constexpr int kHgMinHeads = 64;
 cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, float kv_scale, const void* latent,
                         const void* rope, const int64_t* slot_mapping, int64_t n, void* kv,
                         int64_t num_slots, cudaStream_t s);

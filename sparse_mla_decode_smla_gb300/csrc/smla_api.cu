@@ -79,24 +79,20 @@ struct Plan {
   size_t lse_off, o_off, bytes;
 };
 
-bool use_tc(const smla_desc* d) {
+// The FP8 caches with 64 or more heads take the tensor-core head-group kernel.
+bool use_hg(const smla_desc* d) {
   return (d->kv_format == SMLA_KV_FP8_DS || d->kv_format == SMLA_KV_FP8_TENSOR) &&
-         d->num_heads >= smla::kTcMinHeads;
+         d->num_heads >= smla::kHgMinHeads;
 }
-// 64 heads fit one SM (the head-group kernel); 80..128 heads take a CTA pair.
-bool use_hg(const smla_desc* d) { return use_tc(d) && d->num_heads <= smla::kHgMaxHeads; }
 
 Plan make_plan(const smla_desc* d, int num_sms) {
   int S = d->num_splits;
   if (S == 0) {
     S = 1;
     if (use_hg(d)) {
-      // one CTA per (token, split), one per SM: fill one wave at most
-      if (d->num_tokens < num_sms) S = num_sms / d->num_tokens;
-    } else if (use_tc(d)) {
-      // one CTA pair per (token, split), one pair per two SMs: fill one wave at most
-      const int pairs = num_sms / 2;
-      if (d->num_tokens < pairs) S = pairs / d->num_tokens;
+      // one CTA per (token, split, group of 64 heads), one per SM: fill one wave at most
+      const int units = d->num_tokens * ((d->num_heads + 63) / 64);
+      if (units < num_sms) S = num_sms / units;
     } else {
       const int units = d->num_tokens * (d->num_heads / 16);
       if (units < num_sms) S = (2 * num_sms + units - 1) / units;
@@ -197,6 +193,9 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
                         float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   smla_status st = check_desc(d);
   if (st != SMLA_OK) return st;
+  // the head-group kernel gathers rows by 32-bit row coordinates (one past the last slot
+  // marks a masked row)
+  if (use_hg(d) && (d->num_pages * d->page_size) >= (int64_t(1) << 31) - 1) return SMLA_ERR_SHAPE;
   if (!q || !kv_cache || !page_table || !topk || !out || !workspace) return SMLA_ERR_NULL;
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(topk, 16) || !aligned(out, 16) ||
       !aligned(page_table, 4) || !aligned(workspace, kWsAlign) ||
@@ -221,9 +220,7 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
   a.split_len = plan.split_len;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (t_ev_start && cudaEventRecord(t_ev_start, s) != cudaSuccess) return SMLA_ERR_CUDA;
-  const cudaError_t e = use_hg(d)   ? smla::launch_decode_hg(a, s)
-                            : use_tc(d) ? smla::launch_decode_tc(a, s)
-                                        : smla::launch_decode_mma(a, sms, s);
+  const cudaError_t e = use_hg(d) ? smla::launch_decode_hg(a, s) : smla::launch_decode_mma(a, sms, s);
   if (e != cudaSuccess) return SMLA_ERR_CUDA;
   if (t_ev_stop && cudaEventRecord(t_ev_stop, s) != cudaSuccess) return SMLA_ERR_CUDA;
   if (plan.num_splits > 1 && smla::launch_merge(a, s) != cudaSuccess) return SMLA_ERR_CUDA;

@@ -1,4 +1,4 @@
-// tcgen05 (5th-generation tensor core), TMEM and cluster helpers for sm_103a.
+// tcgen05 (5th-generation tensor core) and TMEM helpers for sm_103a.
 #pragma once
 
 #include <stdint.h>
@@ -133,41 +133,12 @@ __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16]) {
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// ---------------------------------------------------------------- cluster / DSMEM
+// ---------------------------------------------------------------- mbarrier init
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Shared::cluster address of `laddr` (a shared::cta address) in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa(uint32_t laddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(laddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
+// Makes mbarrier initialisations visible to the async proxy (TMA, tensor core) and to other
+// threads before first use.
 __device__ __forceinline__ void fence_mbarrier_init_cluster() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-// 16-byte store into another CTA's shared memory, completing 16 bytes on its mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t raddr, uint32_t a, uint32_t b, uint32_t c,
-                                            uint32_t d, uint32_t rbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-          raddr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar)
-      : "memory");
-}
-__device__ __forceinline__ void st_async_b32(uint32_t raddr, uint32_t a, uint32_t rbar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(raddr),
-               "r"(a), "r"(rbar)
-               : "memory");
 }
 
 }  // namespace tc

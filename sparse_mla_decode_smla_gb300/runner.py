@@ -59,11 +59,10 @@ class DeviceDecode:
         self.workspace = torch.zeros((ws + 255) // 256 * 256 // 4, dtype=torch.int32, device=device)
         self.out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((T, H), dtype=torch.float32, device=device) if with_lse else None
-        # the decode kernel the library dispatches to for this batch (the FP8 caches take the
-        # head-group kernel at 64 heads and the CTA-pair kernel at 80..128)
+        # the decode kernel the library dispatches to for this batch (the FP8 caches with 64
+        # or more heads take the tensor-core head-group kernel)
         fp8 = w.kv_format in ("fp8_ds", "fp8_tensor")
-        self.kernel_name = ("decode_hg_kernel" if fp8 and H == 64 else
-                            "decode_tc_kernel" if fp8 and H > 64 else "decode_mma_kernel")
+        self.kernel_name = "decode_hg_kernel" if fp8 and H >= 64 else "decode_mma_kernel"
 
     def run(self, stream=None):
         decode(self.desc, self.q, self.kv, self.page_table, self.topk, self.req_id, self.sink,
