@@ -217,6 +217,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
+// TMA load of the box at (x, y) of a 2-D tensor map into dst (aligned as the map's swizzle
+// requires), counting the box bytes on bar; elements outside the tensor read as zeros.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];\n" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
 // TMA gather of rows y0..y3 of a 2-D tensor map (columns [x, x + box width)) into four
 // consecutive rows at dst (128-byte aligned), counting the box bytes on bar. A row outside
 // the tensor is not read; its bytes are filled with zeros.

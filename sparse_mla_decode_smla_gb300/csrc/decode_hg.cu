@@ -138,14 +138,16 @@ static_assert(kHgOffK % 1024 == 0 && kHgKLat % 1024 == 0 && kHgOffP % 1024 == 0 
                   kHgOffQr % 512 == 0 && kHgOffRaw % 128 == 0 && kHgOffBars % 8 == 0 && kHgGroup % 128 == 0 &&
                   kHgGroup >= 4 * kFp8RowBytes,
               "swizzle atoms: 1024-byte (128-byte swizzle) and 512-byte (64-byte swizzle) aligned");
-// q staging at start-up: 64 rows of 1152 bytes (+16 for conflict-free 16-byte reads) in the
-// K-tile area, which the pipeline first writes after the start-up barrier
-constexpr uint32_t kHgQRow = 1168;
-static_assert(64 * kHgQRow <= kHgOffRope, "q staging fits in the K-tile area");
+// q staging at start-up, in the K-tile area (first written by the pipeline after the
+// start-up barriers): nine 128-byte-swizzled boxes of [64 heads x 64 dims] bf16
+constexpr uint32_t kHgQBox = 64 * 128;
+constexpr uint32_t kHgQBytes = 9 * kHgQBox;
+static_assert(kHgQBytes <= kHgOffRope, "q staging fits in the K-tile area");
 
 template <bool TENS>
 __global__ void __launch_bounds__(kHgThreads, 1)
-    decode_hg_kernel(const DecodeArgs p, const __grid_constant__ CUtensorMap kv_map) {
+    decode_hg_kernel(const DecodeArgs p, const __grid_constant__ CUtensorMap kv_map,
+                     const __grid_constant__ CUtensorMap q_map) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
@@ -238,6 +240,13 @@ __global__ void __launch_bounds__(kHgThreads, 1)
       mbar_init(bar(H_DRAIN), 1);
       tc::fence_mbarrier_init_cluster();
       if (!req_ok && split == 0 && g == 0) atomicOr(p.err, SMLA_DEVERR_INDEX);
+      // the group's q rows [t H + h0, + 64) as nine 64-dim boxes; they land while the
+      // producers prime their index and page rings (rows past the group are not used)
+      if (nq > 0) {
+        mbar_arrive_expect_tx(bar(H_Q), kHgQBytes);
+        for (int bx = 0; bx < 9; ++bx)
+          tma_load_2d(sb + uint32_t(kHgOffK) + bx * kHgQBox, &q_map, 64 * bx, t * p.H + h0, bar(H_Q));
+      }
     }
     if (warp == kHgMmaWarp) tc::alloc(sb + uint32_t(kHgOffTmem), 512);
     tc::fence_before();
@@ -248,17 +257,16 @@ __global__ void __launch_bounds__(kHgThreads, 1)
 
   // Softmax warps place q: lane l < 64 gets dims [0, 256) of head h0 + l, lane 64 + l dims
   // [256, 512), as f16 in TMEM (A of QK); the RoPE dims go to shared memory, rows 0-63 dims
-  // 512..543 and rows 64-127 dims 544..575 (64-byte swizzle). The q rows arrive by one bulk
-  // copy per head into the still idle K-tile area.
+  // 512..543 and rows 64-127 dims 544..575 (64-byte swizzle). Box b of the staged q holds
+  // dims [64b, 64b+64) of the 64 heads, 16-byte chunk c of head row r at chunk c ^ (r & 7).
   if (warp < 4) {
     const int half = warp >> 1;
     const int hl = 32 * (warp & 1) + lane;
     const uint32_t lrow = tm + (uint32_t(32 * warp) << 16);
-    const uint32_t qs = sb + uint32_t(kHgOffK) + uint32_t(hl) * kHgQRow;
-    if (tid == 0 && nq > 0) mbar_arrive_expect_tx(bar(H_Q), uint32_t(nq) * (2 * kDim));
-    if (half == 0 && hl < nq)
-      bulk_g2s(qs, reinterpret_cast<const uint8_t*>(p.q) + (int64_t(t) * p.H + h0 + hl) * (2 * kDim), 2 * kDim,
-               bar(H_Q));
+    const uint32_t qs = sb + uint32_t(kHgOffK) + uint32_t(hl) * 128;
+    auto qchunk = [&](int dim) -> uint32_t {  // 8 dims [dim, dim + 8) of head hl
+      return qs + (dim >> 6) * kHgQBox + ((((dim >> 3) & 7) ^ (hl & 7)) << 4);
+    };
     const bool got = nq == 0 || mbar_wait(bar(H_Q), 0);
     if (!got && lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
     const bool have = got && hl < nq;
@@ -268,7 +276,7 @@ __global__ void __launch_bounds__(kHgThreads, 1)
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (have) v = lds128(qs + 512 * half + 64 * ch + 16 * k);
+        if (have) v = lds128(qchunk(256 * half + 32 * ch + 8 * k));
         wv[4 * k] = bf16x2_to_f16x2(v.x); wv[4 * k + 1] = bf16x2_to_f16x2(v.y);
         wv[4 * k + 2] = bf16x2_to_f16x2(v.z); wv[4 * k + 3] = bf16x2_to_f16x2(v.w);
       }
@@ -279,7 +287,7 @@ __global__ void __launch_bounds__(kHgThreads, 1)
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint4 v = make_uint4(0, 0, 0, 0);
-      if (have) v = lds128(qs + 2 * kLatent + 64 * half + 16 * c);
+      if (have) v = lds128(qchunk(kLatent + 32 * half + 8 * c));
       const uint32_t dst = sb + uint32_t(kHgOffQr) + row * 64 + ((c ^ ((row >> 1) & 3)) << 4);
       asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(bf16x2_to_f16x2(v.x)),
                    "r"(bf16x2_to_f16x2(v.y)), "r"(bf16x2_to_f16x2(v.z)), "r"(bf16x2_to_f16x2(v.w))
@@ -758,7 +766,7 @@ namespace {
 // Tensor map of the cache as [slots, row bytes / 4] 32-bit words, one row per box, for the
 // producers' row gathers. Encoded on the host through the driver entry point; the last one
 // is reused while the cache and its shape stay the same.
-cudaError_t kv_tensor_map(const DecodeArgs& a, CUtensorMap* out) {
+cudaError_t tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -769,6 +777,13 @@ cudaError_t kv_tensor_map(const DecodeArgs& a, CUtensorMap* out) {
       return cudaErrorNotSupported;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
+  *out = encode;
+  return cudaSuccess;
+}
+
+cudaError_t kv_tensor_map(const DecodeArgs& a, CUtensorMap* out) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (tensor_map_encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
   thread_local const void* last_kv = nullptr;
   thread_local int64_t last_slots = -1;
   thread_local int32_t last_fmt = -1;
@@ -793,6 +808,32 @@ cudaError_t kv_tensor_map(const DecodeArgs& a, CUtensorMap* out) {
   last_map = *out;
   return cudaSuccess;
 }
+
+// Tensor map of q as [T H rows, 576] bf16 with [64 rows x 64 dims] boxes, 128-byte swizzle.
+cudaError_t q_tensor_map(const DecodeArgs& a, CUtensorMap* out) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (tensor_map_encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
+  thread_local const void* last_q = nullptr;
+  thread_local int64_t last_rows = -1;
+  thread_local CUtensorMap last_map;
+  const int64_t rows = int64_t(a.T) * a.H;
+  if (last_q == a.q && last_rows == rows) {
+    *out = last_map;
+    return cudaSuccess;
+  }
+  const cuuint64_t dims[2] = {cuuint64_t(kDim), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(2 * kDim)};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.q), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  last_q = a.q;
+  last_rows = rows;
+  last_map = *out;
+  return cudaSuccess;
+}
 }  // namespace
 
 cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s) {
@@ -810,13 +851,15 @@ cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s) {
   // row coordinates of the gathers are 32-bit, and one past the last slot marks a masked row
   if ((a.num_pages << a.log2_page) >= (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap map;
-  const cudaError_t e = kv_tensor_map(a, &map);
+  alignas(64) CUtensorMap qmap;
+  cudaError_t e = kv_tensor_map(a, &map);
+  if (e == cudaSuccess) e = q_tensor_map(a, &qmap);
   if (e != cudaSuccess) return e;
   const int64_t grid = int64_t(a.T) * a.num_splits * ((a.H + 63) / 64);
   if (a.kv_format == SMLA_KV_FP8_TENSOR)
-    decode_hg_kernel<true><<<static_cast<unsigned>(grid), kHgThreads, kSmemHg, s>>>(a, map);
+    decode_hg_kernel<true><<<static_cast<unsigned>(grid), kHgThreads, kSmemHg, s>>>(a, map, qmap);
   else
-    decode_hg_kernel<false><<<static_cast<unsigned>(grid), kHgThreads, kSmemHg, s>>>(a, map);
+    decode_hg_kernel<false><<<static_cast<unsigned>(grid), kHgThreads, kSmemHg, s>>>(a, map, qmap);
   return cudaGetLastError();
 }
 
