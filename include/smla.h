@@ -107,9 +107,8 @@ smla_status smla_workspace_size(const smla_desc* d, size_t* bytes);
  *   q          [T, H, 576] bf16, 16-byte aligned; dims 0..511 pair with the latent,
  *              512..575 with the RoPE part.
  *   kv_cache   [num_pages, P, R] bytes, R = 656 (FP8_DS), 576 (FP8_TENSOR) or 1152 (BF16),
- *              16-byte aligned. With an FP8 cache and 64 heads, num_pages * P must stay
- *              below 2^31 - 1 (SMLA_ERR_SHAPE otherwise): rows are gathered by 32-bit row
- *              coordinates.
+ *              16-byte aligned. num_pages * P must stay below 2^31 - 1 (SMLA_ERR_SHAPE
+ *              otherwise): rows are gathered by 32-bit row coordinates.
  *   page_table [B, page_table_stride] int32: request-local page -> physical page.
  *   topk       [T, K] int32, 16-byte aligned: request-local slot indices, -1 = padding.
  *              Index i of request r lives in physical slot

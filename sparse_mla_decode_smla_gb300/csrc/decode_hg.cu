@@ -53,8 +53,6 @@
 // Every wait is bounded in time; a wait that gives up sets SMLA_DEVERR_TIMEOUT. The two
 // warps of a head pair meet at named barriers that also AND their status, so both leave the
 // tile loop at the same barrier and neither waits for a partner that has left.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -762,80 +760,6 @@ __global__ void __launch_bounds__(kHgThreads, 1)
 
 }  // namespace
 
-namespace {
-// Tensor map of the cache as [slots, row bytes / 4] 32-bit words, one row per box, for the
-// producers' row gathers. Encoded on the host through the driver entry point; the last one
-// is reused while the cache and its shape stay the same.
-cudaError_t tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (!encode) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-      return cudaErrorNotSupported;
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
-  *out = encode;
-  return cudaSuccess;
-}
-
-cudaError_t kv_tensor_map(const DecodeArgs& a, CUtensorMap* out) {
-  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (tensor_map_encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
-  thread_local const void* last_kv = nullptr;
-  thread_local int64_t last_slots = -1;
-  thread_local int32_t last_fmt = -1;
-  thread_local CUtensorMap last_map;
-  const int64_t slots = a.num_pages << a.log2_page;
-  if (last_kv == a.kv && last_slots == slots && last_fmt == a.kv_format) {
-    *out = last_map;
-    return cudaSuccess;
-  }
-  const cuuint64_t row = a.kv_format == SMLA_KV_FP8_TENSOR ? kFp8TensorRowBytes : kFp8RowBytes;
-  const cuuint64_t dims[2] = {row / 4, cuuint64_t(slots)};
-  const cuuint64_t strides[1] = {row};
-  const cuuint32_t box[2] = {cuuint32_t(row / 4), 1};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(a.kv), dims, strides, box,
-                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  last_kv = a.kv;
-  last_slots = slots;
-  last_fmt = a.kv_format;
-  last_map = *out;
-  return cudaSuccess;
-}
-
-// Tensor map of q as [T H rows, 576] bf16 with [64 rows x 64 dims] boxes, 128-byte swizzle.
-cudaError_t q_tensor_map(const DecodeArgs& a, CUtensorMap* out) {
-  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (tensor_map_encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
-  thread_local const void* last_q = nullptr;
-  thread_local int64_t last_rows = -1;
-  thread_local CUtensorMap last_map;
-  const int64_t rows = int64_t(a.T) * a.H;
-  if (last_q == a.q && last_rows == rows) {
-    *out = last_map;
-    return cudaSuccess;
-  }
-  const cuuint64_t dims[2] = {cuuint64_t(kDim), cuuint64_t(rows)};
-  const cuuint64_t strides[1] = {cuuint64_t(2 * kDim)};
-  const cuuint32_t box[2] = {64, 64};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.q), dims, strides, box,
-                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  last_q = a.q;
-  last_rows = rows;
-  last_map = *out;
-  return cudaSuccess;
-}
-}  // namespace
-
 cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s) {
   static int configured_dev = -1;
   int dev = 0;
@@ -848,12 +772,10 @@ cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  // row coordinates of the gathers are 32-bit, and one past the last slot marks a masked row
-  if ((a.num_pages << a.log2_page) >= (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap map;
   alignas(64) CUtensorMap qmap;
-  cudaError_t e = kv_tensor_map(a, &map);
-  if (e == cudaSuccess) e = q_tensor_map(a, &qmap);
+  cudaError_t e = kv_gather_map(a, &map);
+  if (e == cudaSuccess) e = q_tile_map(a, &qmap);
   if (e != cudaSuccess) return e;
   const int64_t grid = int64_t(a.T) * a.num_splits * ((a.H + 63) / 64);
   if (a.kv_format == SMLA_KV_FP8_TENSOR)

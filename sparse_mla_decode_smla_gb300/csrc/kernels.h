@@ -1,6 +1,7 @@
 // Internal launchers of the sparse MLA decode library (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -35,6 +36,15 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t s);
 // One CTA per (token, split, group of 64 heads); FP8 caches.
 cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);
+
+// Row gathers (TMA tile::gather4) address the cache by 32-bit row coordinates, and one past
+// the last slot marks a masked row: caches must hold fewer slots than this.
+constexpr int64_t kMaxGatherSlots = (int64_t(1) << 31) - 1;
+int kv_row_bytes(int32_t kv_format);
+// Tensor map of the cache as [slots, row bytes / 8] 8-byte words with one-row boxes.
+cudaError_t kv_gather_map(const DecodeArgs& a, CUtensorMap* out);
+// Tensor map of q as [T H rows, 576] bf16 with [64 rows x 64 dims] boxes, 128-byte swizzle.
+cudaError_t q_tile_map(const DecodeArgs& a, CUtensorMap* out);
 
 // The tensor-core head-group kernel serves the FP8 caches with at least this many heads.
 constexpr int kHgMinHeads = 64;

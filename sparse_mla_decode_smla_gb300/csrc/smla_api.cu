@@ -193,9 +193,8 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
                         float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   smla_status st = check_desc(d);
   if (st != SMLA_OK) return st;
-  // the head-group kernel gathers rows by 32-bit row coordinates (one past the last slot
-  // marks a masked row)
-  if (use_hg(d) && (d->num_pages * d->page_size) >= (int64_t(1) << 31) - 1) return SMLA_ERR_SHAPE;
+  // rows are gathered by 32-bit row coordinates (one past the last slot marks a masked row)
+  if (d->num_pages * d->page_size >= smla::kMaxGatherSlots) return SMLA_ERR_SHAPE;
   if (!q || !kv_cache || !page_table || !topk || !out || !workspace) return SMLA_ERR_NULL;
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(topk, 16) || !aligned(out, 16) ||
       !aligned(page_table, 4) || !aligned(workspace, kWsAlign) ||

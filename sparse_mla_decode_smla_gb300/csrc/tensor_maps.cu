@@ -1,0 +1,89 @@
+// Host-side TMA tensor maps of the decode inputs, encoded through the driver entry point
+// (no link against the driver library). The last map of each kind is reused while its
+// tensor and shape stay the same.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace smla {
+namespace {
+
+cudaError_t encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = encode;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+int kv_row_bytes(int32_t kv_format) {
+  return kv_format == SMLA_KV_FP8_TENSOR ? kFp8TensorRowBytes
+                                         : (kv_format == SMLA_KV_FP8_DS ? kFp8RowBytes : kBf16RowBytes);
+}
+
+cudaError_t kv_gather_map(const DecodeArgs& a, CUtensorMap* out) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
+  thread_local const void* last_kv = nullptr;
+  thread_local int64_t last_slots = -1;
+  thread_local int32_t last_fmt = -1;
+  thread_local CUtensorMap last_map;
+  const int64_t slots = a.num_pages << a.log2_page;
+  if (slots >= kMaxGatherSlots) return cudaErrorInvalidValue;
+  if (last_kv == a.kv && last_slots == slots && last_fmt == a.kv_format) {
+    *out = last_map;
+    return cudaSuccess;
+  }
+  const cuuint64_t row = cuuint64_t(kv_row_bytes(a.kv_format));
+  const cuuint64_t dims[2] = {row / 8, cuuint64_t(slots)};
+  const cuuint64_t strides[1] = {row};
+  const cuuint32_t box[2] = {cuuint32_t(row / 8), 1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(a.kv), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  last_kv = a.kv;
+  last_slots = slots;
+  last_fmt = a.kv_format;
+  last_map = *out;
+  return cudaSuccess;
+}
+
+cudaError_t q_tile_map(const DecodeArgs& a, CUtensorMap* out) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
+  thread_local const void* last_q = nullptr;
+  thread_local int64_t last_rows = -1;
+  thread_local CUtensorMap last_map;
+  const int64_t rows = int64_t(a.T) * a.H;
+  if (last_q == a.q && last_rows == rows) {
+    *out = last_map;
+    return cudaSuccess;
+  }
+  const cuuint64_t dims[2] = {cuuint64_t(kDim), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(2 * kDim)};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.q), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  last_q = a.q;
+  last_rows = rows;
+  last_map = *out;
+  return cudaSuccess;
+}
+
+}  // namespace smla

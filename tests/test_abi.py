@@ -88,6 +88,15 @@ def test_decode_rejects_null_and_misaligned_pointers(L):
     assert _decode_status(L, _desc(num_tokens=9, num_requests=2, next_n=4)) == 2
 
 
+def test_decode_rejects_caches_beyond_32_bit_row_coordinates(L):
+    # rows are gathered by 32-bit row coordinates, one past the last slot marking a masked
+    # row: num_pages * page_size must stay below 2^31 - 1
+    # (rejected before any device call; a cache below the limit would go on to launch, so it
+    # is not tried here with these dummy pointers)
+    assert _decode_status(L, _desc(num_pages=1 << 25, page_size=64)) == 2  # 2^31 slots
+    assert _decode_status(L, _desc(num_pages=1 << 31, page_size=1)) == 2   # 2^31 slots
+
+
 def test_pack_rejects_bad_arguments_on_host(L):
     P = ctypes.c_void_p
     assert L.smla_pack_kv(7, 0, P(16), P(16), P(16), 4, P(16), 4, None) == 4
