@@ -59,10 +59,12 @@ def measured_peaks() -> dict:
 # The 16k-context and 8k-16k-context captures gather exactly as many rows (tokens x
 # valid indices) as the full workloads; only the pool they are drawn from is smaller.
 TRAFFIC = {
-    ("fp8_T256_H16_K2048_ctx8k-128k_pad20", "decode_mma_kernel"): (330152960, "1cdb68fa6d5af8ec"),
+    ("fp8_T32_H64_K2048_ctx1k-32k", "decode_hg_kernel"): (52511744, "f7f1cf906c5e1750"),
+    ("fp8_T128_H128_K2048_ctx64k_sink", "decode_hg_kernel"): (229955328, "f7f1cf906c5e1750"),
+    ("fp8_T256_H16_K2048_ctx8k-128k_pad20", "decode_mma_kernel"): (330279936, "bcaa46e6fd6f8f7e"),
 }
 KERNEL_SOURCES = {
-    "decode_hg_kernel": ("common.cuh", "kernels.h", "tcgen05.cuh", "decode_hg.cu"),
+    "decode_hg_kernel": ("common.cuh", "kernels.h", "tcgen05.cuh", "decode_hg.cu", "tensor_maps.cu"),
     "decode_mma_kernel": ("common.cuh", "kernels.h", "decode_mma.cu"),
 }
 

@@ -50,9 +50,11 @@ cudaError_t kv_gather_map(const DecodeArgs& a, CUtensorMap* out) {
   const cuuint64_t strides[1] = {row};
   const cuuint32_t box[2] = {cuuint32_t(row / 8), 1};
   const cuuint32_t estr[2] = {1, 1};
+  // no L2 promotion: a row sits at an arbitrary offset, and promoting its fetches to 256-byte
+  // lines would read about 3.5 lines (900 bytes) of HBM per 656-byte row
   const CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(a.kv), dims, strides, box,
                             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   last_kv = a.kv;
   last_slots = slots;
