@@ -535,16 +535,18 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
   }
 }
 
-// Merge of split partials by log-sum-exp, then the sink (SGLang PR #24692 "关键文件":
-// _merge_partial_attn, _apply_attn_sink). One CTA per (token, 16 heads).
-// Split merge: one warp per (token, head). Lane s (and s + 32) reads lse_s; the warp
-// reduces M = max_s lse_s and W = sum_s e^{lse_s - M}; then every lane accumulates 16 of
-// the 512 output dims over the splits with four coalesced 16-byte loads per split.
+// Split merge (SGLang PR #24692 "关键文件": _merge_partial_attn, then _apply_attn_sink).
+// One warp per (token, head, quarter of the 512 output dims): the lanes reduce
+// M = max_s lse_s and W = sum_s e^{lse_s - M} (every quarter's warp the same way), then every
+// lane accumulates 4 of the quarter's 128 dims over the splits, one 16-byte load per split.
+// Four warps per row keep more loads in flight than one.
 constexpr int kMergeWarps = 8;
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const DecodeArgs p) {
   pdl_wait();  // the decode grid's partials are complete and visible
   const int lane = threadIdx.x & 31;
-  const int64_t row = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);  // t * H + h
+  const int64_t wid = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  const int64_t row = wid >> 2;  // t * H + h
+  const int quarter = int(wid & 3);
   if (row >= int64_t(p.T) * p.H) return;
   const int t = int(row / p.H), h = int(row % p.H);
   const int S = p.num_splits;
@@ -567,32 +569,24 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const DecodeArg
     lse = fmaxf(lse0, sg) + log1pf(expf(-fabsf(lse0 - sg)));
     f *= expf(lse0 - lse);
   }
-  if (lane == 0 && p.lse) p.lse[row] = lse;
+  if (quarter == 0 && lane == 0 && p.lse) p.lse[row] = lse;
 
-  float4 acc[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* op = reinterpret_cast<const float4*>(p.o_part + (int64_t(t) * S * p.H + h) * kLatent) + lane;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* op =
+      reinterpret_cast<const float4*>(p.o_part + (int64_t(t) * S * p.H + h) * kLatent + 128 * quarter) + lane;
   const int64_t sstride = int64_t(p.H) * (kLatent / 4);  // float4 between splits
-#pragma unroll 2
+#pragma unroll 4
   for (int s = 0; s < S; ++s) {
     const float wt = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
     if (wt == 0.f) continue;  // uniform across the warp
-    float4 o[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) o[k] = __ldcs(op + s * sstride + 32 * k);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      acc[k].x = fmaf(wt, o[k].x, acc[k].x);
-      acc[k].y = fmaf(wt, o[k].y, acc[k].y);
-      acc[k].z = fmaf(wt, o[k].z, acc[k].z);
-      acc[k].w = fmaf(wt, o[k].w, acc[k].w);
-    }
+    const float4 o = __ldcs(op + s * sstride);
+    acc.x = fmaf(wt, o.x, acc.x);
+    acc.y = fmaf(wt, o.y, acc.y);
+    acc.z = fmaf(wt, o.z, acc.z);
+    acc.w = fmaf(wt, o.w, acc.w);
   }
-  uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + row * kLatent) + lane;
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-    dst[32 * k] = make_uint2(pack_bf16x2(acc[k].x * f, acc[k].y * f), pack_bf16x2(acc[k].z * f, acc[k].w * f));
+  uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + row * kLatent + 128 * quarter) + lane;
+  *dst = make_uint2(pack_bf16x2(acc.x * f, acc.y * f), pack_bf16x2(acc.z * f, acc.w * f));
 }
 
 template <int FMT>
@@ -625,7 +619,7 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
   // launched with programmatic stream serialisation: its launch overlaps the decode grid's
   // tail, and the kernel waits (pdl_wait) for the decode results before reading them
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps));
+  cfg.gridDim = dim3(static_cast<unsigned>((4 * rows + kMergeWarps - 1) / kMergeWarps));
   cfg.blockDim = dim3(32 * kMergeWarps);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;

@@ -226,9 +226,25 @@ def test_split_count_invariance(small_cases, wi):
         assert_parity(out, lse, ref)
 
 
-def test_unselected_rows_are_never_read(small_cases):
+@pytest.mark.parametrize("heads", [16, 64])
+def test_duplicated_indices_count_per_position(heads):
+    # A slot listed at several positions counts once per position (the plain sum over the
+    # list): positions 200..259 repeat the slots at 0..59, across the two splits.
+    w = W.small_variant(W.WORKLOADS[1], num_requests=2, ctx_lo=600, ctx_hi=600, topk=320).replace(
+        num_heads=heads, name=f"fp8_dup_H{heads}")
+    p = W.make_problem(w)
+    tk = p.topk.clone()
+    assert bool((tk[:, :60] >= 0).all())
+    tk[:, 200:260] = tk[:, 0:60]
+    p.topk = tk
+    out, lse = DeviceDecode(p, num_splits=2).run()
+    assert_parity(out, lse, oracle_decode(p))
+
+
+@pytest.mark.parametrize("wi", [1, 2, 4])  # 64 and 128 heads (tensor-core kernel), 16 heads
+def test_unselected_rows_are_never_read(small_cases, wi):
     # Overwrite every cache row no valid index selects with NaN codes: output is bitwise unchanged.
-    p, _ = small_cases[SMALL[4].name]
+    p, _ = small_cases[SMALL[wi].name]
     dd = DeviceDecode(p, num_splits=2)
     out0, lse0 = [x.clone() for x in dd.run()]
     P = p.w.page_size
