@@ -733,12 +733,14 @@ __global__ void __launch_bounds__(kHgThreads, 1)
               o[e] = pack_bf16x2(__uint_as_float(vv[2 * e]) * f, __uint_as_float(vv[2 * e + 1]) * f);
             dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-          } else {
-            float4* dst = reinterpret_cast<float4*>(p.o_part + orow_g * kLatent + col);
+          } else {  // f16 partial: a convex combination of keys, so within f16's range
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.o_part) + orow_g * kLatent + col);
+            uint32_t o[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              dst[e] = make_float4(__uint_as_float(vv[4 * e]) * f, __uint_as_float(vv[4 * e + 1]) * f,
-                                   __uint_as_float(vv[4 * e + 2]) * f, __uint_as_float(vv[4 * e + 3]) * f);
+            for (int e = 0; e < 8; ++e)
+              o[e] = pack_f16x2(__uint_as_float(vv[2 * e]) * f, __uint_as_float(vv[2 * e + 1]) * f);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
           }
         }
       }

@@ -538,7 +538,8 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
 // Split merge (SGLang PR #24692 "关键文件": _merge_partial_attn, then _apply_attn_sink).
 // One warp per (token, head, quarter of the 512 output dims): the lanes reduce
 // M = max_s lse_s and W = sum_s e^{lse_s - M} (every quarter's warp the same way), then every
-// lane accumulates 4 of the quarter's 128 dims over the splits, one 16-byte load per split.
+// lane accumulates 4 of the quarter's 128 dims over the splits, one load per split (fp32
+// partials, or f16 ones from the tensor-core kernel).
 // Four warps per row keep more loads in flight than one.
 constexpr int kMergeWarps = 8;
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const DecodeArgs p) {
@@ -572,14 +573,22 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const DecodeArg
   if (quarter == 0 && lane == 0 && p.lse) p.lse[row] = lse;
 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* op =
-      reinterpret_cast<const float4*>(p.o_part + (int64_t(t) * S * p.H + h) * kLatent + 128 * quarter) + lane;
-  const int64_t sstride = int64_t(p.H) * (kLatent / 4);  // float4 between splits
+  const int64_t e0 = (int64_t(t) * S * p.H + h) * kLatent + 128 * quarter + 4 * lane;  // first element
+  const int64_t sstride = int64_t(p.H) * kLatent;                                     // elements between splits
 #pragma unroll 4
   for (int s = 0; s < S; ++s) {
     const float wt = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
     if (wt == 0.f) continue;  // uniform across the warp
-    const float4 o = __ldcs(op + s * sstride);
+    float4 o;
+    if (p.part_f16) {
+      const uint2 v = __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(p.o_part) + e0 +
+                                                            s * sstride));
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+      o = make_float4(a.x, a.y, b.x, b.y);
+    } else {
+      o = __ldcs(reinterpret_cast<const float4*>(p.o_part + e0 + s * sstride));
+    }
     acc.x = fmaf(wt, o.x, acc.x);
     acc.y = fmaf(wt, o.y, acc.y);
     acc.z = fmaf(wt, o.z, acc.z);

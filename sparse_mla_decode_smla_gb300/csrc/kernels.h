@@ -22,7 +22,7 @@ struct DecodeArgs {
   const float* sink;
   void* out;
   float* lse;
-  float* o_part;    // [T, S, H, 512] fp32 (S > 1)
+  float* o_part;    // [T, S, H, 512] fp32, or f16 when part_f16 (S > 1)
   float* lse_part;  // [T, S, H] fp32 (S > 1)
   int32_t* err;     // device error word
   int32_t T, H, K, B, next_n, stride, log2_page, kv_format;
@@ -30,6 +30,7 @@ struct DecodeArgs {
   int32_t num_splits, split_len;
   float c2;  // sm_scale * log2(e)
   float kv_scale;  // per-tensor scale (SMLA_KV_FP8_TENSOR)
+  int32_t part_f16;  // the decode kernel writes o_part as f16 (values within f16's range)
 };
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t s);

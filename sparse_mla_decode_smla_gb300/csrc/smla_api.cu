@@ -217,6 +217,8 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
   a.o_part = reinterpret_cast<float*>(ws + plan.o_off);
   a.num_splits = plan.num_splits;
   a.split_len = plan.split_len;
+  // the tensor-core kernel's keys, hence its normalised partials, lie within f16's range
+  a.part_f16 = use_hg(d) ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (t_ev_start && cudaEventRecord(t_ev_start, s) != cudaSuccess) return SMLA_ERR_CUDA;
   const cudaError_t e = use_hg(d) ? smla::launch_decode_hg(a, s) : smla::launch_decode_mma(a, sms, s);
