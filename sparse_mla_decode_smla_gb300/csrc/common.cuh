@@ -212,11 +212,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
-// Bulk prefetch of [src, src + bytes) from global memory into L2 (TMA engine); src 16-byte
-// aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
-}
 // TMA load of the box at (x, y) of a 2-D tensor map into dst (aligned as the map's swizzle
 // requires), counting the box bytes on bar; elements outside the tensor read as zeros.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar) {
