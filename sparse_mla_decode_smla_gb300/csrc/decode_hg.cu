@@ -150,6 +150,14 @@ __global__ void __launch_bounds__(kHgThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
   auto bar = [&](int k) -> uint32_t { return sb + uint32_t(kHgOffBars) + 8u * k; };
+  // Split-merge buffer in the K-tile area, filled by the cluster's CTAs once their pipelines
+  // are done: the f16 partial rows of the heads this CTA merges, row s hp + k for split s and
+  // head k of its range (16-byte chunk c of row r at chunk c ^ (r & 7)), at most 72 rows;
+  // then the rows' LSEs and the merge weights.
+  auto mrow_addr = [&](int r, int c) -> uint32_t {
+    return sb + uint32_t(kHgOffK) + uint32_t(r) * 1024u + uint32_t((c ^ (r & 7)) << 4);
+  };
+  const uint32_t mlse = sb + uint32_t(kHgOffK) + 72u * 1024u;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 #ifdef SMLA_TRACE
   if (tid == 0 && blockIdx.x < 4096) g_hgspan[blockIdx.x][0] = globaltimer_ns();
@@ -161,10 +169,12 @@ __global__ void __launch_bounds__(kHgThreads, 1)
   constexpr bool tens = TENS;
   const float c2 = tens ? p.c2 * p.kv_scale : p.c2;
   const int G = (p.H + 63) >> 6;  // groups of 64 heads, one CTA each
-  const int g = blockIdx.x % G;
-  const int item = blockIdx.x / G;
-  const int split = item % p.num_splits;
-  const int t = item / p.num_splits;
+  // the splits of a (token, head group) are consecutive CTAs: with the in-kernel merge they
+  // form one cluster, and the split is the CTA's rank in it
+  const int split = blockIdx.x % p.num_splits;
+  const int item = blockIdx.x / p.num_splits;
+  const int g = item % G;
+  const int t = item / G;
   const int r = p.req_id ? __ldg(p.req_id + t) : t / p.next_n;
   const bool req_ok = r >= 0 && r < p.B;
   const int32_t* pt_row = p.page_table + int64_t(req_ok ? r : 0) * p.stride;
@@ -176,6 +186,7 @@ __global__ void __launch_bounds__(kHgThreads, 1)
   const int h0 = 64 * g;
   const int gheads = min(64, p.H - h0);  // heads of this group
   const int nq = req_ok ? gheads : 0;     // q rows to load
+  const int mhp = (gheads + p.num_splits - 1) / p.num_splits;  // heads each split merges (cluster merge)
 
   // Producer lanes 0-15 of warp 12 + pw own slots 16q + lane for q in {pw, pw + 2} of every
   // tile. They fetch each slot's index kHgIdxAhead tiles ahead and, once it has landed, its
@@ -298,6 +309,8 @@ __global__ void __launch_bounds__(kHgThreads, 1)
   tc::fence_after();
 
   bool ok = true;
+  // cluster merge: the softmax threads' final row factor and LSE (without the sink)
+  float cm_f = 0.f, cm_lse = -CUDART_INF_F;
   // ------------------------------------------------------------------ producer
   if (producer) {
     uint16_t* meta = reinterpret_cast<uint16_t*>(sm + kHgOffMeta);
@@ -701,14 +714,17 @@ __global__ void __launch_bounds__(kHgThreads, 1)
       if (real && half == 0) {
         if (S == 1) {
           if (p.lse) p.lse[int64_t(t) * p.H + h] = lse_out;
-        } else {
+        } else if (!p.cluster_merge) {
           p.lse_part[(int64_t(t) * S + split) * p.H + h] = lse0;
         }
       }
+      cm_f = f;
+      cm_lse = lse0;
       const int64_t orow_g = S == 1 ? int64_t(t) * p.H + h : (int64_t(t) * S + split) * p.H + h;
       // four 16-column loads in flight per wait; every lane loads, only real heads store
+      // (with the cluster merge the rows go out after the cluster barrier, at the teardown)
 #pragma unroll 1
-      for (int k4 = 0; k4 < 4; ++k4) {
+      for (int k4 = 0; k4 < 4 && !p.cluster_merge; ++k4) {
         uint32_t v4[4][16];
         if (ntiles > 0) {
 #pragma unroll
@@ -734,11 +750,11 @@ __global__ void __launch_bounds__(kHgThreads, 1)
             dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
           } else {  // f16 partial: a convex combination of keys, so within f16's range
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.o_part) + orow_g * kLatent + col);
             uint32_t o[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
               o[e] = pack_f16x2(__uint_as_float(vv[2 * e]) * f, __uint_as_float(vv[2 * e + 1]) * f);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.o_part) + orow_g * kLatent + col);
             dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
           }
@@ -751,6 +767,107 @@ __global__ void __launch_bounds__(kHgThreads, 1)
   if (!ok && lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
   tc::fence_before();
   __syncthreads();
+  if (p.cluster_merge) {
+    // Split merge inside the cluster (SGLang PR #24692 "关键文件": _merge_partial_attn, then
+    // _apply_attn_sink). Rank r merges heads [r hp, r hp + hp) of the group.
+    //  1. Cluster barrier: every CTA's pipeline is done, so its K-tile area is free.
+    //  2. The softmax threads store their normalised f16 partial rows (O / l) and LSEs into
+    //     the shared memory of the CTA that merges their head; remote stores do not stall.
+    //  3. Cluster barrier: every row has landed. Each CTA merges from its own shared memory,
+    //     and no CTA touches another's memory after this point.
+    tc::cluster_arrive();
+    tc::cluster_wait();
+    if (warp < 4) {
+      const int half = warp >> 1, hl = 32 * (warp & 1) + lane;
+      const uint32_t lrow = tm + (uint32_t(32 * warp) << 16);
+      const bool real = hl < gheads;
+      const int mr = split * mhp + hl % mhp;
+      const uint32_t owner = uint32_t(hl / mhp);
+      if (real && half == 0) tc::st_dsmem_f32(tc::mapa(mlse + mr * 4, owner), cm_lse);
+      tc::fence_after();
+#pragma unroll 1
+      for (int k4 = 0; k4 < 4; ++k4) {
+        uint32_t v4[4][16];
+        if (ntiles > 0) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tc::ld16(lrow + kHgTmO + 64 * k4 + 16 * j, v4[j]);
+          tc::wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v4[j][e] = 0u;
+        }
+        if (!real) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t o[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            o[e] = pack_f16x2(__uint_as_float(v4[j][2 * e]) * cm_f, __uint_as_float(v4[j][2 * e + 1]) * cm_f);
+          const int c0 = (256 * half + 64 * k4 + 16 * j) >> 3;
+          tc::st_dsmem_v4(tc::mapa(mrow_addr(mr, c0), owner), o[0], o[1], o[2], o[3]);
+          tc::st_dsmem_v4(tc::mapa(mrow_addr(mr, c0 + 1), owner), o[4], o[5], o[6], o[7]);
+        }
+      }
+    }
+    tc::cluster_arrive();
+    tc::cluster_wait();
+    const int S = p.num_splits;
+    const int hs = split * mhp, nk = max(0, min(gheads, hs + mhp) - hs);
+    const uint32_t wtab = mlse + 512;  // [head - hs][8] merge weights (times the final factor)
+    for (int k = tid; k < nk; k += kHgThreads) {
+      float ls[kMaxClusterMerge];
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int s = 0; s < kMaxClusterMerge; ++s) {
+        ls[s] = s < S ? lds_f32(mlse + (s * mhp + k) * 4) : -CUDART_INF_F;
+        M = fmaxf(M, ls[s]);
+      }
+      float W = 0.f;
+#pragma unroll
+      for (int s = 0; s < kMaxClusterMerge; ++s) {
+        ls[s] = (M == -CUDART_INF_F || ls[s] == -CUDART_INF_F) ? 0.f : expf(ls[s] - M);
+        W += ls[s];
+      }
+      const float lse0 = W > 0.f ? M + logf(W) : -CUDART_INF_F;
+      float lse = lse0, f = W > 0.f ? 1.f / W : 0.f;
+      if (p.sink) {
+        const float sg = __ldg(p.sink + h0 + hs + k);
+        lse = fmaxf(lse0, sg) + log1pf(expf(-fabsf(lse0 - sg)));
+        f *= expf(lse0 - lse);
+      }
+      if (p.lse) p.lse[int64_t(t) * p.H + h0 + hs + k] = lse;
+#pragma unroll
+      for (int s = 0; s < kMaxClusterMerge; ++s)
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(wtab + (k * kMaxClusterMerge + s) * 4), "f"(ls[s] * f)
+                     : "memory");
+    }
+    __syncthreads();
+    for (int j = tid; j < nk * 64; j += kHgThreads) {  // 8 output dims per job
+      const int k = j >> 6, c = j & 63;
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int s = 0; s < kMaxClusterMerge; ++s) {
+        if (s >= S) break;
+        const float w = lds_f32(wtab + (k * kMaxClusterMerge + s) * 4);
+        const uint4 v = lds128(mrow_addr(s * mhp + k, c));
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&vw[e]));
+          acc[2 * e] = fmaf(w, x.x, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(w, x.y, acc[2 * e + 1]);
+        }
+      }
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                            (int64_t(t) * p.H + h0 + hs + k) * kLatent + 8 * c);
+      *dst = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                        pack_bf16x2(acc[6], acc[7]));
+    }
+  }
   if (warp == kHgMmaWarp) {
     tc::fence_after();
     tc::dealloc(tm, 512);
@@ -780,11 +897,22 @@ cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s) {
   if (e == cudaSuccess) e = q_tile_map(a, &qmap);
   if (e != cudaSuccess) return e;
   const int64_t grid = int64_t(a.T) * a.num_splits * ((a.H + 63) / 64);
-  if (a.kv_format == SMLA_KV_FP8_TENSOR)
-    decode_hg_kernel<true><<<static_cast<unsigned>(grid), kHgThreads, kSmemHg, s>>>(a, map, qmap);
-  else
-    decode_hg_kernel<false><<<static_cast<unsigned>(grid), kHgThreads, kSmemHg, s>>>(a, map, qmap);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kHgThreads);
+  cfg.dynamicSmemBytes = kSmemHg;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (a.cluster_merge) {  // the splits of a (token, head group) share one cluster
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(a.num_splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (a.kv_format == SMLA_KV_FP8_TENSOR) return cudaLaunchKernelEx(&cfg, decode_hg_kernel<true>, a, map, qmap);
+  return cudaLaunchKernelEx(&cfg, decode_hg_kernel<false>, a, map, qmap);
 }
 
 }  // namespace smla

@@ -31,7 +31,12 @@ struct DecodeArgs {
   float c2;  // sm_scale * log2(e)
   float kv_scale;  // per-tensor scale (SMLA_KV_FP8_TENSOR)
   int32_t part_f16;  // the decode kernel writes o_part as f16 (values within f16's range)
+  // The split CTAs of a (token, head group) form one thread-block cluster (cluster size =
+  // num_splits) and merge their partials through distributed shared memory; no o_part.
+  int32_t cluster_merge;
 };
+// Largest cluster the in-kernel split merge uses (the portable cluster size).
+constexpr int kMaxClusterMerge = 8;
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t s);
 // One CTA per (token, split, group of 64 heads); FP8 caches.

@@ -4,6 +4,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "../../include/smla.h"
 #include "kernels.h"
 
@@ -90,9 +92,10 @@ Plan make_plan(const smla_desc* d, int num_sms) {
   if (S == 0) {
     S = 1;
     if (use_hg(d)) {
-      // one CTA per (token, split, group of 64 heads), one per SM: fill one wave at most
+      // one CTA per (token, split, group of 64 heads), one per SM: fill one wave at most,
+      // with splits that fit one cluster (merged in the kernel)
       const int units = d->num_tokens * ((d->num_heads + 63) / 64);
-      if (units < num_sms) S = num_sms / units;
+      if (units < num_sms) S = std::min(num_sms / units, smla::kMaxClusterMerge);
     } else {
       const int units = d->num_tokens * (d->num_heads / 16);
       if (units < num_sms) S = (2 * num_sms + units - 1) / units;
@@ -217,14 +220,16 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
   a.o_part = reinterpret_cast<float*>(ws + plan.o_off);
   a.num_splits = plan.num_splits;
   a.split_len = plan.split_len;
-  // the tensor-core kernel's keys, hence its normalised partials, lie within f16's range
+  // the tensor-core kernel's keys, hence its normalised partials, lie within f16's range;
+  // up to a cluster's worth of its splits merge inside the kernel
   a.part_f16 = use_hg(d) ? 1 : 0;
+  a.cluster_merge = use_hg(d) && plan.num_splits > 1 && plan.num_splits <= smla::kMaxClusterMerge ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (t_ev_start && cudaEventRecord(t_ev_start, s) != cudaSuccess) return SMLA_ERR_CUDA;
   const cudaError_t e = use_hg(d) ? smla::launch_decode_hg(a, s) : smla::launch_decode_mma(a, sms, s);
   if (e != cudaSuccess) return SMLA_ERR_CUDA;
   if (t_ev_stop && cudaEventRecord(t_ev_stop, s) != cudaSuccess) return SMLA_ERR_CUDA;
-  if (plan.num_splits > 1 && smla::launch_merge(a, s) != cudaSuccess) return SMLA_ERR_CUDA;
+  if (plan.num_splits > 1 && !a.cluster_merge && smla::launch_merge(a, s) != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;
 }
 

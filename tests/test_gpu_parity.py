@@ -384,9 +384,11 @@ def test_decode_other_page_sizes(page_size):
     assert_parity(*DeviceDecode(p).run(), oracle_decode(p))
 
 
-@pytest.mark.parametrize("wi,splits", [(1, 0), (1, 8), (4, 0), (2, 5)])
+@pytest.mark.parametrize("wi,splits", [(1, 0), (1, 8), (4, 0), (2, 5), (1, 12), (2, 12)])
 def test_decode_long_index_rows(wi, splits):
-    # 8192 entries per row: more than one split's 2048-entry index list, so at least 4 splits
+    # 8192 entries per row: more than one split's 2048-entry index list, so at least 4 splits.
+    # Up to 8 splits of the tensor-core kernel merge inside a thread-block cluster; 12 take
+    # the partials through global memory and the merge kernel.
     w = W.small_variant(W.WORKLOADS[wi], num_requests=1, ctx_lo=9000, ctx_hi=9000, topk=8192,
                         tail_pad=1000 if wi == 4 else 0)
     p = W.make_problem(w)
