@@ -1,7 +1,8 @@
 // Sparse MLA decode on the 5th-generation tensor cores (tcgen05, TMEM accumulators) for the
 // FP8 caches (fp8_ds: 656-byte rows with per-128 scales and bf16 RoPE; per-tensor FP8: 576
 // E4M3 codes with one scale, vLLM PR #43827), one CTA per (query token, top-k split, group of
-// 64 heads).
+// 64 heads). Up to 8 splits of a (token, head group) form one thread-block cluster and merge
+// their partials through distributed shared memory.
 //
 // What it computes is the sparse decode of vLLM PR #43477 "关键源码片段" (forward_mqa) with
 // the sink and split merge of SGLang PR #24692 "关键文件": out_h = softmax over the selected
@@ -34,13 +35,15 @@
 // f16's range (+-65504).
 //
 // Per CTA (480 threads):
-//  * warps 12-13, producers: index entries six tiles ahead and page-table entries three
+//  * start-up: one thread initialises the barriers and issues q as nine TMA boxes of
+//    [64 heads x 64 dims] (128-byte swizzle), which land while the producers prime their rings.
+//  * warps 12-13, producers: index entries five tiles ahead and page-table entries three
 //    tiles ahead by 4-byte cp.async, then the selected rows by TMA gathers of four rows each
-//    (tile::gather4 on a tensor map of the cache) into a 3-stage ring of 16-row stages; a
-//    masked slot gets a row outside the tensor, which the TMA fills with zeros without
-//    reading memory. One gather per four rows keeps the TMA engine, which serialises its
-//    operations, off the critical path. Warp 12 fills stages 0 and 2 of every tile, warp 13
-//    stages 1 and 3.
+//    (tile::gather4 on a tensor map of the cache) into a ring of four 16-row stages, a whole
+//    tile; a masked slot gets a row outside the tensor, which the TMA fills with zeros
+//    without reading memory. One gather per four rows keeps the TMA engine, which serialises
+//    its operations, off the critical path. Warp 12 fills stages 0 and 2 of every tile,
+//    warp 13 stages 1 and 3.
 //  * warps 4-11, dequant: e4m3 (* scale) -> f16 into the latent K tile (two buffers): four
 //    128-byte-swizzled blocks of [64 slots x 64 low dims | 64 slots x 64 high dims], which
 //    are B of QK (K-major) and B of PV (MN-major). A 16-row quarter of a buffer is rewritten
@@ -50,6 +53,11 @@
 //    of the two, whichever is ready is issued first (PV of tile i when its P is written).
 //  * warps 0-3, softmax and epilogue: base-2 online softmax with lazy rescaling (the running
 //    max moves only when it grows by more than 8, as in FlashAttention-4).
+//  * split merge (more than one split, at most 8): after a cluster barrier the softmax
+//    threads store their normalised f16 rows and LSEs into the shared memory of the cluster
+//    CTA that merges their head; after a second barrier every CTA merges its share of the
+//    heads from its own shared memory. More splits go through global memory and the merge
+//    kernel.
 // Every wait is bounded in time; a wait that gives up sets SMLA_DEVERR_TIMEOUT. The two
 // warps of a head pair meet at named barriers that also AND their status, so both leave the
 // tile loop at the same barrier and neither waits for a partner that has left.
