@@ -135,7 +135,8 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
 
 /*
  * Measurement hook (the pages' interface has none): time the main decode kernel on its
- * own, apart from the split merge that may follow it.
+ * own, apart from a split-merge kernel that may follow it (the tensor-core kernel merges up
+ * to 8 splits itself, so its time includes that merge).
  *   start, stop  cudaEvent_t handles (passed as void*) created and destroyed by the
  *                caller; both NULL turns recording off, exactly one NULL is
  *                SMLA_ERR_NULL.
