@@ -94,11 +94,12 @@ const char* smla_status_string(int32_t status);
 int32_t smla_abi_version(void);
 
 /*
- * Bytes of device workspace smla_decode needs for `d` on the current device
- * (split partials, merge bookkeeping, the device error word). The caller
- * allocates it (256-byte aligned) and zeroes it once before first use; the
- * library leaves the bookkeeping zeroed again after every call. Writes 0 into
- * *bytes on error.
+ * Bytes of device workspace smla_decode needs for `d` on the current device: the
+ * device error word, plus the split partials when the plan merges its splits in a
+ * separate kernel (the tensor-core path merges up to 8 splits inside the decode kernel
+ * and needs none). The caller allocates it (256-byte aligned) and zeroes it once before
+ * first use; the library leaves the error word zeroed again after smla_read_error.
+ * Writes 0 into *bytes on error.
  */
 smla_status smla_workspace_size(const smla_desc* d, size_t* bytes);
 

@@ -78,6 +78,7 @@ smla_status check_desc(const smla_desc* d) {
 struct Plan {
   int num_splits;
   int split_len;
+  bool cluster_merge;  // the tensor-core kernel merges its splits inside a thread-block cluster
   size_t lse_off, o_off, bytes;
 };
 
@@ -112,9 +113,10 @@ Plan make_plan(const smla_desc* d, int num_sms) {
   Plan p;
   p.num_splits = S;
   p.split_len = len;
+  p.cluster_merge = use_hg(d) && S > 1 && S <= smla::kMaxClusterMerge;
   p.lse_off = kWsAlign;
   size_t bytes = kWsAlign;
-  if (S > 1) {
+  if (S > 1 && !p.cluster_merge) {  // split partials in global memory, for the merge kernel
     const size_t rows = size_t(d->num_tokens) * S * d->num_heads;
     bytes = round_up(p.lse_off + rows * 4, kWsAlign);
     p.o_off = bytes;
@@ -223,7 +225,7 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
   // the tensor-core kernel's keys, hence its normalised partials, lie within f16's range;
   // up to a cluster's worth of its splits merge inside the kernel
   a.part_f16 = use_hg(d) ? 1 : 0;
-  a.cluster_merge = use_hg(d) && plan.num_splits > 1 && plan.num_splits <= smla::kMaxClusterMerge ? 1 : 0;
+  a.cluster_merge = plan.cluster_merge ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (t_ev_start && cudaEventRecord(t_ev_start, s) != cudaSuccess) return SMLA_ERR_CUDA;
   const cudaError_t e = use_hg(d) ? smla::launch_decode_hg(a, s) : smla::launch_decode_mma(a, sms, s);

@@ -34,14 +34,18 @@ def _close(out, lse, out_ref, lse_ref):
 
 
 def test_noalloc_matches_workspace_entry_on_consecutive_calls():
+    # (workload, splits, whether the partials go through the scratch): up to 8 splits of the
+    # tensor-core kernel merge inside the kernel and need none; 11 splits of it, and the
+    # mma.sync kernel's splits, keep real partials in the scratch
     cases = [
-        W.small_variant(W.WORKLOADS[1], num_requests=3, ctx_lo=100, ctx_hi=900, topk=320),
-        W.small_variant(W.WORKLOADS[2], num_requests=2, ctx_lo=700, ctx_hi=700, topk=448),
+        (W.small_variant(W.WORKLOADS[1], num_requests=3, ctx_lo=100, ctx_hi=900, topk=320), 3, False),
+        (W.small_variant(W.WORKLOADS[4], num_requests=3, ctx_lo=400, ctx_hi=900, topk=320), 3, True),
+        (W.small_variant(W.WORKLOADS[2], num_requests=2, ctx_lo=900, ctx_hi=900, topk=704), 12, True),
     ]
-    for w, splits in zip(cases, (3, 5)):  # several splits: the scratch holds real partials
+    for w, splits, partials in cases:
         p = W.make_problem(w)
         dd = DeviceDecode(p, num_splits=splits)
-        assert smla.workspace_size(dd.desc) > 256
+        assert (smla.workspace_size(dd.desc) > 256) == partials
         out_ref, lse_ref = [x.clone() for x in dd.run()]
         for _ in range(2):
             out = torch.full_like(dd.out, float("nan"))
@@ -53,8 +57,9 @@ def test_noalloc_matches_workspace_entry_on_consecutive_calls():
 
 def test_noalloc_rejects_work_beyond_its_scratch():
     w = W.small_variant(W.WORKLOADS[2], num_requests=64, ctx_lo=300, ctx_hi=300, topk=2048)
+    # 16 splits: more than a cluster merges, so they need partials beyond the 16 MiB scratch
     d = smla.make_desc(w.num_tokens, w.num_heads, w.topk, w.num_requests, w.page_size, 320,
-                       w.page_table_stride, smla.SMLA_KV_FP8_DS, w.sm_scale, num_splits=8)
+                       w.page_table_stride, smla.SMLA_KV_FP8_DS, w.sm_scale, num_splits=16)
     assert smla.workspace_size(d) > smla.NOALLOC_SCRATCH_BYTES
     dummy = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(smla.SmlaError) as e:
