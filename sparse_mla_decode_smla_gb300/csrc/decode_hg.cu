@@ -462,9 +462,10 @@ __global__ void __launch_bounds__(kHgThreads, 1)
         const int u = 4 * i + q, st = u % kHgRawStages;
         if (!mbar_wait(bar(H_RAW_FULL + st), (u / kHgRawStages) & 1)) { ok = false; break; }
         if (dtid == 0 && q == 0) HTRACE(1, i);
-        // rows [16q, 16q+16) of the K buffer are free once that chunk of PV(i-2) is done
-        if (i >= 2 && !mbar_wait(bar(H_K_FREE + 4 * b + q), ((i - 2) >> 1) & 1)) { ok = false; break; }
+        // convert the stage's codes into registers first: the raw stage goes back to the
+        // producers at once, and only the stores wait for PV(i-2) to release the K rows
         const uint32_t raw = sb + uint32_t(kHgOffRaw) + uint32_t(st * kHgRawStage);
+        uint32_t o[2][8];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int id = dtid + kHgDequantThreads * k;
@@ -473,31 +474,21 @@ __global__ void __launch_bounds__(kHgThreads, 1)
           const uint4 v = lds128(rrow + 16 * ch);
           const float sc = tens ? 1.f : lds_f32(rrow + kScaleOff + 4 * (ch >> 3));
           const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-          uint32_t o[8];
           const __half2 s2 = __float2half2_rn(sc);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             uint32_t lo, hi;
             e4m3x4_to_f16x4(wv[e], lo, hi);  // exact
             if constexpr (tens) {  // the scale comes later, in fp32
-              o[2 * e] = lo;
-              o[2 * e + 1] = hi;
+              o[k][2 * e] = lo;
+              o[k][2 * e + 1] = hi;
             } else {  // code * scale in f16 (exact for power-of-two scales in f16's range)
               __half2 x = __hmul2(*reinterpret_cast<const __half2*>(&lo), s2);
               __half2 y = __hmul2(*reinterpret_cast<const __half2*>(&hi), s2);
-              o[2 * e] = *reinterpret_cast<uint32_t*>(&x);
-              o[2 * e + 1] = *reinterpret_cast<uint32_t*>(&y);
+              o[k][2 * e] = *reinterpret_cast<uint32_t*>(&x);
+              o[k][2 * e + 1] = *reinterpret_cast<uint32_t*>(&y);
             }
           }
-          // dims [16ch, 16ch+16): block ch/4 mod 4, low rows for ch < 16, high rows after
-          const int rr = kHgN * (ch >> 4) + kHgSub * q + slot;
-          const uint32_t row = kt + ((ch >> 2) & 3) * kHgPairBlk + rr * 128;
-          const int c0 = 2 * (ch & 3);
-          const uint32_t sw = rr & 7;
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + ((c0 ^ sw) << 4)), "r"(o[0]),
-                       "r"(o[1]), "r"(o[2]), "r"(o[3]) : "memory");
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + (((c0 + 1) ^ sw) << 4)), "r"(o[4]),
-                       "r"(o[5]), "r"(o[6]), "r"(o[7]) : "memory");
         }
         if ((q & ~1) == rq0) {  // this thread's RoPE chunk of the stage, kept in registers
           uint4 v;
@@ -519,6 +510,22 @@ __global__ void __launch_bounds__(kHgThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(H_RAW_EMPTY + st));
+        // rows [16q, 16q+16) of the K buffer are free once that chunk of PV(i-2) is done
+        if (i >= 2 && !mbar_wait(bar(H_K_FREE + 4 * b + q), ((i - 2) >> 1) & 1)) { ok = false; break; }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int id = dtid + kHgDequantThreads * k;
+          const int slot = id & 15, ch = id >> 4;
+          // dims [16ch, 16ch+16): block ch/4 mod 4, low rows for ch < 16, high rows after
+          const int rr = kHgN * (ch >> 4) + kHgSub * q + slot;
+          const uint32_t row = kt + ((ch >> 2) & 3) * kHgPairBlk + rr * 128;
+          const int c0 = 2 * (ch & 3);
+          const uint32_t sw = rr & 7;
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + ((c0 ^ sw) << 4)), "r"(o[k][0]),
+                       "r"(o[k][1]), "r"(o[k][2]), "r"(o[k][3]) : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + (((c0 + 1) ^ sw) << 4)), "r"(o[k][4]),
+                       "r"(o[k][5]), "r"(o[k][6]), "r"(o[k][7]) : "memory");
+        }
       }
       if (!ok) break;
       fence_proxy_async_smem();
