@@ -429,9 +429,9 @@ def test_bounded_wait_runs_out_and_reports():
 # ------------------------------------------------------------------ full-size, sampled
 
 
-@pytest.mark.parametrize("wi", [1, 2, 3, 4])
-def test_full_size_sampled_tokens(wi):
-    w = W.WORKLOADS[wi]
+@pytest.mark.parametrize("name", [w.name for w in W.WORKLOADS[1:]] + [w.name for w in W.EXTRA_WORKLOADS])
+def test_full_size_sampled_tokens(name):
+    w = W.BY_NAME[name]
     p = W.make_problem(w, device="cuda")
     dd = DeviceDecode(p)  # the launch configuration the bench times (library-chosen splits)
     out, lse = dd.run()
