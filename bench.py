@@ -59,8 +59,8 @@ def measured_peaks() -> dict:
 # The 16k-context and 8k-16k-context captures gather exactly as many rows (tokens x
 # valid indices) as the full workloads; only the pool they are drawn from is smaller.
 TRAFFIC = {
-    ("fp8_T32_H64_K2048_ctx1k-32k", "decode_hg_kernel"): (51854080, "f5948bb6a4626479"),
-    ("fp8_T128_H128_K2048_ctx64k_sink", "decode_hg_kernel"): (229486848, "f5948bb6a4626479"),
+    ("fp8_T32_H64_K2048_ctx1k-32k", "decode_hg_kernel"): (51857920, "f9be707488ff4262"),
+    ("fp8_T128_H128_K2048_ctx64k_sink", "decode_hg_kernel"): (228806400, "f9be707488ff4262"),
     ("fp8_T256_H16_K2048_ctx8k-128k_pad20", "decode_mma_kernel"): (329885184, "75d1688af362a058"),
 }
 KERNEL_SOURCES = {

@@ -94,6 +94,9 @@ constexpr int kHgProducers = 2;
 constexpr int kHgMmaWarp = kHgFirstProducer + kHgProducers;
 constexpr int kHgThreads = 32 * (kHgMmaWarp + 1);
 constexpr int kHgDequantThreads = 32 * kHgDequantWarps;
+// Named barrier of every warp but the producers, once q is placed (ids 1-10 belong to the
+// softmax warp pairs, 0 to __syncthreads)
+constexpr int kHgBarQPlaced = 11;
 constexpr int kHgRawStages = 4;  // a whole tile
 constexpr int kHgGroup = 2688;              // four gathered rows (<= 4 x 656 B), 128-byte aligned
 constexpr int kHgRawStage = 4 * kHgGroup;   // 16 rows
@@ -312,9 +315,14 @@ __global__ void __launch_bounds__(kHgThreads, 1)
     }
     fence_proxy_async_smem();  // read by the tensor core
   }
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
+  // q is in place for the MMA warp, and its staging copy in the K-tile area has been read
+  // before the dequant warps write there. The producer warps write only their own rings and
+  // start gathering without waiting for it.
+  if (!producer) {
+    tc::fence_before();
+    named_bar(kHgBarQPlaced, kHgThreads - 32 * kHgProducers);
+    tc::fence_after();
+  }
 
   bool ok = true;
   // cluster merge: the softmax threads' final row factor and LSE (without the sink)
@@ -780,49 +788,69 @@ __global__ void __launch_bounds__(kHgThreads, 1)
 
   // ------------------------------------------------------------------ teardown
   if (!ok && lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
+  // the softmax threads' final row factors, for the warps that help push the rows (the P
+  // block is free: every MMA has completed)
+  const uint32_t cmf = sb + uint32_t(kHgOffP);
+  if (p.cluster_merge && warp < 4) asm volatile("st.shared.f32 [%0], %1;" ::"r"(cmf + 4 * tid), "f"(cm_f) : "memory");
   tc::fence_before();
   __syncthreads();
   if (p.cluster_merge) {
     // Split merge inside the cluster (SGLang PR #24692 "关键文件": _merge_partial_attn, then
     // _apply_attn_sink). Rank r merges heads [r hp, r hp + hp) of the group.
     //  1. Cluster barrier: every CTA's pipeline is done, so its K-tile area is free.
-    //  2. The softmax threads store their normalised f16 partial rows (O / l) and LSEs into
-    //     the shared memory of the CTA that merges their head; remote stores do not stall.
+    //  2. The softmax and dequant warps store the normalised f16 partial rows (O / l), and
+    //     the softmax warps the LSEs, into the shared memory of the CTA that merges the head;
+    //     remote stores do not stall.
     //  3. Cluster barrier: every row has landed. Each CTA merges from its own shared memory,
     //     and no CTA touches another's memory after this point.
     tc::cluster_arrive();
     tc::cluster_wait();
-    if (warp < 4) {
-      const int half = warp >> 1, hl = 32 * (warp & 1) + lane;
-      const uint32_t lrow = tm + (uint32_t(32 * warp) << 16);
+    if (warp < kHgFirstProducer) {
+      // warp w reads TMEM lane quarter w % 4 (32 rows) and pushes its part w / 4 of the 16
+      // 16-column chunks of each row: chunks [0, 6), [6, 11), [11, 16)
+      const int qw = warp & 3, part = warp >> 2;
+      const int half = qw >> 1, hl = 32 * (qw & 1) + lane;
+      const uint32_t lrow = tm + (uint32_t(32 * qw) << 16);
       const bool real = hl < gheads;
       const int mr = split * mhp + hl % mhp;
       const uint32_t owner = uint32_t(hl / mhp);
-      if (real && half == 0) tc::st_dsmem_f32(tc::mapa(mlse + mr * 4, owner), cm_lse);
+      const float f = lds_f32(cmf + 4 * (32 * qw + lane));
+      if (real && half == 0 && part == 0) tc::st_dsmem_f32(tc::mapa(mlse + mr * 4, owner), cm_lse);
       tc::fence_after();
+      const int cb = part == 0 ? 0 : 1 + 5 * part, ce = 6 + 5 * part;
 #pragma unroll 1
-      for (int k4 = 0; k4 < 4; ++k4) {
-        uint32_t v4[4][16];
+      for (int c = cb; c < ce; c += 2) {
+        const bool two = c + 1 < ce;
+        uint32_t v2[2][16];
+        __syncwarp();  // the TMEM loads are warp-wide
         if (ntiles > 0) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) tc::ld16(lrow + kHgTmO + 64 * k4 + 16 * j, v4[j]);
+          tc::ld16(lrow + kHgTmO + 16 * c, v2[0]);
+          if (two) tc::ld16(lrow + kHgTmO + 16 * (c + 1), v2[1]);
           tc::wait_ld();
         } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
+          for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v4[j][e] = 0u;
+            for (int e = 0; e < 16; ++e) v2[j][e] = 0u;
         }
         if (!real) continue;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
+          if (j == 1 && !two) break;
           uint32_t o[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            o[e] = pack_f16x2(__uint_as_float(v4[j][2 * e]) * cm_f, __uint_as_float(v4[j][2 * e + 1]) * cm_f);
-          const int c0 = (256 * half + 64 * k4 + 16 * j) >> 3;
-          tc::st_dsmem_v4(tc::mapa(mrow_addr(mr, c0), owner), o[0], o[1], o[2], o[3]);
-          tc::st_dsmem_v4(tc::mapa(mrow_addr(mr, c0 + 1), owner), o[4], o[5], o[6], o[7]);
+            o[e] = pack_f16x2(__uint_as_float(v2[j][2 * e]) * f, __uint_as_float(v2[j][2 * e + 1]) * f);
+          const int c0 = 32 * half + 2 * (c + j);  // 16-byte chunk of the 1024-byte merge row
+          if (owner == uint32_t(split)) {  // a head this CTA merges: its own shared memory
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(mrow_addr(mr, c0)), "r"(o[0]), "r"(o[1]),
+                         "r"(o[2]), "r"(o[3]) : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(mrow_addr(mr, c0 + 1)), "r"(o[4]),
+                         "r"(o[5]), "r"(o[6]), "r"(o[7]) : "memory");
+          } else {
+            tc::st_dsmem_v4(tc::mapa(mrow_addr(mr, c0), owner), o[0], o[1], o[2], o[3]);
+            tc::st_dsmem_v4(tc::mapa(mrow_addr(mr, c0 + 1), owner), o[4], o[5], o[6], o[7]);
+          }
         }
       }
     }
