@@ -389,7 +389,7 @@ def gpu_arm(args):
     line = {
         "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
         "config": {"workload": w.name, "tokens": w.num_tokens, "heads": w.num_heads,
                    "topk": w.topk, "valid_indices": valid, "kv_format": w.kv_format,
