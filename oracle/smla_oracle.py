@@ -25,8 +25,10 @@ the softmax denominator including the sink term; the sink adds exp(sigma_h)
 to the denominator only; only -1 means padding.
 
 Every function here is a plain definition evaluated in float64: there is no
-online softmax, no tiling and no split-K. Functions whose parity is pinned
-only partly say so in their docstring.
+online softmax, no tiling and no split-K. Each one is pinned by
+tests/test_oracle_pins.py against something other than itself (closed forms,
+torch's number formats, dense float64 attention, brute force), so none is
+parity unpinned.
 """
 from __future__ import annotations
 
