@@ -92,6 +92,17 @@ def algorithmic_work(problem) -> tuple[int, int, int]:
     return valid, valid * w.row_bytes, valid * w.num_heads * 2 * (576 + 512)
 
 
+def workload_config(problem, valid: int, num_splits: int, world: int) -> dict:
+    """The `config` object of both arms' JSON lines (identical for the same workload)."""
+    w = problem.w
+    return {"workload": w.name, "tokens": w.num_tokens, "heads": w.num_heads,
+            "topk": w.topk, "valid_indices": valid, "kv_format": w.kv_format,
+            "kv_row_bytes": w.row_bytes, "page_size": w.page_size,
+            "num_pages": problem.num_pages, "sink": w.sink,
+            "l2": "flushed between timed steps (512 MiB write, outside the events)",
+            "num_splits": num_splits or "auto", "parallelism": f"replicas x{world}"}
+
+
 def roofline(valid_bytes, flops, seconds, peaks) -> dict:
     t_hbm = valid_bytes / (peaks["hbm_gbs"] * 1e9)
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
@@ -253,8 +264,7 @@ def reference_arm(args):
             "n_gpus": 1, "steps": n, "steps_requested": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * el / n, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "tokens": w.num_tokens, "heads": w.num_heads,
-                       "topk": w.topk, "kv_format": w.kv_format},
+            "config": workload_config(problem, algorithmic_work(problem)[0], args.num_splits, world),
             "cpu_baseline": {"value": value, "unit": "query-tokens/s", "cores": 1, "kind": "oracle",
                              "sample": f"{n} query tokens of {w.name}, one per step, oracle decode "
                                        f"time {el:.1f} s (cache rows packed beforehand, untimed), "
@@ -391,12 +401,7 @@ def gpu_arm(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": w.name, "tokens": w.num_tokens, "heads": w.num_heads,
-                   "topk": w.topk, "valid_indices": valid, "kv_format": w.kv_format,
-                   "kv_row_bytes": w.row_bytes, "page_size": w.page_size,
-                   "num_pages": problem.num_pages, "sink": w.sink,
-                   "l2": "flushed between timed steps (512 MiB write, outside the events)",
-                   "num_splits": args.num_splits or "auto", "parallelism": f"replicas x{world}"},
+        "config": workload_config(problem, valid, args.num_splits, world),
         "roofline": rl,
         "roofline_step_frac": step_rl["frac"],
         "roofline_sustained_frac": (rl["achieved"] / peaks["bf16_tflops_sustained"]

@@ -50,3 +50,26 @@ def test_clock_summary_flags_throttle_reasons(tmp_path):
     s = cs.summary()
     assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 3
     assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_both_arms_share_one_config():
+    # the reference arm's line carries the same `config` object as the GPU arm's line for the
+    # same workload and world size, so the two lines describe one workload
+    import json
+    import subprocess
+    import sys
+
+    import workloads as W
+    w = W.BY_NAME["tiny_bf16_T2_H16_K128"]
+    problem = W.make_problem(w, device="cpu")
+    valid = bench.algorithmic_work(problem)[0]
+    cfg = bench.workload_config(problem, valid, 0, 1)
+    assert cfg["workload"] == w.name and cfg["valid_indices"] == valid == w.num_tokens * w.topk
+    assert cfg["num_splits"] == "auto" and cfg["parallelism"] == "replicas x1"
+    out = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", w.name, "--steps", "2", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=300, check=True).stdout
+    line = json.loads(out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["config"] == cfg
+    assert line["metric"] == bench.METRIC and line["unit"] == "query-tokens/s" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
