@@ -35,7 +35,9 @@ sys.path.insert(0, ROOT)
 
 import workloads as W  # noqa: E402
 
-DEFAULT_WORKLOAD = W.WORKLOADS[1].name
+# The largest configuration the throughput target is quoted on: MTP decode, 64 requests x 4
+# query tokens with independent top-k sets, 128 heads, 4k-128k contexts, per-head sink.
+DEFAULT_WORKLOAD = W.WORKLOADS[3].name
 METRIC = "sparse-MLA decode query-tokens/s"
 L2_FLUSH_BYTES = 512 << 20
 

@@ -36,7 +36,10 @@ typedef enum smla_status {
   SMLA_ERR_WORKSPACE = 5,    /* workspace smaller than smla_workspace_size() */
   SMLA_ERR_CUDA = 6,         /* a CUDA runtime call or launch failed */
   SMLA_ERR_INDEX_RANGE = 7,  /* device met an invalid index or page entry (smla_read_error) */
-  SMLA_ERR_DEVICE = 8        /* no usable device, or not an sm_103 GPU */
+  SMLA_ERR_DEVICE = 8,       /* no usable device, or not an sm_103 GPU */
+  SMLA_ERR_TIMEOUT = 9,      /* a pipeline wait on the device gave up (smla_read_error) */
+  SMLA_ERR_OPERAND_RANGE = 10 /* device met an operand outside the f16 window of the
+                                 tensor-core path (SMLA_DEVERR_RANGE, smla_read_error) */
 } smla_status;
 
 /* Cache row formats. */
@@ -65,7 +68,11 @@ enum {
 enum {
   SMLA_DEVERR_INDEX = 1, /* a top-k entry other than -1 outside [0, page_table_stride*page_size) */
   SMLA_DEVERR_PAGE = 2,  /* a page-table entry used by a valid index outside [0, num_pages) */
-  SMLA_DEVERR_TIMEOUT = 4 /* an internal pipeline wait gave up (bounded waits; outputs invalid) */
+  SMLA_DEVERR_TIMEOUT = 4, /* an internal pipeline wait gave up (bounded waits; outputs invalid) */
+  SMLA_DEVERR_RANGE = 8    /* fp8_ds with 64+ heads: a selected row holds a block scale outside
+                              the f16 window [2^-15, 2^7] ([2^-14, 2^7] for scales that are not
+                              powers of two); the outputs of that call may be inaccurate or
+                              non-finite (see smla_decode) */
 };
 
 typedef struct smla_desc {
@@ -90,7 +97,9 @@ typedef struct smla_desc {
 /* Human-readable name of a status (static string). */
 const char* smla_status_string(int32_t status);
 
-/* ABI version of this header (increments on any incompatible change; 2 added kv_scale). */
+/* ABI version of this header (increments on any incompatible change; 2 added kv_scale,
+ * 3 added SMLA_ERR_TIMEOUT, SMLA_ERR_OPERAND_RANGE, SMLA_DEVERR_RANGE and
+ * smla_noalloc_read_error). */
 int32_t smla_abi_version(void);
 
 /*
@@ -128,6 +137,20 @@ smla_status smla_workspace_size(const smla_desc* d, size_t* bytes);
  * a bit of the device error word, readable with smla_read_error. Duplicated indices
  * count once per occurrence. Rows skipped as padding are never read, so their bytes
  * may hold anything.
+ *
+ * Operand range. q may hold any finite bf16 values: every kernel brings each q row (or
+ * row block) to [1, 2) by a power-of-two factor before its 16-bit MMAs and applies the
+ * factor to the fp32 scores, so q is exact in f16 (elements below 2^-17 of their row's
+ * largest keep 2^-25 of it in absolute error). For SMLA_KV_FP8_DS with 64 or more heads
+ * the keys enter the tensor cores as f16 values code * scale: this is exact for
+ * power-of-two block scales in [2^-15, 2^7] (every block amax in (0.0068, 57344] under
+ * SMLA_SCALE_POW2), within two f16 roundings of 2^-11 each for other scales in
+ * [2^-14, 2^7]. A selected row with a block scale outside that window sets
+ * SMLA_DEVERR_RANGE, and the outputs of that call may be inaccurate or non-finite. The
+ * bf16 RoPE values of such rows enter as f16 too: they must stay below 65504 in
+ * magnitude (larger ones make the outputs of their heads non-finite; nothing flags them),
+ * and values below 2^-17 keep 2^-25 in absolute error. Fewer than 64 heads,
+ * SMLA_KV_FP8_TENSOR and SMLA_KV_BF16 apply scales in fp32 and have neither limit.
  */
 smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
                         const int32_t* page_table, const int32_t* topk,
@@ -201,7 +224,10 @@ smla_status smla_selftest_wait_timeout(int32_t* error_word, uint32_t limit_us, v
 
 /*
  * Synchronises `stream`, copies the device error word of `workspace` into
- * *error_word and clears it. Returns SMLA_ERR_INDEX_RANGE when any bit was set.
+ * *error_word (SMLA_DEVERR_* bits accumulated since the last read) and clears it.
+ * Returns SMLA_ERR_TIMEOUT when the timeout bit is set, else SMLA_ERR_INDEX_RANGE when
+ * an index or page bit is set, else SMLA_ERR_OPERAND_RANGE when the range bit is set,
+ * else SMLA_OK.
  */
 smla_status smla_read_error(const smla_desc* d, void* workspace, size_t workspace_bytes,
                             int32_t* error_word, void* stream);
@@ -231,13 +257,24 @@ smla_status smla_read_error(const smla_desc* d, void* workspace, size_t workspac
  * (choose num_splits = 1, which needs no partials, or fewer splits). All calls share
  * the one array, and its contents persist from call to call: calls that overlap on
  * the GPU (different streams, or different host threads) race on it and must be
- * serialised by the caller. The device error word is cleared at the start of each
- * call; it is not readable through this entry point.
+ * serialised by the caller. The device error word lives in the array too: it starts at
+ * zero when the library loads, collects the SMLA_DEVERR_* bits of every call, and is read
+ * and cleared with smla_noalloc_read_error.
  */
 smla_status smla_decode_noalloc(const smla_desc* d, const void* q, const void* kv_cache,
                                 const int32_t* page_table, const int32_t* topk,
                                 const int32_t* req_id_per_token, const float* sink, void* out,
                                 float* lse, void* stream);
+
+/*
+ * The device error word of smla_decode_noalloc on the current device (its counterpart of
+ * smla_read_error; the pages have none either). Synchronises `stream`, copies the SMLA_DEVERR_*
+ * bits collected since the last read into *error_word (host memory) and clears them, with one
+ * device-to-host copy and one memset on `stream` and no allocation. Returns the status
+ * smla_read_error would give for the same bits. Serialise it with the decode calls, as
+ * those calls are serialised among themselves.
+ */
+smla_status smla_noalloc_read_error(int32_t* error_word, void* stream);
 
 #ifdef __cplusplus
 }

@@ -20,13 +20,17 @@ SMLA_SCALE_FP32 = 1
 SMLA_DEVERR_INDEX = 1
 SMLA_DEVERR_PAGE = 2
 SMLA_DEVERR_TIMEOUT = 4
+SMLA_DEVERR_RANGE = 8
 
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_NULL", 2: "SMLA_ERR_SHAPE", 3: "SMLA_ERR_ALIGN",
           4: "SMLA_ERR_UNSUPPORTED", 5: "SMLA_ERR_WORKSPACE", 6: "SMLA_ERR_CUDA",
-          7: "SMLA_ERR_INDEX_RANGE", 8: "SMLA_ERR_DEVICE"}
+          7: "SMLA_ERR_INDEX_RANGE", 8: "SMLA_ERR_DEVICE", 9: "SMLA_ERR_TIMEOUT",
+          10: "SMLA_ERR_OPERAND_RANGE"}
+DEVICE_ERROR_STATUSES = (0, 7, 9, 10)  # statuses that report device error bits
 EXPORTS = ["smla_status_string", "smla_abi_version", "smla_workspace_size", "smla_decode",
            "smla_pack_kv", "smla_gather_dequant", "smla_read_error", "smla_decode_noalloc",
-           "smla_set_kernel_events", "smla_pack_kv_fp8_tensor", "smla_selftest_wait_timeout"]
+           "smla_set_kernel_events", "smla_pack_kv_fp8_tensor", "smla_selftest_wait_timeout",
+           "smla_noalloc_read_error"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -80,6 +84,8 @@ def lib() -> ctypes.CDLL:
         L.smla_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P]
         L.smla_read_error.restype = I32
         L.smla_read_error.argtypes = [D, P, SZ, ctypes.POINTER(I32), P]
+        L.smla_noalloc_read_error.restype = I32
+        L.smla_noalloc_read_error.argtypes = [ctypes.POINTER(I32), P]
         _lib = L
     return _lib
 
@@ -186,6 +192,15 @@ def read_error(desc, workspace, stream=None) -> int:
     st = lib().smla_read_error(ctypes.byref(desc), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), ctypes.byref(v),
                                _stream(stream))
-    if st not in (0, 7):
+    if st not in DEVICE_ERROR_STATUSES:
         raise SmlaError("smla_read_error", st)
+    return v.value
+
+
+def noalloc_read_error(stream=None) -> int:
+    """Synchronises, returns and clears the error word of decode_noalloc (SMLA_DEVERR_* bits)."""
+    v = ctypes.c_int32(0)
+    st = lib().smla_noalloc_read_error(ctypes.byref(v), _stream(stream))
+    if st not in DEVICE_ERROR_STATUSES:
+        raise SmlaError("smla_noalloc_read_error", st)
     return v.value

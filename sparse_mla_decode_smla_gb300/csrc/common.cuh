@@ -66,6 +66,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// 2^n as fp32, for n in [-126, 127].
+__device__ __forceinline__ float exp2_int(int n) { return __uint_as_float(uint32_t(127 + n) << 23); }
+
+// Exponent f of a power-of-two normaliser for a set of bf16 values whose largest magnitude
+// has the bit pattern `mag` (sign cleared): 2^-f brings that magnitude into [1, 2). 0 for an
+// all-zero set or a non-finite largest value; -126 for bf16 subnormals; at most 126.
+__device__ __forceinline__ int pow2_exponent_of_bf16(uint32_t mag) {
+  const int e = int(mag >> 7);
+  if (e == 0) return mag ? -126 : 0;
+  if (e >= 255) return 0;
+  return min(e - 127, 126);
+}
+
+// Elementwise max of two bf16x2 words of magnitudes (sign bits clear): max.bf16x2.
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// Largest magnitude of the bf16 pair in `acc` (both halves magnitudes), as a 15-bit pattern.
+__device__ __forceinline__ uint32_t bf16x2_hmax_bits(uint32_t acc) { return max(acc & 0xffffu, acc >> 16); }
+
 // bf16 pair -> f16 pair (exact for values inside the f16 normal range).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(bf16_lo(w), bf16_hi(w));

@@ -67,21 +67,6 @@
 #include "kernels.h"
 #include "tcgen05.cuh"
 
-// Optional timeline of the first CTA's pipeline events (compiled in with -DSMLA_TRACE; read
-// back with smla_hgtrace_read). Off in normal builds: the macro expands to nothing.
-#ifdef SMLA_TRACE
-__device__ unsigned long long g_hgtrace[128][12];
-__device__ unsigned long long g_hgspan[4096][2];
-#define HTRACE(ev, tile)                                                                    \
-  do {                                                                                      \
-    if (blockIdx.x == 0 && (tile) < 128) g_hgtrace[(tile)][(ev)] = globaltimer_ns();        \
-  } while (0)
-#else
-#define HTRACE(ev, tile) \
-  do {                   \
-  } while (0)
-#endif
-
 namespace smla {
 namespace {
 
@@ -92,11 +77,16 @@ constexpr int kHgDequantWarps = 8;
 constexpr int kHgFirstProducer = kHgFirstDequant + kHgDequantWarps;
 constexpr int kHgProducers = 2;
 constexpr int kHgMmaWarp = kHgFirstProducer + kHgProducers;
-constexpr int kHgThreads = 32 * (kHgMmaWarp + 1);
+// fp8_ds: the block scales of every raw stage are checked against the f16 window by a warp
+// of their own, so the dequant warps, which set the tile period, do no extra work for it
+constexpr int kHgCheckWarp = kHgMmaWarp + 1;
+constexpr int kHgThreads = 32 * (kHgCheckWarp + 1);
 constexpr int kHgDequantThreads = 32 * kHgDequantWarps;
 // Named barrier of every warp but the producers, once q is placed (ids 1-10 belong to the
 // softmax warp pairs, 0 to __syncthreads)
 constexpr int kHgBarQPlaced = 11;
+// Named barrier of the softmax and dequant warps between the two passes of q placement
+constexpr int kHgBarQMax = 12;
 constexpr int kHgRawStages = 4;  // a whole tile
 constexpr int kHgGroup = 2688;              // four gathered rows (<= 4 x 656 B), 128-byte aligned
 constexpr int kHgRawStage = 4 * kHgGroup;   // 16 rows
@@ -170,9 +160,6 @@ __global__ void __launch_bounds__(kHgThreads, 1)
   };
   const uint32_t mlse = sb + uint32_t(kHgOffK) + 72u * 1024u;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-#ifdef SMLA_TRACE
-  if (tid == 0 && blockIdx.x < 4096) g_hgspan[blockIdx.x][0] = globaltimer_ns();
-#endif
 
   // Per-tensor FP8 codes go into the K tile unscaled (exact in f16); kv_scale is applied in
   // fp32 to the scores (bmm1_scale = sm_scale * kv_scale) and to O (bmm2_scale = kv_scale),
@@ -247,7 +234,7 @@ __global__ void __launch_bounds__(kHgThreads, 1)
     if (tid == 0) {
       for (int s = 0; s < kHgRawStages; ++s) {
         mbar_init(bar(H_RAW_FULL + s), 1);  // the expect_tx arrival of the stage's producer warp
-        mbar_init(bar(H_RAW_EMPTY + s), kHgDequantWarps);
+        mbar_init(bar(H_RAW_EMPTY + s), kHgDequantWarps + (tens ? 0 : 1));  // + the check warp
       }
       for (int b = 0; b < 2; ++b) mbar_init(bar(H_K_FULL + b), kHgDequantWarps);
       for (int c = 0; c < 8; ++c) mbar_init(bar(H_K_FREE + c), 1);
@@ -275,52 +262,90 @@ __global__ void __launch_bounds__(kHgThreads, 1)
   }
   const uint32_t tm = *reinterpret_cast<volatile uint32_t*>(sm + kHgOffTmem);
 
-  // Softmax warps place q: lane l < 64 gets dims [0, 256) of head h0 + l, lane 64 + l dims
-  // [256, 512), as f16 in TMEM (A of QK); the RoPE dims go to shared memory, rows 0-63 dims
-  // 512..543 and rows 64-127 dims 544..575 (64-byte swizzle). Box b of the staged q holds
-  // dims [64b, 64b+64) of the 64 heads, 16-byte chunk c of head row r at chunk c ^ (r & 7).
-  if (warp < 4) {
-    const int half = warp >> 1;
-    const int hl = 32 * (warp & 1) + lane;
-    const uint32_t lrow = tm + (uint32_t(32 * warp) << 16);
+  // The softmax and dequant warps place q: lane l < 64 gets dims [0, 256) of head h0 + l,
+  // lane 64 + l dims [256, 512), as f16 in TMEM (A of QK); the RoPE dims go to shared memory,
+  // rows 0-63 dims 512..543 and rows 64-127 dims 544..575 (64-byte swizzle). Box b of the
+  // staged q holds dims [64b, 64b+64) of the 64 heads, 16-byte chunk c of head row r at
+  // chunk c ^ (r & 7). Warp w serves TMEM lane quarter w % 4 and part w / 4 of each row:
+  // 32-dim chunks {0, 1, 2}, {3, 4, 5} or {6, 7} and the row's 32 RoPE dims.
+  //
+  // Each row gets a power-of-two normaliser: its largest |q| over the 288 dims it holds
+  // (256 latent + 32 RoPE) is brought into [1, 2), and the factor 2^f goes back into the
+  // fp32 scores. So any finite bf16 q is exact in f16 (elements below 2^-17 of the row's
+  // largest keep 2^-25 of it in absolute error), whatever its magnitude. The three parts'
+  // maxima meet in shared memory (the score-exchange rows, unused until the tile loop).
+  if (warp < kHgFirstProducer) {
+    const int quarter = warp & 3, part = warp >> 2;
+    const int half = quarter >> 1;
+    const int hl = 32 * (quarter & 1) + lane;
+    const int row = 32 * quarter + lane;
+    const uint32_t lrow = tm + (uint32_t(32 * quarter) << 16);
     const uint32_t qs = sb + uint32_t(kHgOffK) + uint32_t(hl) * 128;
     auto qchunk = [&](int dim) -> uint32_t {  // 8 dims [dim, dim + 8) of head hl
       return qs + (dim >> 6) * kHgQBox + ((((dim >> 3) & 7) ^ (hl & 7)) << 4);
     };
+    const int ch0 = 3 * part, ch1 = min(8, ch0 + 3);  // this part's 32-dim latent chunks
+    const bool rope = part == 2;
     const bool got = nq == 0 || mbar_wait(bar(H_Q), 0);
-    if (!got && lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
+    if (!got && lane == 0 && part == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
     const bool have = got && hl < nq;
+    uint32_t m4[4] = {0, 0, 0, 0};  // bf16x2 magnitudes, four independent running maxima
+    if (have) {
+      for (int k = 4 * ch0; k < 4 * ch1 + (rope ? 4 : 0); ++k) {  // 8-dim chunks; RoPE last
+        const uint4 v = lds128(qchunk(k < 4 * ch1 ? 256 * half + 8 * k : kLatent + 32 * half + 8 * (k - 4 * ch1)));
+        m4[0] = bf16x2_max(m4[0], v.x & 0x7fff7fffu);
+        m4[1] = bf16x2_max(m4[1], v.y & 0x7fff7fffu);
+        m4[2] = bf16x2_max(m4[2], v.z & 0x7fff7fffu);
+        m4[3] = bf16x2_max(m4[3], v.w & 0x7fff7fffu);
+      }
+    }
+    const uint32_t mx = bf16x2_hmax_bits(bf16x2_max(bf16x2_max(m4[0], m4[1]), bf16x2_max(m4[2], m4[3])));
+    const uint32_t pmax = sb + uint32_t(kHgOffXs);  // [part][row] u32
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(pmax + uint32_t(128 * part + row) * 4), "r"(mx) : "memory");
+    named_bar(kHgBarQMax, 32 * kHgFirstProducer);
+    const uint32_t rmax = max(max(lds_u32(pmax + uint32_t(row) * 4), lds_u32(pmax + uint32_t(128 + row) * 4)),
+                              lds_u32(pmax + uint32_t(256 + row) * 4));
+    const int qf = pow2_exponent_of_bf16(rmax);
+    const float qdown = exp2_int(-qf);
+    auto cvt = [&](uint32_t w) { return pack_f16x2(bf16_lo(w) * qdown, bf16_hi(w) * qdown); };
 #pragma unroll 1
-    for (int ch = 0; ch < 8; ++ch) {
+    for (int ch = ch0; ch < ch1; ++ch) {
       uint32_t wv[16];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         uint4 v = make_uint4(0, 0, 0, 0);
         if (have) v = lds128(qchunk(256 * half + 32 * ch + 8 * k));
-        wv[4 * k] = bf16x2_to_f16x2(v.x); wv[4 * k + 1] = bf16x2_to_f16x2(v.y);
-        wv[4 * k + 2] = bf16x2_to_f16x2(v.z); wv[4 * k + 3] = bf16x2_to_f16x2(v.w);
+        wv[4 * k] = cvt(v.x); wv[4 * k + 1] = cvt(v.y);
+        wv[4 * k + 2] = cvt(v.z); wv[4 * k + 3] = cvt(v.w);
       }
       tc::st16(lrow + kHgTmQ + 16 * ch, wv);
     }
     tc::wait_st();
-    const int row = 32 * warp + lane;
+    if (rope) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (have) v = lds128(qchunk(kLatent + 32 * half + 8 * c));
-      const uint32_t dst = sb + uint32_t(kHgOffQr) + row * 64 + ((c ^ ((row >> 1) & 3)) << 4);
-      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(bf16x2_to_f16x2(v.x)),
-                   "r"(bf16x2_to_f16x2(v.y)), "r"(bf16x2_to_f16x2(v.z)), "r"(bf16x2_to_f16x2(v.w))
-                   : "memory");
+      for (int c = 0; c < 4; ++c) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (have) v = lds128(qchunk(kLatent + 32 * half + 8 * c));
+        const uint32_t dst = sb + uint32_t(kHgOffQr) + row * 64 + ((c ^ ((row >> 1) & 3)) << 4);
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(cvt(v.x)), "r"(cvt(v.y)),
+                     "r"(cvt(v.z)), "r"(cvt(v.w))
+                     : "memory");
+      }
+      fence_proxy_async_smem();  // read by the tensor core
     }
-    fence_proxy_async_smem();  // read by the tensor core
+    // the factor of this row, read by the softmax warps of both halves of the head after
+    // the barrier below; the slot is next written in the tile loop, after both warps of a
+    // pair have met at a barrier
+    if (part == 0)
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(sb + uint32_t(kHgOffXm) + uint32_t(row) * 4), "f"(exp2_int(qf))
+                   : "memory");
   }
   // q is in place for the MMA warp, and its staging copy in the K-tile area has been read
   // before the dequant warps write there. The producer warps write only their own rings and
   // start gathering without waiting for it.
-  if (!producer) {
+  if (!producer && warp != kHgCheckWarp) {
     tc::fence_before();
-    named_bar(kHgBarQPlaced, kHgThreads - 32 * kHgProducers);
+    named_bar(kHgBarQPlaced, kHgThreads - 32 * (kHgProducers + 1));
     tc::fence_after();
   }
 
@@ -366,7 +391,6 @@ __global__ void __launch_bounds__(kHgThreads, 1)
         uint32_t groups = 0;
 #pragma unroll
         for (int gq = 0; gq < 4; ++gq) groups |= ((vm >> (4 * gq)) & 15u) ? (1u << gq) : 0u;
-        if (lane == 0 && pw == 0 && k == 0) HTRACE(0, i);
         if (lane == 0) {
           meta[(i % kHgMetaRing) * 4 + q] = uint16_t(vm);
           mbar_arrive_expect_tx(bar(H_RAW_FULL + st), uint32_t(__popc(groups)) * 4u * rowbytes);
@@ -399,7 +423,6 @@ __global__ void __launch_bounds__(kHgThreads, 1)
                (i == 0 || mbar_test_wait(bar(H_S_FREE), (i - 1) & 1)) && mbar_test_wait(bar(H_ROPE_FULL), i & 1);
       };
       auto qk = [&](int i) {
-        HTRACE(4, i);
         tc::fence_after();
         const uint32_t kt = sb + uint32_t(kHgOffK) + uint32_t((i & 1) * kHgKLat);
 #pragma unroll
@@ -412,7 +435,6 @@ __global__ void __launch_bounds__(kHgThreads, 1)
         tc::commit(bar(H_S_FULL));
       };
       auto pv = [&](int i) {
-        HTRACE(5, i);
         tc::fence_after();
         const uint32_t kt = sb + uint32_t(kHgOffK) + uint32_t((i & 1) * kHgKLat);
         const uint32_t pa = sb + uint32_t(kHgOffP) + uint32_t(kHgPBlk);  // P rows
@@ -452,6 +474,48 @@ __global__ void __launch_bounds__(kHgThreads, 1)
     }
     __syncwarp();
   }
+  // ------------------------------------------------------------------ f16 window check
+  else if (warp == kHgCheckWarp) {
+    if (!tens) {
+      // lane l reads row l % 16 of each raw stage, block scales 2h and 2h+1 (h = l / 16).
+      // Rows of the stage that were not gathered this time hold bytes checked when they
+      // were (or zeros), so they never raise a false flag. Running extremes of the scales'
+      // bit patterns (branch-free integer ops, so a stage goes back to the producers soon
+      // after it lands) are compared with the window once, at the end: the largest scale
+      // (inf and NaN count as the largest), the smallest non-zero power-of-two scale and
+      // the smallest other scale. Only the 16 scale bytes of a row are read here: the
+      // kernel's shared-memory traffic sets its pace.
+      const int r = lane & 15, hh = lane >> 4;
+      uint32_t smax = 0, smin_p2 = ~0u, smin_other = ~0u;
+      for (int i = 0; i < ntiles && ok; ++i) {
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          const int u = 4 * i + q, st = u % kHgRawStages;
+          if (!mbar_wait(bar(H_RAW_FULL + st), (u / kHgRawStages) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t row = sb + uint32_t(kHgOffRaw) + uint32_t(st * kHgRawStage) +
+                               uint32_t((r >> 2) * kHgGroup + (r & 3) * kFp8RowBytes);
+          const uint2 sc2 = lds64(row + kScaleOff + 8 * hh);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint32_t a = (e ? sc2.y : sc2.x) & 0x7fffffffu;
+            const bool p2 = (a & 0x7fffffu) == 0;
+            smax = max(smax, a);
+            smin_p2 = min(smin_p2, (p2 && a != 0) ? a : ~0u);
+            smin_other = min(smin_other, p2 ? ~0u : a);
+          }
+          // both loaded scales have been used: the stage may be overwritten
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(H_RAW_EMPTY + st));
+        }
+      }
+      // window: power-of-two scales in [2^-15, 2^7], others in [2^-14, 2^7]
+      const bool out_of_window = smax > 0x43000000u || smin_p2 < 0x38000000u || smin_other < 0x38800000u;
+      if (__any_sync(0xffffffffu, out_of_window) && lane == 0) atomicOr(p.err, SMLA_DEVERR_RANGE);
+    }
+  }
   // ------------------------------------------------------------------ dequant
   else if (warp >= kHgFirstDequant) {
     const int dtid = tid - 32 * kHgFirstDequant;
@@ -469,7 +533,6 @@ __global__ void __launch_bounds__(kHgThreads, 1)
       for (int q = 0; q < 4 && ok; ++q) {
         const int u = 4 * i + q, st = u % kHgRawStages;
         if (!mbar_wait(bar(H_RAW_FULL + st), (u / kHgRawStages) & 1)) { ok = false; break; }
-        if (dtid == 0 && q == 0) HTRACE(1, i);
         // convert the stage's codes into registers first: the raw stage goes back to the
         // producers at once, and only the stores wait for PV(i-2) to release the K rows
         const uint32_t raw = sb + uint32_t(kHgOffRaw) + uint32_t(st * kHgRawStage);
@@ -539,7 +602,6 @@ __global__ void __launch_bounds__(kHgThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(H_K_FULL + b));
-      if (dtid == 0) HTRACE(3, i);
       // the single RoPE block is free once QK of the previous tile has completed
       if (i >= 1 && !mbar_wait(bar(H_S_FULL), (i - 1) & 1)) { ok = false; break; }
 #pragma unroll
@@ -576,6 +638,9 @@ __global__ void __launch_bounds__(kHgThreads, 1)
     const int bar_x2 = 9 + pr;                    // both second halves are written
     float m = -CUDART_INF_F, l = 0.f;
     bool good = true;
+    // the scores' factors: sm_scale * log2(e) times the q normaliser of my row and of the
+    // partner's row (my partial and the partner's partial of the same head)
+    const float c2m = c2 * lds_f32(mmine), c2p = c2 * lds_f32(mpart);
 
     // rescale this thread's O lane (256 columns) by a; PV of the previous tile is complete.
     // The TMEM loads and stores are warp-wide: the whole warp calls this when any lane
@@ -616,7 +681,6 @@ __global__ void __launch_bounds__(kHgThreads, 1)
       }
       __syncwarp();
       if (lane == 0 && got) mbar_arrive(bar(H_S_FREE));
-      if (lane == 0 && (warp == 0 || warp == 2)) HTRACE(6 + warp / 2, i);
       // the low warp finishes slots 0-31 and sends its partials of slots 32-63; the high warp
       // the other way round (selects keep the arrays in registers)
       float own[32], send[32];
@@ -663,12 +727,11 @@ __global__ void __launch_bounds__(kHgThreads, 1)
       float mx = -CUDART_INF_F;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float sv = ((msk >> j) & 1u) ? (own[j] + x[j]) * c2 : -CUDART_INF_F;
+        const float sv = ((msk >> j) & 1u) ? fmaf(own[j], c2m, x[j] * c2p) : -CUDART_INF_F;
         s[j] = sv;
         mx = fmaxf(mx, sv);
       }
       named_bar_arrive(bar_part, 64);
-      if (lane == 0 && warp == 0) HTRACE(8, i);
       // both warps of the pair take the max over all 64 slots
       asm volatile("st.shared.f32 [%0], %1;" ::"r"(mmine), "f"(mx) : "memory");
       named_bar(bar_max, 64);
@@ -707,7 +770,6 @@ __global__ void __launch_bounds__(kHgThreads, 1)
       tc::fence_before();
       __syncwarp();
       if (lane == 0 && good) mbar_arrive(bar(H_P_READY));
-      if (lane == 0 && (warp == 0 || warp == 2)) HTRACE(9 + warp / 2, i);
     }
 
     // ---- epilogue: both row halves' sums, final row factor, then O lane -> output
@@ -915,9 +977,6 @@ __global__ void __launch_bounds__(kHgThreads, 1)
     tc::fence_after();
     tc::dealloc(tm, 512);
   }
-#ifdef SMLA_TRACE
-  if (tid == 0 && blockIdx.x < 4096) g_hgspan[blockIdx.x][1] = globaltimer_ns();
-#endif
 }
 
 }  // namespace
@@ -960,11 +1019,3 @@ cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s) {
 
 }  // namespace smla
 
-#ifdef SMLA_TRACE
-extern "C" int smla_hgtrace_read(unsigned long long* host) {
-  return int(cudaMemcpyFromSymbol(host, g_hgtrace, sizeof(g_hgtrace)));
-}
-extern "C" int smla_hgspan_read(unsigned long long* host) {
-  return int(cudaMemcpyFromSymbol(host, g_hgspan, sizeof(g_hgspan)));
-}
-#endif

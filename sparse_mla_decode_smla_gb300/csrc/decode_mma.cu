@@ -204,6 +204,12 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
       reinterpret_cast<const __nv_bfloat16*>(p.q) + (int64_t(t) * p.H + h0) * kDim;
   uint32_t qa[8][4];
   uint32_t qr[4];
+  // FP8 caches: q enters the f16 MMAs scaled by a power-of-two normaliser per (head row,
+  // 128-dim latent block) that brings the block's largest |q| into [1, 2); the factor goes
+  // back into the block's fp32 partial score. So any finite bf16 q is exact in f16
+  // (elements below 2^-17 of their block's largest keep 2^-25 of it in absolute error).
+  // The per-tensor format's RoPE part (f16 too) gets its own normaliser per head row.
+  float qf_g = 1.f, qf_g8 = 1.f, rf_g = 1.f, rf_g8 = 1.f;
   {
     const uint4* rg = reinterpret_cast<const uint4*>(qt + g * kDim + 128 * w + 32 * c);
     const uint4* rg8 = reinterpret_cast<const uint4*>(qt + (g + 8) * kDim + 128 * w + 32 * c);
@@ -214,13 +220,32 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
       a[4 * i] = v.x; a[4 * i + 1] = v.y; a[4 * i + 2] = v.z; a[4 * i + 3] = v.w;
       b[4 * i] = v8.x; b[4 * i + 1] = v8.y; b[4 * i + 2] = v8.z; b[4 * i + 3] = v8.w;
     }
+    // largest bf16 magnitude of rows g and g+8 over the warp's block (the quad's 4 x 32 dims)
+    auto quad_max = [&](uint32_t m) {
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      return max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    };
+    uint32_t ma = 0, mb = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      ma = bf16x2_max(ma, a[i] & 0x7fff7fffu);
+      mb = bf16x2_max(mb, b[i] & 0x7fff7fffu);
+    }
+    const int fa = pow2_exponent_of_bf16(quad_max(bf16x2_hmax_bits(ma)));
+    const int fb = pow2_exponent_of_bf16(quad_max(bf16x2_hmax_bits(mb)));
+    const float da = exp2_int(-fa), db = exp2_int(-fb);
+    if (kFp8) {
+      qf_g = exp2_int(fa);
+      qf_g8 = exp2_int(fb);
+    }
+    auto cvt = [](uint32_t w, float d) { return pack_f16x2(bf16_lo(w) * d, bf16_hi(w) * d); };
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       if (kFp8) {
-        qa[s][0] = bf16x2_to_f16x2(a[2 * s]);
-        qa[s][1] = bf16x2_to_f16x2(b[2 * s]);
-        qa[s][2] = bf16x2_to_f16x2(a[2 * s + 1]);
-        qa[s][3] = bf16x2_to_f16x2(b[2 * s + 1]);
+        qa[s][0] = cvt(a[2 * s], da);
+        qa[s][1] = cvt(b[2 * s], db);
+        qa[s][2] = cvt(a[2 * s + 1], da);
+        qa[s][3] = cvt(b[2 * s + 1], db);
       } else {
         qa[s][0] = a[2 * s];
         qa[s][1] = b[2 * s];
@@ -232,9 +257,16 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
     const uint2 rv8 =
         __ldg(reinterpret_cast<const uint2*>(qt + (g + 8) * kDim + kLatent + 16 * w + 4 * c));
     qr[0] = rv.x; qr[1] = rv8.x; qr[2] = rv.y; qr[3] = rv8.y;
-    if (C::kTensor)  // the RoPE codes become f16 B fragments: q's RoPE part goes f16 too
-#pragma unroll
-      for (int e = 0; e < 4; ++e) qr[e] = bf16x2_to_f16x2(qr[e]);
+    if (C::kTensor) {  // the RoPE codes become f16 B fragments: q's RoPE part goes f16 too
+      const uint32_t m1 = bf16x2_max(rv.x & 0x7fff7fffu, rv.y & 0x7fff7fffu);
+      const uint32_t m2 = bf16x2_max(rv8.x & 0x7fff7fffu, rv8.y & 0x7fff7fffu);
+      const int f1 = pow2_exponent_of_bf16(quad_max(bf16x2_hmax_bits(m1)));
+      const int f2 = pow2_exponent_of_bf16(quad_max(bf16x2_hmax_bits(m2)));
+      rf_g = exp2_int(f1);
+      rf_g8 = exp2_int(f2);
+      const float d1 = exp2_int(-f1), d2 = exp2_int(-f2);
+      qr[0] = cvt(rv.x, d1); qr[1] = cvt(rv8.x, d2); qr[2] = cvt(rv.y, d1); qr[3] = cvt(rv8.y, d2);
+    }
   }
 
   float O[8][2][4];
@@ -314,14 +346,17 @@ __global__ void __launch_bounds__(kThreads, SMLA_MMA_MIN_BLOCKS) decode_mma_kern
           }
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
-          if (C::kTensor) {  // the RoPE part carries the scale too
-#pragma unroll
-            for (int e = 0; e < 4; ++e) accr[nt][e] *= p.kv_scale;
+          if (C::kTensor) {  // the RoPE part carries the scale too (and q's RoPE normaliser)
+            accr[nt][0] *= p.kv_scale * rf_g;
+            accr[nt][1] *= p.kv_scale * rf_g;
+            accr[nt][2] *= p.kv_scale * rf_g8;
+            accr[nt][3] *= p.kv_scale * rf_g8;
           }
-          acc[nt][0] = fmaf(acc[nt][0], sc[nt][0], accr[nt][0]);
-          acc[nt][1] = fmaf(acc[nt][1], sc[nt][1], accr[nt][1]);
-          acc[nt][2] = fmaf(acc[nt][2], sc[nt][0], accr[nt][2]);
-          acc[nt][3] = fmaf(acc[nt][3], sc[nt][1], accr[nt][3]);
+          // the block's scale and q's normaliser of rows g (elements 0, 1) and g+8 (2, 3)
+          acc[nt][0] = fmaf(acc[nt][0], sc[nt][0] * qf_g, accr[nt][0]);
+          acc[nt][1] = fmaf(acc[nt][1], sc[nt][1] * qf_g, accr[nt][1]);
+          acc[nt][2] = fmaf(acc[nt][2], sc[nt][0] * qf_g8, accr[nt][2]);
+          acc[nt][3] = fmaf(acc[nt][3], sc[nt][1] * qf_g8, accr[nt][3]);
         }
       } else {
 #pragma unroll

@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "../../include/smla.h"
 #include "kernels.h"
@@ -14,9 +15,11 @@ namespace {
 constexpr size_t kWsAlign = 256;
 constexpr int kMaxDevices = 64;
 
+// Per-device facts, looked up on first use. Several host threads may look them up at
+// once; they store the same values, through atomics.
 struct DevInfo {
-  int ok = -1;  // -1 unknown, 0 unusable, 1 sm_103
-  int num_sms = 0;
+  std::atomic<int> ok{-1};  // -1 unknown, 0 unusable, 1 sm_103
+  std::atomic<int> num_sms{0};
 };
 DevInfo g_dev[kMaxDevices];
 
@@ -31,21 +34,24 @@ smla_status current_device(int* num_sms) {
     return SMLA_ERR_DEVICE;
   }
   DevInfo* di = dev < kMaxDevices ? &g_dev[dev] : nullptr;
-  DevInfo local;
-  if (!di) di = &local;
-  if (di->ok < 0) {
-    int major = 0, minor = 0, sms = 0;
+  int ok = di ? di->ok.load(std::memory_order_acquire) : -1;
+  int sms = di ? di->num_sms.load(std::memory_order_relaxed) : 0;
+  if (ok < 0) {
+    int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
       cudaGetLastError();
       return SMLA_ERR_DEVICE;
     }
-    di->ok = (major == 10 && minor == 3) ? 1 : 0;
-    di->num_sms = sms;
+    ok = (major == 10 && minor == 3) ? 1 : 0;
+    if (di) {
+      di->num_sms.store(sms, std::memory_order_relaxed);
+      di->ok.store(ok, std::memory_order_release);
+    }
   }
-  if (di->ok != 1) return SMLA_ERR_DEVICE;
-  *num_sms = di->num_sms;
+  if (ok != 1) return SMLA_ERR_DEVICE;
+  *num_sms = sms;
   return SMLA_OK;
 }
 
@@ -120,7 +126,8 @@ Plan make_plan(const smla_desc* d, int num_sms) {
     const size_t rows = size_t(d->num_tokens) * S * d->num_heads;
     bytes = round_up(p.lse_off + rows * 4, kWsAlign);
     p.o_off = bytes;
-    bytes += rows * 512 * 4;
+    // the tensor-core kernel writes f16 partial rows, the mma.sync kernel fp32 ones
+    bytes += rows * 512 * (use_hg(d) ? 2 : 4);
   } else {
     p.o_off = bytes;
   }
@@ -159,6 +166,15 @@ smla::DecodeArgs make_args(const smla_desc* d, const void* q, const void* kv,
   return a;
 }
 
+// The status smla_read_error reports for a device error word: a timeout first (every
+// output of the call is invalid), then invalid entries, then operands outside the f16 window.
+smla_status error_status(int32_t v) {
+  if (v & SMLA_DEVERR_TIMEOUT) return SMLA_ERR_TIMEOUT;
+  if (v & (SMLA_DEVERR_INDEX | SMLA_DEVERR_PAGE)) return SMLA_ERR_INDEX_RANGE;
+  if (v & SMLA_DEVERR_RANGE) return SMLA_ERR_OPERAND_RANGE;
+  return SMLA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -174,11 +190,13 @@ const char* smla_status_string(int32_t s) {
     case SMLA_ERR_CUDA: return "CUDA error";
     case SMLA_ERR_INDEX_RANGE: return "invalid index or page entry met on the device";
     case SMLA_ERR_DEVICE: return "no sm_103 device";
+    case SMLA_ERR_TIMEOUT: return "a pipeline wait on the device gave up (outputs invalid)";
+    case SMLA_ERR_OPERAND_RANGE: return "a block scale or RoPE value outside the f16 window met on the device";
     default: return "unknown status";
   }
 }
 
-int32_t smla_abi_version(void) { return 2; }
+int32_t smla_abi_version(void) { return 3; }
 
 smla_status smla_workspace_size(const smla_desc* d, size_t* bytes) {
   if (!bytes) return SMLA_ERR_NULL;
@@ -330,7 +348,7 @@ smla_status smla_read_error(const smla_desc* d, void* workspace, size_t workspac
       cudaStreamSynchronize(s) != cudaSuccess)
     return SMLA_ERR_CUDA;
   *error_word = v;
-  return v ? SMLA_ERR_INDEX_RANGE : SMLA_OK;
+  return error_status(v);
 }
 
 }  // extern "C"
@@ -342,8 +360,9 @@ namespace {
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[SMLA_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch, looked up once per device with that device current.
-void* g_noalloc_addr[kMaxDevices];
+// Device address of g_noalloc_scratch, looked up once per device with that device current
+// (concurrent first calls store the same address).
+std::atomic<void*> g_noalloc_addr[kMaxDevices];
 
 smla_status noalloc_scratch(void** ptr) {
   int dev = 0;
@@ -351,15 +370,15 @@ smla_status noalloc_scratch(void** ptr) {
     cudaGetLastError();
     return SMLA_ERR_DEVICE;
   }
-  if (!g_noalloc_addr[dev]) {
-    void* p = nullptr;
+  void* p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
       return SMLA_ERR_CUDA;
     }
-    g_noalloc_addr[dev] = p;
+    g_noalloc_addr[dev].store(p, std::memory_order_release);
   }
-  *ptr = g_noalloc_addr[dev];
+  *ptr = p;
   return SMLA_OK;
 }
 
@@ -379,9 +398,26 @@ extern "C" smla_status smla_decode_noalloc(const smla_desc* d, const void* q, co
   void* scratch = nullptr;
   st = noalloc_scratch(&scratch);
   if (st != SMLA_OK) return st;
-  // the error word (first 4 bytes) is the only part that must start at zero
-  if (cudaMemsetAsync(scratch, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return SMLA_ERR_CUDA;
+  // The error word (the array's first 4 bytes, zero when the library loads) accumulates
+  // the device error bits of every call until smla_noalloc_read_error reads and clears it.
+  // smla_decode checks every argument before it launches anything.
   return smla_decode(d, q, kv_cache, page_table, topk, req_id_per_token, sink, out, lse, scratch,
                      SMLA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" smla_status smla_noalloc_read_error(int32_t* error_word, void* stream) {
+  if (!error_word) return SMLA_ERR_NULL;
+  int sms = 0;
+  smla_status st = current_device(&sms);
+  if (st != SMLA_OK) return st;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != SMLA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, scratch, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(scratch, 0, sizeof(v), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    return SMLA_ERR_CUDA;
+  *error_word = v;
+  return error_status(v);
 }

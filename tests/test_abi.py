@@ -38,10 +38,27 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.smla_abi_version() == 2
-    for s in range(9):
-        assert smla.status_string(s)
+    assert L.smla_abi_version() == 3
+    for s in range(11):
+        assert smla.status_string(s) != "unknown status"
     assert smla.status_string(99) == "unknown status"
+
+
+def _header_enum(prefix):
+    text = open(os.path.join(ROOT, "include", "smla.h")).read()
+    return {m.group(1): int(m.group(2)) for m in re.finditer(rf"\b({prefix}\w+)\s*=\s*(\d+)", text)}
+
+
+def test_binding_statuses_and_error_bits_match_header():
+    st = _header_enum("SMLA_ERR_") | {"SMLA_OK": 0}
+    assert {v: k for k, v in st.items()} == smla.STATUS
+    # a distinct status for a timeout, apart from the index/page one and the device one
+    assert len({st["SMLA_ERR_TIMEOUT"], st["SMLA_ERR_INDEX_RANGE"], st["SMLA_ERR_DEVICE"],
+                st["SMLA_ERR_OPERAND_RANGE"]}) == 4
+    bits = _header_enum("SMLA_DEVERR_")
+    assert bits == {"SMLA_DEVERR_INDEX": smla.SMLA_DEVERR_INDEX, "SMLA_DEVERR_PAGE": smla.SMLA_DEVERR_PAGE,
+                    "SMLA_DEVERR_TIMEOUT": smla.SMLA_DEVERR_TIMEOUT, "SMLA_DEVERR_RANGE": smla.SMLA_DEVERR_RANGE}
+    assert all(v & (v - 1) == 0 for v in bits.values()) and len(set(bits.values())) == len(bits)
 
 
 def test_desc_layout_matches_header():
@@ -117,6 +134,7 @@ def test_workspace_size_checks_desc_first(L):
 def test_read_error_null(L):
     v = ctypes.c_int32(0)
     assert L.smla_read_error(None, None, 4, ctypes.byref(v), None) == 1
+    assert L.smla_noalloc_read_error(None, None) == 1
 
 
 def test_kernel_events_hook_needs_both_or_neither(L):

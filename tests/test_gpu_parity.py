@@ -426,6 +426,38 @@ def test_bounded_wait_runs_out_and_reports():
     assert_parity(*DeviceDecode(p).run(), oracle_decode(p))
 
 
+def test_read_error_status_per_bit():
+    # smla_read_error: SMLA_ERR_TIMEOUT (9) whenever the timeout bit is set, else
+    # SMLA_ERR_INDEX_RANGE (7) for index/page bits, else SMLA_ERR_OPERAND_RANGE (10)
+    import ctypes
+    d = smla.make_desc(1, 16, 64, 1, 64, 4, 4, smla.SMLA_KV_FP8_DS, 1 / 24)
+    ws = torch.zeros(64, dtype=torch.int32, device="cuda")
+    L = smla.lib()
+
+    def status():
+        v = ctypes.c_int32(0)
+        st = L.smla_read_error(ctypes.byref(d), ctypes.c_void_p(ws.data_ptr()), 256, ctypes.byref(v), None)
+        return st, v.value
+
+    smla.selftest_wait_timeout(ws, 1000)
+    assert status() == (9, smla.SMLA_DEVERR_TIMEOUT)
+    assert status() == (0, 0)  # read clears the word
+    for word, st in [(1, 7), (2, 7), (5, 9), (8, 10), (9, 7), (12, 9)]:
+        ws[0] = word
+        assert status() == (st, word)
+
+
+@pytest.mark.parametrize("heads,fmt,elem", [(128, smla.SMLA_KV_FP8_DS, 2), (64, smla.SMLA_KV_FP8_TENSOR, 2),
+                                            (16, smla.SMLA_KV_FP8_DS, 4), (64, smla.SMLA_KV_BF16, 4)])
+def test_workspace_holds_partials_at_their_element_size(heads, fmt, elem):
+    # 12 splits merge in the merge kernel: the tensor-core kernel writes f16 partial rows,
+    # the mma.sync kernel fp32 ones; the workspace is the error word, the LSEs and the rows
+    T, S = 3, 12
+    d = smla.make_desc(T, heads, S * 256, T, 64, 64, 64, fmt, 1 / 24, num_splits=S)
+    rows = T * S * heads
+    assert smla.workspace_size(d) == 256 + (rows * 4 + 255) // 256 * 256 + rows * 512 * elem
+
+
 # ------------------------------------------------------------------ full-size, sampled
 
 
@@ -437,7 +469,13 @@ def test_full_size_sampled_tokens(name):
     out, lse = dd.run()
     torch.cuda.synchronize()
     T = w.num_tokens
-    tokens = sorted({0, T // 2 + 1, T - 1})
+    # a token in every eighth of the batch (so in every wave of CTAs), the last token, and
+    # the first and last tokens of the requests with the shortest and longest contexts
+    ctx = p.ctx.cpu()
+    lo, hi = int(ctx.argmin()), int(ctx.argmax())
+    tokens = set(range(0, T, max(1, T // 8))) | {T - 1}
+    tokens |= {lo * w.next_n, lo * w.next_n + w.next_n - 1, hi * w.next_n, hi * w.next_n + w.next_n - 1}
+    tokens = sorted(tokens)
     ref = oracle_decode(p, tokens=tokens)
     assert_parity(out, lse, ref, tokens=tokens)
     assert torch.isfinite(out.float()).all()

@@ -197,6 +197,49 @@ def test_physical_slots_hand_example():
     assert keep == [0, 2, 3] and phys.tolist() == [1, 8, 7] and bad == 0
 
 
+def test_request_of_token_hand_example_next_n():
+    # next_n = 4 query rows per request (MTP): tokens 0-3 -> request 0, 4-7 -> 1, 8-11 -> 2.
+    assert [O.request_of_token(t, 4, None) for t in range(12)] == [0] * 4 + [1] * 4 + [2] * 4
+    # next_n = 1: every token is its own request
+    assert [O.request_of_token(t, 1, None) for t in range(5)] == [0, 1, 2, 3, 4]
+    # next_n = 3 with a ragged last request: tokens 6, 7 -> request 2
+    assert [O.request_of_token(t, 3, None) for t in range(8)] == [0, 0, 0, 1, 1, 1, 2, 2]
+
+
+def test_request_of_token_explicit_map_overrides_next_n():
+    # a mixed batch: a 3-token chunk of request 2, one decode token of request 0 and two
+    # speculative rows of request 1; the explicit map wins over t // next_n
+    req = np.array([2, 2, 2, 0, 1, 1], dtype=np.int32)
+    assert [O.request_of_token(t, 1, req) for t in range(6)] == [2, 2, 2, 0, 1, 1]
+    assert [O.request_of_token(t, 4, req) for t in range(6)] == [2, 2, 2, 0, 1, 1]
+
+
+def test_decode_routes_tokens_to_their_request_page_table():
+    # Two requests over one pool of 4 pages of 4 slots; request 0 maps its pages to
+    # physical [3, 1], request 1 to [0, 2]. With next_n = 2, tokens 0, 1 read request 0's
+    # slots and tokens 2, 3 request 1's: check each token against attend() on the rows
+    # picked out by hand (physical slot = page * 4 + offset).
+    g = torch.Generator().manual_seed(5)
+    P, H = 4, 2
+    lat = torch.randn(16, 512, generator=g).to(torch.bfloat16)
+    rope = torch.randn(16, 64, generator=g).to(torch.bfloat16)
+    rows = O.pack_bf16(_bits(lat), _bits(rope))
+    q = torch.randn(4, H, 576, generator=g).to(torch.bfloat16)
+    pt = np.array([[3, 1], [0, 2]], dtype=np.int32)
+    topk = np.array([[0, 5, -1], [7, 2, 1], [0, 5, -1], [7, 2, 1]], dtype=np.int32)
+    by_hand = {0: [12, 5], 1: [7, 14, 13], 2: [0, 9], 3: [11, 2, 1]}
+    res = O.decode(_bits(q), lambda ph: rows[ph], "bf16", pt, topk, P, 4, 0.05, next_n=2)
+    for t, slots in by_hand.items():
+        keys = O.dequant_rows(rows[slots], "bf16")
+        o, l, _ = O.attend(O.bf16_bits_to_f64(_bits(q)[t]), keys, 0.05, None)
+        assert np.array_equal(res["out"][t], o) and np.array_equal(res["lse"][t], l)
+    # an explicit map that swaps the requests: token 2 now reads request 0's slots
+    res2 = O.decode(_bits(q), lambda ph: rows[ph], "bf16", pt, topk, P, 4, 0.05, next_n=2,
+                    req_id_per_token=np.array([1, 1, 0, 0], dtype=np.int32))
+    o, _, _ = O.attend(O.bf16_bits_to_f64(_bits(q)[2]), O.dequant_rows(rows[[12, 5]], "bf16"), 0.05, None)
+    assert np.array_equal(res2["out"][2], o)
+
+
 def test_physical_slots_invalid_entries_dropped_and_counted():
     keep, phys, bad = O.physical_slots(np.array([-5, 12, 4, 0, -1]), np.array([2, -1, 1]), 4, 3)
     # -5: negative non-padding; 12: beyond stride*P; 4: page entry -1; 0: page 2 -> slot 8

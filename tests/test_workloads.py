@@ -59,3 +59,20 @@ def test_per_tensor_fp8_workload_shape():
     small = W.small_variant(w, num_requests=2, ctx_lo=100, ctx_hi=300, topk=128)
     p = W.make_problem(small)
     assert p.topk.shape == (2, 128) and p.q.shape == (2, 64, 576)
+
+
+def test_magnitude_gains_multiply_the_draw_before_rounding():
+    base = W.small_variant(W.WORKLOADS[2], num_requests=2, ctx_lo=300, ctx_hi=300, topk=64)
+    w = base.replace(q_gains=(1e5, 1.0), q_dim_gains=(1.0, 1e-3), latent_gains=(1e-4, 2.0, 3.0),
+                     rope_gains=(7.0,))
+    p0, p1 = W.make_problem(base), W.make_problem(w)
+    q0, q1 = p0.q.float(), p1.q.float()
+    # same draw: q1 = bf16(q_f32 * gain); compare against the bf16 rounding of the gained draw
+    assert torch.equal(torch.sign(q0), torch.sign(q1))
+    assert torch.allclose(q1[:, 0, 0], q0[:, 0, 0] * 1e5, rtol=1e-2)
+    assert torch.allclose(q1[:, 1, 1], q0[:, 1, 1] * 1e-3, rtol=1e-2)
+    lat0, rope0 = p0.raw_chunk(0)
+    lat1, rope1 = p1.raw_chunk(0)
+    assert torch.allclose(lat1[0].float(), lat0[0].float() * 1e-4, rtol=1e-2)
+    assert torch.allclose(lat1[4].float(), lat0[4].float() * 2.0, rtol=1e-2)
+    assert torch.allclose(rope1[5].float(), rope0[5].float() * 7.0, rtol=1e-2)

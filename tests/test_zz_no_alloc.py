@@ -65,3 +65,22 @@ def test_noalloc_rejects_work_beyond_its_scratch():
     with pytest.raises(smla.SmlaError) as e:
         smla.decode_noalloc(d, dummy, dummy, dummy, dummy, None, None, dummy, None)
     assert e.value.status == 5  # SMLA_ERR_WORKSPACE, nothing launched
+
+
+def test_noalloc_reports_device_errors_until_read():
+    # The scratch holds the device error word too: it collects the bits of every call until
+    # smla_noalloc_read_error reads and clears it, so an invalid entry is never lost.
+    w = W.small_variant(W.WORKLOADS[2], num_requests=2, ctx_lo=500, ctx_hi=500, topk=256)
+    p = W.make_problem(w)
+    dd = DeviceDecode(p)
+    out, lse = torch.empty_like(dd.out), torch.empty_like(dd.lse)
+    smla.noalloc_read_error()  # whatever an earlier caller left
+    smla.decode_noalloc(dd.desc, dd.q, dd.kv, dd.page_table, dd.topk, None, dd.sink, out, lse)
+    assert smla.noalloc_read_error() == 0
+    bad = dd.topk.clone()
+    bad[1, 7] = 10 ** 6  # beyond the request's page table: masked and flagged
+    for _ in range(2):
+        smla.decode_noalloc(dd.desc, dd.q, dd.kv, dd.page_table, bad, None, dd.sink, out, lse)
+    smla.decode_noalloc(dd.desc, dd.q, dd.kv, dd.page_table, dd.topk, None, dd.sink, out, lse)
+    assert smla.noalloc_read_error() == smla.SMLA_DEVERR_INDEX  # kept across the clean call
+    assert smla.noalloc_read_error() == 0  # and cleared by the read

@@ -22,6 +22,11 @@ per slot, a paged cache, request-local top-k indices padded with -1, output
   slot. For the bf16 cache format these ARE the cache rows. For the FP8
   format they are the values each side quantises itself (the CUDA path with
   its pack kernel, the oracle with its own packer).
+* optional magnitude sweeps for operand-range tests: a gain per head on q
+  (q_gains, cycled over heads), per dimension on q (q_dim_gains, cycled over
+  the 576 dims), and per physical slot on the latent and RoPE source values
+  (latent_gains / rope_gains, cycled over slots); each multiplies the N(0, 1)
+  draw in fp32 before the rounding to bf16.
 
 Large pools are produced in chunks of CHUNK_SLOTS slots, each from its own
 seeded generator, so any chunk can be regenerated on its own.
@@ -59,6 +64,10 @@ class Workload:
     sm_scale: float = SM_SCALE_576
     seed_offset: int = 0
     kv_scale: float = 1.0  # per-tensor scale of the fp8_tensor format (unused otherwise)
+    q_gains: tuple = ()       # per-head multipliers of q (cycled), empty = 1
+    q_dim_gains: tuple = ()   # per-dim multipliers of q (cycled over 576 dims), empty = 1
+    latent_gains: tuple = ()  # per-slot multipliers of the latent source values (cycled)
+    rope_gains: tuple = ()    # per-slot multipliers of the RoPE source values (cycled)
 
     @property
     def num_tokens(self) -> int:
@@ -147,6 +156,11 @@ class Problem:
         n = min(CHUNK_SLOTS, self.num_slots - lo)
         g = _gen(self.seed, 1000 + c, dev)
         x = torch.randn((n, HEAD_DIM), generator=g, device=dev, dtype=torch.float32)
+        for gains, cols in ((self.w.latent_gains, slice(0, LATENT_DIM)), (self.w.rope_gains, slice(LATENT_DIM, None))):
+            if gains:
+                gt = torch.tensor(gains, dtype=torch.float32, device=dev)
+                slot = torch.arange(lo, lo + n, device=dev) % len(gains)
+                x[:, cols] *= gt[slot][:, None]
         x = x.to(torch.bfloat16)
         return x[:, :LATENT_DIM].contiguous(), x[:, LATENT_DIM:].contiguous()
 
@@ -213,7 +227,14 @@ def make_problem(w: Workload, seed: int | None = None, device="cpu") -> Problem:
         topk[t, :nvalid] = idx.to(torch.int32).cpu()
 
     q = torch.randn((T, H, HEAD_DIM), generator=_gen(seed, 4, device), device=device,
-                    dtype=torch.float32).to(torch.bfloat16)
+                    dtype=torch.float32)
+    if w.q_gains:
+        qg = torch.tensor(w.q_gains, dtype=torch.float32, device=device)
+        q *= qg[torch.arange(H, device=device) % len(w.q_gains)][None, :, None]
+    if w.q_dim_gains:
+        dg = torch.tensor(w.q_dim_gains, dtype=torch.float32, device=device)
+        q *= dg[torch.arange(HEAD_DIM, device=device) % len(w.q_dim_gains)][None, None, :]
+    q = q.to(torch.bfloat16)
     sink = None
     if w.sink:
         sink = torch.randn((H,), generator=_gen(seed, 5, device), device=device, dtype=torch.float32)
