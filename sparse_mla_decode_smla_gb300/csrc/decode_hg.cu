@@ -63,6 +63,8 @@
 // tile loop at the same barrier and neither waits for a partner that has left.
 #include <math_constants.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
@@ -982,16 +984,18 @@ __global__ void __launch_bounds__(kHgThreads, 1)
 }  // namespace
 
 cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s) {
-  static int configured_dev = -1;
+  // devices (below 64) whose kernel attributes are set; concurrent first calls set them twice
+  static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (configured_dev != dev) {
+  const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (!(configured.load(std::memory_order_acquire) & bit) || !bit) {
     cudaError_t e = cudaFuncSetAttribute(decode_hg_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemHg));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_hg_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemHg));
     if (e != cudaSuccess) return e;
-    configured_dev = dev;
+    configured.fetch_or(bit, std::memory_order_release);
   }
   alignas(64) CUtensorMap map;
   alignas(64) CUtensorMap qmap;

@@ -38,6 +38,8 @@
 // SMLA_DEVERR_TIMEOUT and the CTA leaves after its copies in flight have landed.
 #include <math_constants.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -636,14 +638,16 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const DecodeArg
 template <int FMT>
 cudaError_t launch_fmt(const DecodeArgs& a, cudaStream_t s) {
   const size_t smem = Cfg<FMT>::kSmem;
-  static int configured_dev = -1;
+  // devices (below 64) whose kernel attribute is set; concurrent first calls set it twice
+  static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (configured_dev != dev) {
+  const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (!(configured.load(std::memory_order_acquire) & bit) || !bit) {
     cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    configured_dev = dev;
+    configured.fetch_or(bit, std::memory_order_release);
   }
   const int64_t grid = int64_t(a.T) * a.num_splits * (a.H >> 4);
   decode_mma_kernel<FMT><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(a);
