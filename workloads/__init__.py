@@ -253,3 +253,48 @@ def small_variant(w: Workload, num_requests: int, ctx_lo: int, ctx_hi: int, topk
     """A reduced copy of a workload (same heads, format, sink, next_n) for oracle-speed tests."""
     return w.replace(name=f"{w.name}:{name_suffix}", num_requests=num_requests, ctx_lo=ctx_lo,
                      ctx_hi=ctx_hi, topk=topk, tail_pad=tail_pad, shared_pool_pages=0)
+
+
+# ------------------------------------------------------------------------------ indexer inputs
+
+INDEX_HEADS = 64
+INDEX_DIM = 128
+
+
+@dataclasses.dataclass
+class IndexerInputs:
+    """Inputs of the sparse-attention indexer for a decode batch (same requests and pages).
+
+    q [T, H_I, 128] E4M3 codes (uint8); weights [T, H_I] fp32; cache [num_pages, P * 132]
+    bytes, each page P x 128 E4M3 key codes (slot-major) followed by P fp32 key scales;
+    ctx [B] int32 context lengths. The codes are drawn as N(0, 1) values (q) and
+    N(0, 1) * 32 values (keys) cast to float8_e4m3fn by torch; the key scales are powers of
+    two 2^e with e uniform in [-10, -4]; the weights are N(0, 1) / 8.
+    """
+
+    q: torch.Tensor
+    weights: torch.Tensor
+    cache: torch.Tensor
+    ctx: torch.Tensor
+    heads: int = INDEX_HEADS
+
+
+def make_indexer_inputs(problem: Problem, seed: int | None = None, heads: int = INDEX_HEADS,
+                        device=None) -> IndexerInputs:
+    dev = problem.device if device is None else torch.device(device)
+    seed = problem.seed if seed is None else seed
+    w = problem.w
+    T, P = w.num_tokens, w.page_size
+    q = torch.randn((T, heads, INDEX_DIM), generator=_gen(seed, 40, dev), device=dev, dtype=torch.float32)
+    q = q.to(torch.float8_e4m3fn).view(torch.uint8)
+    weights = torch.randn((T, heads), generator=_gen(seed, 41, dev), device=dev, dtype=torch.float32) / 8.0
+    cache = torch.empty((problem.num_pages, P * (INDEX_DIM + 4)), dtype=torch.uint8, device=dev)
+    step = max(1, (1 << 26) // (P * INDEX_DIM))  # pages per draw (bounded memory)
+    for p0 in range(0, problem.num_pages, step):
+        n = min(step, problem.num_pages - p0)
+        g = _gen(seed, 2000 + p0 // step, dev)
+        k = torch.randn((n, P * INDEX_DIM), generator=g, device=dev, dtype=torch.float32) * 32.0
+        cache[p0:p0 + n, :P * INDEX_DIM] = k.to(torch.float8_e4m3fn).view(torch.uint8)
+        e = torch.randint(-10, -3, (n, P), generator=g, device=dev).to(torch.float32)
+        cache[p0:p0 + n, P * INDEX_DIM:] = torch.exp2(e).contiguous().view(torch.uint8).view(n, P * 4)
+    return IndexerInputs(q=q, weights=weights, cache=cache, ctx=problem.ctx.to(torch.int32).to(dev), heads=heads)
