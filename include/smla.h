@@ -98,8 +98,8 @@ typedef struct smla_desc {
 const char* smla_status_string(int32_t status);
 
 /* ABI version of this header (increments on any incompatible change; 2 added kv_scale,
- * 3 added SMLA_ERR_TIMEOUT, SMLA_ERR_OPERAND_RANGE, SMLA_DEVERR_RANGE and
- * smla_noalloc_read_error). */
+ * 3 added SMLA_ERR_TIMEOUT, SMLA_ERR_OPERAND_RANGE, SMLA_DEVERR_RANGE,
+ * smla_noalloc_read_error and the indexer calls). */
 int32_t smla_abi_version(void);
 
 /*
@@ -231,6 +231,66 @@ smla_status smla_selftest_wait_timeout(int32_t* error_word, uint32_t limit_us, v
  */
 smla_status smla_read_error(const smla_desc* d, void* workspace, size_t workspace_bytes,
                             int32_t* error_word, void* stream);
+
+/*
+ * ---------------------------------------------------------------------------------------
+ * Sparse-attention indexer: the step before smla_decode that chooses each query token's
+ * top-k slots (the vLLM PR #52164 page, "功能与动机" and "实现拆解 1-5": the FP8 paged MQA
+ * logits kernel fp8_paged_mqa_logits, scheduled from the requests' context lengths, with the
+ * next_n query rows of a request handled natively instead of flattened; the SGLang PR #24692
+ * page, "实现拆解 5"). The pages give no formula; this library computes, for query row i of
+ * request r (token t = r * next_n + i) and every slot s < ctx_r - next_n + 1 + i:
+ *     logit[t, s] = sum_h weights[t, h] * max(0, scale_s * <q[t, h], k_s>)
+ * with q[t, h] and k_s vectors of 128 E4M3 values and scale_s one fp32 per key, and then the
+ * indices of each token's K largest logits.
+ * ---------------------------------------------------------------------------------------
+ */
+typedef struct smla_indexer_desc {
+  int32_t num_tokens;        /* T = num_requests * next_n */
+  int32_t num_heads;         /* H_I: 32 or 64 index heads */
+  int32_t num_requests;      /* B: 1..8192 */
+  int32_t next_n;            /* query rows per request, 1..4, with H_I * next_n <= 256 */
+  int32_t page_size;         /* P: 16, 32, 64 or 128 slots per page */
+  int32_t page_table_stride; /* entries per page_table row (>= 1) */
+  int64_t num_pages;         /* pages in k_cache (1 .. 2^31 - 1) */
+  int32_t logits_stride;     /* floats per logits row (>= 1); contexts are served up to it */
+  int32_t topk;              /* K of smla_indexer_topk (>= 1) */
+  int32_t reserved[4];       /* must be zero */
+} smla_indexer_desc;
+
+/*
+ * FP8 paged MQA logits of every query token over its visible context.
+ *   q            [T, H_I, 128] E4M3 codes (uint8), 16-byte aligned.
+ *   weights      [T, H_I] fp32, 16-byte aligned.
+ *   k_cache      [num_pages, P * 132] bytes, 16-byte aligned: page p holds the P keys of its
+ *                slots as P x 128 E4M3 codes (slot-major), followed by their P fp32 scales.
+ *   page_table   [B, page_table_stride] int32: request-local page -> physical page.
+ *   context_lens [B] int32: request r's slots are 0 .. ctx_r - 1 (slot s in page
+ *                page_table[r, s / P] at position s % P); ctx_r above page_table_stride * P or
+ *                logits_stride is served up to that bound and sets SMLA_DEVERR_INDEX.
+ *   logits       [T, logits_stride] fp32: row t receives its visible slots; the rest of the
+ *                row is not written.
+ *   error_word   device int32 receiving SMLA_DEVERR_* bits: SMLA_DEVERR_PAGE for a page entry
+ *                outside [0, num_pages) that a visible slot needs (those slots' logits are
+ *                undefined), SMLA_DEVERR_INDEX as above, SMLA_DEVERR_TIMEOUT (outputs invalid).
+ * All pointers are device memory owned by the caller; nothing is allocated or synchronised.
+ * Argument errors return before anything is launched.
+ */
+smla_status smla_indexer_logits(const smla_indexer_desc* d, const void* q, const float* weights,
+                                const void* k_cache, const int32_t* page_table,
+                                const int32_t* context_lens, float* logits, int32_t* error_word,
+                                void* stream);
+
+/*
+ * Top-k of the indexer logits: topk [T, K] int32 receives, for token t, the request-local
+ * indices of its K largest visible logits in ascending index order; at a tie on the K-th
+ * value the lowest indices are taken. With fewer than K visible slots the row is 0, 1, ...,
+ * visible - 1, then -1 padding: the topk_indices argument of smla_decode.
+ *   logits [T, logits_stride] fp32 as smla_indexer_logits wrote them (only the visible
+ *   part of each row is read); context_lens [B] int32 as given to that call.
+ */
+smla_status smla_indexer_topk(const smla_indexer_desc* d, const float* logits,
+                              const int32_t* context_lens, int32_t* topk, void* stream);
 
 /*
  * Size of the library-owned scratch array used by smla_decode_noalloc (16 MiB per device).

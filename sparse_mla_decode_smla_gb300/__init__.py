@@ -30,7 +30,7 @@ DEVICE_ERROR_STATUSES = (0, 7, 9, 10)  # statuses that report device error bits
 EXPORTS = ["smla_status_string", "smla_abi_version", "smla_workspace_size", "smla_decode",
            "smla_pack_kv", "smla_gather_dequant", "smla_read_error", "smla_decode_noalloc",
            "smla_set_kernel_events", "smla_pack_kv_fp8_tensor", "smla_selftest_wait_timeout",
-           "smla_noalloc_read_error"]
+           "smla_noalloc_read_error", "smla_indexer_logits", "smla_indexer_topk"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -48,6 +48,14 @@ class smla_desc(ctypes.Structure):
                 ("kv_format", ctypes.c_int32), ("sm_scale", ctypes.c_float),
                 ("num_splits", ctypes.c_int32), ("kv_scale", ctypes.c_float),
                 ("reserved", ctypes.c_int32 * 3)]
+
+
+class smla_indexer_desc(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("num_requests", ctypes.c_int32), ("next_n", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("page_table_stride", ctypes.c_int32),
+                ("num_pages", ctypes.c_int64), ("logits_stride", ctypes.c_int32),
+                ("topk", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
 
 
 _lib = None
@@ -86,6 +94,11 @@ def lib() -> ctypes.CDLL:
         L.smla_read_error.argtypes = [D, P, SZ, ctypes.POINTER(I32), P]
         L.smla_noalloc_read_error.restype = I32
         L.smla_noalloc_read_error.argtypes = [ctypes.POINTER(I32), P]
+        XD = ctypes.POINTER(smla_indexer_desc)
+        L.smla_indexer_logits.restype = I32
+        L.smla_indexer_logits.argtypes = [XD, P, P, P, P, P, P, P, P]
+        L.smla_indexer_topk.restype = I32
+        L.smla_indexer_topk.argtypes = [XD, P, P, P, P]
         _lib = L
     return _lib
 
@@ -204,3 +217,26 @@ def noalloc_read_error(stream=None) -> int:
     if st not in DEVICE_ERROR_STATUSES:
         raise SmlaError("smla_noalloc_read_error", st)
     return v.value
+
+
+def make_indexer_desc(num_requests, next_n, num_heads, page_size, num_pages, page_table_stride,
+                      logits_stride, topk) -> smla_indexer_desc:
+    d = smla_indexer_desc()
+    d.num_tokens, d.num_heads, d.num_requests = num_requests * next_n, num_heads, num_requests
+    d.next_n, d.page_size, d.page_table_stride = next_n, page_size, page_table_stride
+    d.num_pages, d.logits_stride, d.topk = num_pages, logits_stride, topk
+    return d
+
+
+def indexer_logits(desc, q, weights, k_cache, page_table, context_lens, logits, error_word,
+                   stream=None):
+    """FP8 paged MQA logits (smla_indexer_logits): logits[t, s] for every visible slot."""
+    _check("smla_indexer_logits", lib().smla_indexer_logits(
+        ctypes.byref(desc), _ptr(q), _ptr(weights), _ptr(k_cache), _ptr(page_table),
+        _ptr(context_lens), _ptr(logits), _ptr(error_word), _stream(stream)))
+
+
+def indexer_topk(desc, logits, context_lens, topk, stream=None):
+    """Top-k slots of every token's visible logits (smla_indexer_topk), ascending, -1 padded."""
+    _check("smla_indexer_topk", lib().smla_indexer_topk(
+        ctypes.byref(desc), _ptr(logits), _ptr(context_lens), _ptr(topk), _stream(stream)))

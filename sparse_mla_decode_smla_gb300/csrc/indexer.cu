@@ -1,0 +1,477 @@
+// Sparse-attention indexer on sm_103a: FP8 paged MQA logits and their top-k, the step that
+// chooses each query token's top-k slots for the sparse decode (the vLLM PR #52164 page,
+// "功能与动机" and "实现拆解 1-5": fp8_paged_mqa_logits, scheduled from the requests' context
+// lengths, with the next_n query rows of a request handled natively; the SGLang PR #24692
+// page, "实现拆解 5": fp8_paged_mqa_logits for the indexer).
+//
+// What it computes, per query token t (row i of request r, next_n rows per request) and visible
+// slot s < ctx_r - next_n + 1 + i:
+//     logit[t, s] = sum_h w[t, h] * max(0, scale_s * <q[t, h], k_s>)
+// with q and k_s E4M3 (128 dims) and one fp32 scale per key; then the indices of the K largest
+// logits of each token.
+//
+// indexer_logits_kernel: persistent, one CTA per SM. Every CTA derives the same schedule from the
+// context lengths (a block-wide scan of the requests' 1024-slot chunk counts) and takes a
+// contiguous, balanced range of (request, chunk) items, so its q and weights change rarely.
+//  * producer (warp 0, one thread): per 128-slot tile, one 3-D TMA load per key page (P x 128
+//    codes, 128-byte swizzle: the K-major operand layout as it lands) and one bulk copy of the
+//    page's P scales, into a 4-stage ring; q of the item's request (next_n x H_I rows of 128
+//    codes) and its weights when the request changes.
+//  * MMA (warp 1, one thread): D[128 slots, N] = K_tile x q^T with N = H_I x next_n, four
+//    tcgen05.mma kind::f8f6f4 (K = 32 each), into one of two TMEM accumulators. The next_n query
+//    rows of a request share every key tile: it is read once, not next_n times.
+//  * epilogue (warps 2-9): thread = slot; each warp pair of a TMEM lane quarter splits the
+//    request's query rows; scale, ReLU and the weighted sum over heads in fp32; coalesced
+//    stores of the visible logits.
+// Every wait is bounded; a wait that gives up sets SMLA_DEVERR_TIMEOUT.
+//
+// indexer_topk_kernel: one CTA per token, radix select over the token's visible logits (keys
+// made order-preserving as unsigned 32-bit integers; three passes of 11, 11 and 10 bits with
+// shared-memory histograms) to the K-th largest value, then one ordered pass that writes every
+// index above it and, among indices equal to it, the lowest ones up to K: the output is the
+// top-k set in ascending index order.
+#include <math_constants.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace smla {
+namespace {
+
+constexpr int kIxDim = 128;              // index dims (bytes of E4M3 per key or q row)
+constexpr int kIxTile = 128;             // slots per tile (the MMA's M)
+constexpr int kIxChunk = 1024;           // slots per scheduled item
+constexpr int kIxStages = 4;
+constexpr int kIxEpiWarps = 8;
+constexpr int kIxFirstEpi = 2;
+constexpr int kIxThreads = 32 * (kIxFirstEpi + kIxEpiWarps);
+constexpr int kIxMaxN = 256;             // H_I x next_n
+
+constexpr size_t kIxOffQ = 0;                                   // [N rows x 128 B], 128-byte swizzle
+constexpr size_t kIxOffK = kIxOffQ + size_t(kIxMaxN) * kIxDim;  // [stage][128 x 128 B]
+constexpr size_t kIxStageK = size_t(kIxTile) * kIxDim;
+constexpr size_t kIxOffSc = kIxOffK + kIxStages * kIxStageK;    // [stage][128] fp32 scales
+constexpr size_t kIxOffW = kIxOffSc + kIxStages * kIxTile * 4;  // [N] fp32 weights
+constexpr size_t kIxOffPre = kIxOffW + kIxMaxN * 4;             // [kIxMaxReq + 1] item prefix
+constexpr size_t kIxOffTm = kIxOffPre + size_t(kIxMaxRequests + 1) * 4;
+constexpr size_t kIxOffBars = (kIxOffTm + 16 + 7) / 8 * 8;
+enum { X_FULL = 0, X_EMPTY = X_FULL + kIxStages, X_DFULL = X_EMPTY + kIxStages, X_DEMPTY = X_DFULL + 2,
+       X_QFULL = X_DEMPTY + 2, X_QFREE, X_DRAIN, X_COUNT };
+constexpr size_t kIxSmem = kIxOffBars + X_COUNT * 8 + 1024;
+static_assert(kIxOffK % 1024 == 0 && kIxStageK % 1024 == 0 && kIxOffSc % 16 == 0, "swizzle atoms, bulk copies");
+static_assert(kIxSmem <= 232448, "shared memory budget");
+
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B, fp32 accumulator, both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// TMA load of box (x, y, z) of a 3-D tensor map into dst, counting the box bytes on bar.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];\n" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+struct Item {
+  int r, c;  // request, chunk
+};
+
+__global__ void __launch_bounds__(kIxThreads, 1)
+    indexer_logits_kernel(const IndexerArgs p, const __grid_constant__ CUtensorMap kmap,
+                          const __grid_constant__ CUtensorMap qmap) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  auto bar = [&](int k) -> uint32_t { return sb + uint32_t(kIxOffBars) + 8u * k; };
+  int32_t* pre = reinterpret_cast<int32_t*>(sm + kIxOffPre);  // pre[r] = items of requests < r
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int N = p.H * p.next_n;
+  const int P = 1 << p.log2_page;
+
+  // a request's context as served: at most its page table's capacity and the logits row
+  auto ctx_of = [&](int r) -> int {
+    return min(__ldg(p.ctx + r), min(p.stride << p.log2_page, p.logits_stride));
+  };
+  // ---- schedule: a block-wide scan of the requests' chunk counts (their largest visible
+  // length is ctx_r: the last query row sees the whole context)
+  auto nchunks = [&](int r) -> int {
+    const int ctx = ctx_of(r);
+    return ctx > 0 ? (ctx + kIxChunk - 1) / kIxChunk : 0;
+  };
+  {
+    int* wsum = reinterpret_cast<int*>(sm + kIxOffW);  // scratch before the weights are loaded
+    int carry = 0;
+    for (int base = 0; base < p.B; base += kIxThreads) {
+      const int r = base + tid;
+      const int v = r < p.B ? nchunks(r) : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wsum[warp] = x;
+      __syncthreads();
+      int before = carry;
+      for (int w2 = 0; w2 < warp; ++w2) before += wsum[w2];
+      if (r < p.B) pre[r] = before + x - v;
+      int tot = 0;
+      for (int w2 = 0; w2 < kIxThreads / 32; ++w2) tot += wsum[w2];
+      __syncthreads();
+      carry += tot;
+    }
+    if (tid == 0) pre[p.B] = carry;
+    if (blockIdx.x == 0)  // a context longer than the page table or the logits row is cut and flagged
+      for (int r = tid; r < p.B; r += kIxThreads)
+        if (__ldg(p.ctx + r) > ctx_of(r)) atomicOr(p.err, SMLA_DEVERR_INDEX);
+    if (tid == 0) {
+      mbar_init(bar(X_QFULL), 1);
+      mbar_init(bar(X_QFREE), 1 + kIxEpiWarps);
+      mbar_init(bar(X_DRAIN), 1);
+      for (int s = 0; s < kIxStages; ++s) {
+        mbar_init(bar(X_FULL + s), 1);
+        mbar_init(bar(X_EMPTY + s), 1 + kIxEpiWarps);  // the MMAs' commit + the epilogue (scales)
+      }
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(bar(X_DFULL + b), 1);
+        mbar_init(bar(X_DEMPTY + b), kIxEpiWarps);
+      }
+      tc::fence_mbarrier_init_cluster();
+    }
+    if (warp == 1) tc::alloc(sb + uint32_t(kIxOffTm), 512);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+  }
+  const uint32_t tm = *reinterpret_cast<volatile uint32_t*>(sm + kIxOffTm);
+  const int total = pre[p.B];
+  const int G = gridDim.x;
+  const int it0 = int((int64_t(total) * blockIdx.x) / G), it1 = int((int64_t(total) * (blockIdx.x + 1)) / G);
+  // the item at flat index `it`: the request whose prefix range holds it
+  auto item_at = [&](int it, int hint) -> Item {
+    int r = hint;
+    while (r + 1 < p.B && pre[r + 1] <= it) ++r;
+    return Item{r, it - pre[r]};
+  };
+  int r_first = 0;
+  {
+    int lo = 0, hi = p.B - 1;  // last r with pre[r] <= it0
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= it0) lo = mid; else hi = mid - 1;
+    }
+    r_first = lo;
+  }
+  auto tiles_of = [&](const Item& x) -> int {
+    const int ctx = ctx_of(x.r);
+    const int s0 = x.c * kIxChunk;
+    return (min(ctx, s0 + kIxChunk) - s0 + kIxTile - 1) / kIxTile;
+  };
+
+  bool ok = true;
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int u = 0, qloads = 0, rq = -1, r = r_first;
+      for (int it = it0; it < it1 && ok; ++it) {
+        const Item x = item_at(it, r);
+        r = x.r;
+        if (x.r != rq) {  // q and weights of the request, once the previous ones are unused
+          if (qloads > 0 && !mbar_wait(bar(X_QFREE), (qloads - 1) & 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(X_QFULL), uint32_t(N) * kIxDim + uint32_t(N) * 4u);
+          tma_load_2d(sb + uint32_t(kIxOffQ), &qmap, 0, x.r * N, bar(X_QFULL));
+          bulk_g2s(sb + uint32_t(kIxOffW), p.weights + int64_t(x.r) * N, uint32_t(N) * 4u, bar(X_QFULL));
+          ++qloads;
+          rq = x.r;
+        }
+        const int32_t* pt_row = p.page_table + int64_t(x.r) * p.stride;
+        const int nt = tiles_of(x);
+        for (int j = 0; j < nt; ++j, ++u) {
+          const int st = u % kIxStages;
+          if (!mbar_wait(bar(X_EMPTY + st), ((u / kIxStages) & 1) ^ 1)) { ok = false; break; }
+          const int s0 = x.c * kIxChunk + j * kIxTile;
+          const int npg = kIxTile >> p.log2_page;  // pages per tile (P <= 128)
+          // pages outside the request's table or the pool are not fetched: their rows keep
+          // stale bytes, which only feed logits beyond the visible range or flagged ones
+          uint32_t bytes = 0, mask = 0;
+          const int ctx = ctx_of(x.r);
+          for (int g = 0; g < npg; ++g) {
+            const int lp = (s0 >> p.log2_page) + g;
+            const int32_t pg = lp < p.stride ? __ldg(pt_row + lp) : -1;
+            if (pg >= 0 && pg < p.num_pages) {
+              mask |= 1u << g;
+              bytes += uint32_t(P) * (kIxDim + 4);
+            } else if ((lp << p.log2_page) < ctx) {  // a page the visible context needs
+              atomicOr(p.err, SMLA_DEVERR_PAGE);
+            }
+          }
+          mbar_arrive_expect_tx(bar(X_FULL + st), bytes);
+          for (int g = 0; g < npg; ++g) {
+            if (!((mask >> g) & 1u)) continue;
+            const int32_t pg = __ldg(pt_row + (s0 >> p.log2_page) + g);
+            tma_load_3d(sb + uint32_t(kIxOffK + st * kIxStageK) + uint32_t(g * P * kIxDim), &kmap, 0, 0, pg,
+                        bar(X_FULL + st));
+            bulk_g2s(sb + uint32_t(kIxOffSc) + uint32_t(st * kIxTile * 4 + g * P * 4),
+                     p.cache + int64_t(pg) * P * (kIxDim + 4) + int64_t(P) * kIxDim, uint32_t(P) * 4u,
+                     bar(X_FULL + st));
+          }
+        }
+      }
+      // no copy may land after the CTA has left
+      for (int v = max(0, u - kIxStages); v < u; ++v)
+        if (!mbar_wait(bar(X_FULL + v % kIxStages), (v / kIxStages) & 1)) break;
+      if (qloads > 0) mbar_wait(bar(X_QFULL), (qloads - 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_e4m3_f32(128, N);
+      int u = 0, qloads = 0, rq = -1, r = r_first;
+      for (int it = it0; it < it1 && ok; ++it) {
+        const Item x = item_at(it, r);
+        r = x.r;
+        if (x.r != rq) {
+          if (!mbar_wait(bar(X_QFULL), qloads & 1)) { ok = false; break; }
+          ++qloads;
+          rq = x.r;
+        }
+        const int nt = tiles_of(x);
+        for (int j = 0; j < nt; ++j, ++u) {
+          const int st = u % kIxStages, b = u & 1;
+          if (!mbar_wait(bar(X_FULL + st), (u / kIxStages) & 1)) { ok = false; break; }
+          if (u >= 2 && !mbar_wait(bar(X_DEMPTY + b), ((u >> 1) - 1) & 1)) { ok = false; break; }
+          tc::fence_after();
+          const uint32_t ka = sb + uint32_t(kIxOffK + st * kIxStageK);
+#pragma unroll
+          for (int k = 0; k < kIxDim / 32; ++k)
+            mma_f8(tm + uint32_t(b * N), tc::sdesc_sw128(ka + 32 * k, 16, 1024),
+                   tc::sdesc_sw128(sb + uint32_t(kIxOffQ) + 32 * k, 16, 1024), idesc, k > 0);
+          tc::commit(bar(X_EMPTY + st));
+          tc::commit(bar(X_DFULL + b));
+        }
+        // the last item of this request: q and weights may be replaced once its MMAs are done
+        const bool last_of_req = it + 1 >= it1 || item_at(it + 1, r).r != x.r;
+        if (last_of_req && ok) tc::commit(bar(X_QFREE));
+      }
+      // every MMA issued has completed before the tensor memory is released
+      tc::commit(bar(X_DRAIN));
+      if (!mbar_wait(bar(X_DRAIN), 0)) ok = false;
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int ew = warp - kIxFirstEpi;
+    const int quarter = warp & 3, half = ew >> 2;
+    const int row = 32 * quarter + lane;  // slot within the tile
+    const uint32_t lrow = tm + (uint32_t(32 * quarter) << 16);
+    const int nn = p.next_n, i_lo = half ? (nn + 1) / 2 : 0, i_hi = half ? nn : (nn + 1) / 2;
+    const float* wsm = reinterpret_cast<const float*>(sm + kIxOffW);
+    int u = 0, r = r_first, rq = -1, qloads = 0;
+    for (int it = it0; it < it1 && ok; ++it) {
+      const Item x = item_at(it, r);
+      r = x.r;
+      if (x.r != rq) {
+        if (!mbar_wait(bar(X_QFULL), qloads & 1)) { ok = false; break; }
+        ++qloads;
+        rq = x.r;
+      }
+      const int ctx = ctx_of(x.r);
+      const int nt = tiles_of(x);
+      for (int j = 0; j < nt; ++j, ++u) {
+        const int st = u % kIxStages, b = u & 1;
+        if (!mbar_wait(bar(X_DFULL + b), (u >> 1) & 1)) { ok = false; break; }
+        tc::fence_after();
+        const int s = x.c * kIxChunk + j * kIxTile + row;
+        const float sc = lds_f32(sb + uint32_t(kIxOffSc) + uint32_t(st * kIxTile + row) * 4);
+        for (int i = i_lo; i < i_hi; ++i) {
+          float acc = 0.f;
+#pragma unroll
+          for (int h0 = 0; h0 < 64; h0 += 32) {
+            if (h0 >= p.H) break;
+            uint32_t v[32];
+            tc::ld32(lrow + uint32_t(b * N + i * p.H + h0), v);
+            tc::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              acc = fmaf(wsm[i * p.H + h0 + e], fmaxf(0.f, __uint_as_float(v[e]) * sc), acc);
+          }
+          const int vis = ctx - nn + 1 + i;
+          const int t = x.r * nn + i;
+          if (s < vis) p.logits[int64_t(t) * p.logits_stride + s] = acc;
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(X_DEMPTY + b));
+          mbar_arrive(bar(X_EMPTY + st));
+        }
+      }
+      const bool last_of_req = it + 1 >= it1 || item_at(it + 1, r).r != x.r;
+      if (last_of_req && ok) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(X_QFREE));
+      }
+    }
+  }
+  if (!ok && lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::dealloc(tm, 512);
+  }
+}
+
+// ------------------------------------------------------------------------------ top-k
+
+constexpr int kTkThreads = 512;
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerArgs p) {
+  __shared__ uint32_t hist[2048];
+  __shared__ uint32_t s_need, s_sel;
+  __shared__ uint32_t wcount[kTkThreads / 32];
+  __shared__ uint32_t s_base_gt, s_base_eq;
+  const int t = blockIdx.x;
+  const int r = t / p.next_n;
+  const int i = t - r * p.next_n;
+  int32_t* out = p.topk + int64_t(t) * p.K;
+  const int ctx = min(__ldg(p.ctx + r), min(p.stride << p.log2_page, p.logits_stride));
+  const int vis = max(0, ctx - p.next_n + 1 + i);
+  const float* lg = p.logits + int64_t(t) * p.logits_stride;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (vis <= p.K) {  // every visible slot, then padding
+    for (int j = tid; j < p.K; j += kTkThreads) out[j] = j < vis ? j : -1;
+    return;
+  }
+  // radix select of the K-th largest key: bits [31:21], [20:10], [9:0]
+  uint32_t prefix = 0, need = uint32_t(p.K);
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int width = pass == 2 ? 10 : 11;
+    const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0), nb = 1 << width;
+    const uint32_t hmask = pass == 0 ? 0u : (0xffffffffu << (sh + width));
+    for (int k = tid; k < nb; k += kTkThreads) hist[k] = 0;
+    __syncthreads();
+    for (int s = tid; s < vis; s += kTkThreads) {
+      const uint32_t key = order_key(__ldg(lg + s));
+      if ((key & hmask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {  // walk the bins from the top until `need` is reached
+      uint32_t acc = 0;
+      int sel = -1;
+      for (int b0 = nb - 32; b0 >= 0 && sel < 0; b0 -= 32) {
+        const uint32_t c = hist[b0 + 31 - lane];  // lane 0 holds the highest bin of the group
+        uint32_t x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        const bool reach = acc + x >= need;
+        const uint32_t m = __ballot_sync(0xffffffffu, reach);
+        if (m) {
+          const int l = __ffs(m) - 1;
+          const uint32_t before = __shfl_sync(0xffffffffu, x - c, l);
+          if (lane == 0) {
+            s_sel = uint32_t(b0 + 31 - l);
+            s_need = need - (acc + before);
+          }
+          sel = 1;
+        }
+        acc += __shfl_sync(0xffffffffu, x, 31);
+      }
+    }
+    __syncthreads();
+    prefix |= s_sel << sh;
+    need = s_need;
+    __syncthreads();
+  }
+  // prefix is the K-th largest key; `need` keys equal to it complete the set (the lowest
+  // indices among them). One ordered pass: block-wide ranks of the "above" and "equal" flags.
+  if (tid == 0) {
+    s_base_gt = 0;
+    s_base_eq = 0;
+  }
+  __syncthreads();
+  for (int s0 = 0; s0 < vis; s0 += kTkThreads) {
+    const int s = s0 + tid;
+    const uint32_t key = s < vis ? order_key(__ldg(lg + s)) : 0u;
+    const bool gt = s < vis && key > prefix, eq = s < vis && key == prefix;
+    const uint32_t mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
+    if (lane == 0) wcount[warp] = (__popc(mg) << 16) | __popc(me);
+    __syncthreads();
+    uint32_t bg = s_base_gt, be = s_base_eq;
+    for (int w2 = 0; w2 < warp; ++w2) {
+      bg += wcount[w2] >> 16;
+      be += wcount[w2] & 0xffffu;
+    }
+    const uint32_t below = (1u << lane) - 1u;
+    const uint32_t rg = bg + __popc(mg & below), re = be + __popc(me & below);
+    // position in the output: ascending index order, "equal" keys only while the quota lasts
+    // (the rank among all selected = rank among "above" + rank among the admitted "equal")
+    if (gt) out[rg + min(re, need)] = s;
+    if (eq && re < need) out[rg + re] = s;
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t tg = 0, te = 0;
+      for (int w2 = 0; w2 < kTkThreads / 32; ++w2) {
+        tg += wcount[w2] >> 16;
+        te += wcount[w2] & 0xffffu;
+      }
+      s_base_gt += tg;
+      s_base_eq += te;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_indexer_logits(const IndexerArgs& a, int num_sms, cudaStream_t s) {
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (!(configured.load(std::memory_order_acquire) & bit) || !bit) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(indexer_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kIxSmem));
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_release);
+  }
+  alignas(64) CUtensorMap kmap;
+  alignas(64) CUtensorMap qmap;
+  cudaError_t e = index_key_map(a, &kmap);
+  if (e == cudaSuccess) e = index_q_map(a, &qmap);
+  if (e != cudaSuccess) return e;
+  indexer_logits_kernel<<<num_sms, kIxThreads, kIxSmem, s>>>(a, kmap, qmap);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_indexer_topk(const IndexerArgs& a, cudaStream_t s) {
+  indexer_topk_kernel<<<a.T, kTkThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace smla

@@ -58,6 +58,31 @@ cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, float kv_scale, c
                         const void* rope, const int64_t* slot_mapping, int64_t n, void* kv,
                         int64_t num_slots, cudaStream_t s);
 cudaError_t launch_gather_dequant(const DecodeArgs& a, float* rows, cudaStream_t s);
+
+// ------------------------------------------------------------------------------ indexer
+
+// Requests an indexer call may hold (the logits kernel keeps their schedule prefix in
+// shared memory).
+constexpr int kIxMaxRequests = 8192;
+
+struct IndexerArgs {
+  const uint8_t* q;         // [T, H, 128] E4M3 codes
+  const float* weights;     // [T, H] fp32
+  const uint8_t* cache;     // [num_pages, P * 132]: P x 128 E4M3 codes, then P fp32 scales
+  const int32_t* page_table;
+  const int32_t* ctx;       // [B] context lengths
+  float* logits;            // [T, logits_stride] fp32
+  int32_t* topk;            // [T, K] int32
+  int32_t* err;             // device error word
+  int32_t T, H, B, next_n, stride, log2_page, logits_stride, K;
+  int64_t num_pages;
+};
+// Tensor map of the index-key cache as [num_pages][P][128] bytes with [1 x P x 128] boxes,
+// 128-byte swizzle; of q as [T H rows, 128] bytes with [H next_n x 128] boxes, 128-byte swizzle.
+cudaError_t index_key_map(const IndexerArgs& a, CUtensorMap* out);
+cudaError_t index_q_map(const IndexerArgs& a, CUtensorMap* out);
+cudaError_t launch_indexer_logits(const IndexerArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_indexer_topk(const IndexerArgs& a, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t* err, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace smla

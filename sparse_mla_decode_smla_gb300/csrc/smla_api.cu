@@ -166,6 +166,37 @@ smla::DecodeArgs make_args(const smla_desc* d, const void* q, const void* kv,
   return a;
 }
 
+smla_status check_indexer_desc(const smla_indexer_desc* d) {
+  if (!d) return SMLA_ERR_NULL;
+  if (d->num_requests < 1 || d->num_requests > smla::kIxMaxRequests || d->next_n < 1 || d->next_n > 4)
+    return SMLA_ERR_SHAPE;
+  if (int64_t(d->num_tokens) != int64_t(d->num_requests) * d->next_n) return SMLA_ERR_SHAPE;
+  if (d->num_heads != 32 && d->num_heads != 64) return SMLA_ERR_SHAPE;
+  if (d->num_heads * d->next_n > 256) return SMLA_ERR_SHAPE;
+  if (d->page_size != 16 && d->page_size != 32 && d->page_size != 64 && d->page_size != 128) return SMLA_ERR_SHAPE;
+  if (d->page_table_stride < 1 || d->num_pages < 1 || d->num_pages >= (int64_t(1) << 31)) return SMLA_ERR_SHAPE;
+  if (d->logits_stride < 1 || d->topk < 1) return SMLA_ERR_SHAPE;
+  for (int i = 0; i < 4; ++i)
+    if (d->reserved[i] != 0) return SMLA_ERR_SHAPE;
+  return SMLA_OK;
+}
+
+smla::IndexerArgs make_indexer_args(const smla_indexer_desc* d, const int32_t* ctx) {
+  smla::IndexerArgs a;
+  memset(&a, 0, sizeof(a));
+  a.ctx = ctx;
+  a.T = d->num_tokens;
+  a.H = d->num_heads;
+  a.B = d->num_requests;
+  a.next_n = d->next_n;
+  a.stride = d->page_table_stride;
+  a.log2_page = ilog2(d->page_size);
+  a.logits_stride = d->logits_stride;
+  a.K = d->topk;
+  a.num_pages = d->num_pages;
+  return a;
+}
+
 // The status smla_read_error reports for a device error word: a timeout first (every
 // output of the call is invalid), then invalid entries, then operands outside the f16 window.
 smla_status error_status(int32_t v) {
@@ -320,6 +351,45 @@ smla_status smla_gather_dequant(const smla_desc* d, const void* kv_cache,
   a.err = error_word;
   if (smla::launch_gather_dequant(a, rows, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+smla_status smla_indexer_logits(const smla_indexer_desc* d, const void* q, const float* weights,
+                                const void* k_cache, const int32_t* page_table, const int32_t* context_lens,
+                                float* logits, int32_t* error_word, void* stream) {
+  smla_status st = check_indexer_desc(d);
+  if (st != SMLA_OK) return st;
+  if (!q || !weights || !k_cache || !page_table || !context_lens || !logits || !error_word) return SMLA_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(weights, 16) || !aligned(k_cache, 16) || !aligned(page_table, 4) ||
+      !aligned(context_lens, 4) || !aligned(logits, 4) || !aligned(error_word, 4))
+    return SMLA_ERR_ALIGN;
+  int sms = 0;
+  st = current_device(&sms);
+  if (st != SMLA_OK) return st;
+  smla::IndexerArgs a = make_indexer_args(d, context_lens);
+  a.q = static_cast<const uint8_t*>(q);
+  a.weights = weights;
+  a.cache = static_cast<const uint8_t*>(k_cache);
+  a.page_table = page_table;
+  a.logits = logits;
+  a.err = error_word;
+  if (smla::launch_indexer_logits(a, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+smla_status smla_indexer_topk(const smla_indexer_desc* d, const float* logits, const int32_t* context_lens,
+                              int32_t* topk, void* stream) {
+  smla_status st = check_indexer_desc(d);
+  if (st != SMLA_OK) return st;
+  if (!logits || !context_lens || !topk) return SMLA_ERR_NULL;
+  if (!aligned(logits, 4) || !aligned(context_lens, 4) || !aligned(topk, 4)) return SMLA_ERR_ALIGN;
+  int sms = 0;
+  st = current_device(&sms);
+  if (st != SMLA_OK) return st;
+  smla::IndexerArgs a = make_indexer_args(d, context_lens);
+  a.logits = const_cast<float*>(logits);
+  a.topk = topk;
+  if (smla::launch_indexer_topk(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;
 }
 

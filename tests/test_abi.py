@@ -158,3 +158,25 @@ def test_selftest_wait_rejects_bad_arguments(L):
     assert L.smla_selftest_wait_timeout(None, 10, None) == 1
     assert L.smla_selftest_wait_timeout(P(16), 0, None) == 2
     assert L.smla_selftest_wait_timeout(P(16), 200000, None) == 2
+
+
+def test_indexer_desc_layout_and_host_checks(L):
+    assert ctypes.sizeof(smla.smla_indexer_desc) == 56
+    assert smla.smla_indexer_desc.num_pages.offset == 24
+    P = ctypes.c_void_p
+
+    def status(**kw):
+        d = smla.make_indexer_desc(4, 1, 64, 64, 16, 8, 1024, 256)
+        for k, v in kw.items():
+            setattr(d, k, v)
+        return L.smla_indexer_logits(ctypes.byref(d), P(16), P(16), P(16), P(16), P(16), P(16), P(16), None)
+
+    assert status(num_heads=48) == 2
+    assert status(next_n=5, num_tokens=20) == 2
+    assert status(num_tokens=5) == 2                       # T must be B * next_n
+    assert status(page_size=256) == 2
+    assert status(num_requests=9000, num_tokens=9000) == 2
+    d = smla.make_indexer_desc(4, 1, 64, 64, 16, 8, 1024, 256)
+    assert L.smla_indexer_logits(ctypes.byref(d), None, P(16), P(16), P(16), P(16), P(16), P(16), None) == 1
+    assert L.smla_indexer_logits(ctypes.byref(d), P(8), P(16), P(16), P(16), P(16), P(16), P(16), None) == 3
+    assert L.smla_indexer_topk(ctypes.byref(d), P(16), None, P(16), None) == 1
