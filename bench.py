@@ -429,6 +429,119 @@ def gpu_arm(args):
     return 0
 
 
+# ------------------------------------------------------------------------------ indexer arm
+
+
+def indexer_work(problem, ix) -> dict:
+    """Algorithmic work of one indexer pass (logits + top-k) over a batch."""
+    w = problem.w
+    ctx = ix.ctx.cpu().tolist()
+    vis = [max(0, ctx[t // w.next_n] - w.next_n + 1 + t % w.next_n) for t in range(w.num_tokens)]
+    key_bytes = sum(max(0, c) for c in ctx) * (W.INDEX_DIM + 4)  # each request's keys, read once
+    io_bytes = w.num_tokens * ix.heads * (W.INDEX_DIM + 4) + w.num_tokens * w.topk * 4
+    flops = sum(vis) * ix.heads * W.INDEX_DIM * 2
+    return {"key_bytes": key_bytes, "bytes": key_bytes + io_bytes, "flops": flops,
+            "logit_bytes": sum(vis) * 4, "visible": sum(vis)}
+
+
+def run_indexer_oracle_sample(problem, ix, budget_s: float):
+    """The float64 indexer oracle (logits + top-k) on whole query tokens, until budget_s."""
+    from oracle import indexer_oracle as IX
+    w = problem.w
+    pt = problem.page_table.cpu().numpy()
+    q = ix.q.cpu().numpy()
+    wt = ix.weights.cpu().double().numpy()
+    ctx = ix.ctx.cpu().numpy()
+    done, el = 0, 0.0
+    for t in range(0, w.num_tokens, max(1, w.num_tokens // 32)):
+        r, i = divmod(t, w.next_n)
+        n = IX.visible_len(ctx[r], w.next_n, i)
+        npg = -(-n // w.page_size)
+        cache = {int(pg): ix.cache[int(pg)].cpu().numpy() for pg in pt[r][:npg]}
+        t0 = time.perf_counter()
+        keys, sc = IX.request_keys(cache, pt[r], n, w.page_size)
+        IX.topk_set(IX.logits_of_token(q[t], wt[t], keys, sc), w.topk)
+        el += time.perf_counter() - t0
+        done += 1
+        if el >= budget_s:
+            break
+    return done, el
+
+
+def indexer_arm(args):
+    """The indexer (smla_indexer_logits + smla_indexer_topk) on the batch shape of a decode workload."""
+    import sparse_mla_decode_smla_gb300 as smla
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = workload_from_args(args)
+    problem = W.make_problem(w, device=dev)
+    ix = W.make_indexer_inputs(problem, device=dev)
+    stride = w.page_table_stride * w.page_size
+    desc = smla.make_indexer_desc(w.num_requests, w.next_n, ix.heads, w.page_size, problem.num_pages,
+                                  w.page_table_stride, stride, w.topk)
+    pt = problem.page_table.to(device=dev, dtype=torch.int32).contiguous()
+    logits = torch.empty((w.num_tokens, stride), dtype=torch.float32, device=dev)
+    topk = torch.empty((w.num_tokens, w.topk), dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    work = indexer_work(problem, ix)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        smla.indexer_logits(desc, ix.q, ix.weights, ix.cache, pt, ix.ctx, logits, err)
+        if ev:
+            ev[1].record(stream)
+        smla.indexer_topk(desc, logits, ix.ctx, topk)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            step(evs[i])
+        torch.cuda.synchronize(dev)
+    lg_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    tk_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    ms = lg_ms + tk_ms
+    assert err.item() == 0, f"indexer error word {err.item()}"
+    peaks = measured_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # the measured bf16 peak x the nominal fp8 / bf16 ratio of 2
+    t_hbm = work["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = work["flops"] / (fp8_peak * 1e12)
+    if t_hbm >= t_tc:
+        ach = work["bytes"] / (lg_ms * 1e-3) / 1e9
+        rl = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+              "frac": ach / peaks["hbm_gbs"], "peak_source": peaks["source"] + " hbm_gbs (burst)"}
+    else:
+        ach = work["flops"] / (lg_ms * 1e-3) / 1e12
+        rl = {"bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
+              "frac": ach / fp8_peak, "peak_source": peaks["source"] + " bf16_tflops (burst) x 2 (fp8)"}
+    rl.update({"kernel": "indexer_logits_kernel", "kernel_ms": lg_ms, "traffic": None})
+    line = {"metric": "indexer query-tokens/s", "value": w.num_tokens / (ms * 1e-3), "unit": "query-tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": w.name, "op": "indexer", "tokens": w.num_tokens, "next_n": w.next_n,
+                       "index_heads": ix.heads, "topk": w.topk, "visible_slots": work["visible"],
+                       "l2": "flushed between timed steps (512 MiB write, outside the events)"},
+            "roofline": rl, "kernels_ms": {"indexer_logits_kernel": lg_ms, "indexer_topk_kernel": tk_ms},
+            "algorithmic": work, "gpu_launches": 2 * args.steps, "clocks": clk.summary()}
+    if args.cpu_baseline_seconds > 0:
+        n, el = run_indexer_oracle_sample(problem, ix, args.cpu_baseline_seconds)
+        line["cpu_baseline"] = {"value": n / el, "unit": "query-tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{n} of {w.num_tokens} query tokens, indexer oracle (logits + top-k) "
+                                          f"time {el:.1f} s, numpy float64, 1 BLAS thread"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -437,6 +550,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=[w.name for w in W.WORKLOADS + W.EXTRA_WORKLOADS])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--op", default="decode", choices=["decode", "indexer"],
+                    help="decode (the hot path, default) or the indexer that produces its top-k indices")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     ap.add_argument("--ref-budget-seconds", type=float, default=60.0,
@@ -450,6 +565,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return reference_arm(args)
+    if args.op == "indexer":
+        return indexer_arm(args)
     return gpu_arm(args)
 
 

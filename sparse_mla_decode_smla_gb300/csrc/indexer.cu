@@ -25,11 +25,16 @@
 //    stores of the visible logits.
 // Every wait is bounded; a wait that gives up sets SMLA_DEVERR_TIMEOUT.
 //
-// indexer_topk_kernel: one CTA per token, radix select over the token's visible logits (keys
-// made order-preserving as unsigned 32-bit integers; three passes of 11, 11 and 10 bits with
-// shared-memory histograms) to the K-th largest value, then one ordered pass that writes every
-// index above it and, among indices equal to it, the lowest ones up to K: the output is the
-// top-k set in ascending index order.
+// indexer_topk_kernel: one CTA of 1024 threads per token, radix select over the token's visible
+// logits (keys made order-preserving as unsigned 32-bit integers; three passes of 11, 11 and
+// 10 bits with shared-memory histograms, eight loads in flight per thread) to the K-th largest
+// value; then each warp counts the keys above and equal to it in its contiguous segment, the
+// counts are scanned across warps, and each warp writes every index above the threshold and,
+// among indices equal to it, the lowest ones up to K: the top-k set in ascending index order.
+//
+// The producer warp prefetches the next item's page-table entries into shared memory by
+// cp.async while lane 0 issues the current item's copies, and the epilogue hands a stage back
+// as soon as it has read the stage's key scales.
 #include <math_constants.h>
 #include <string.h>
 
@@ -45,7 +50,7 @@ namespace {
 constexpr int kIxDim = 128;              // index dims (bytes of E4M3 per key or q row)
 constexpr int kIxTile = 128;             // slots per tile (the MMA's M)
 constexpr int kIxChunk = 1024;           // slots per scheduled item
-constexpr int kIxStages = 4;
+constexpr int kIxStages = 6;
 constexpr int kIxEpiWarps = 8;
 constexpr int kIxFirstEpi = 2;
 constexpr int kIxThreads = 32 * (kIxFirstEpi + kIxEpiWarps);
@@ -57,7 +62,8 @@ constexpr size_t kIxStageK = size_t(kIxTile) * kIxDim;
 constexpr size_t kIxOffSc = kIxOffK + kIxStages * kIxStageK;    // [stage][128] fp32 scales
 constexpr size_t kIxOffW = kIxOffSc + kIxStages * kIxTile * 4;  // [N] fp32 weights
 constexpr size_t kIxOffPre = kIxOffW + kIxMaxN * 4;             // [kIxMaxReq + 1] item prefix
-constexpr size_t kIxOffTm = kIxOffPre + size_t(kIxMaxRequests + 1) * 4;
+constexpr size_t kIxOffPg = kIxOffPre + size_t(kIxMaxRequests + 1) * 4;  // [2][64] page entries
+constexpr size_t kIxOffTm = kIxOffPg + 2 * 64 * 4;
 constexpr size_t kIxOffBars = (kIxOffTm + 16 + 7) / 8 * 8;
 enum { X_FULL = 0, X_EMPTY = X_FULL + kIxStages, X_DFULL = X_EMPTY + kIxStages, X_DEMPTY = X_DFULL + 2,
        X_QFULL = X_DEMPTY + 2, X_QFREE, X_DRAIN, X_COUNT };
@@ -186,44 +192,69 @@ __global__ void __launch_bounds__(kIxThreads, 1)
   bool ok = true;
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      int u = 0, qloads = 0, rq = -1, r = r_first;
-      for (int it = it0; it < it1 && ok; ++it) {
-        const Item x = item_at(it, r);
-        r = x.r;
+    // The warp prefetches the next item's page-table entries (1024 / P pages, two per lane) by
+    // 4-byte cp.async into a two-item shared ring while lane 0 issues the current item's
+    // copies, so no tile waits on a dependent page-table load.
+    const int ppi = kIxChunk >> p.log2_page;  // pages per item
+    const int npg = kIxTile >> p.log2_page;   // pages per tile (P <= 128)
+    int32_t* spg = reinterpret_cast<int32_t*>(sm + kIxOffPg);
+    auto prefetch = [&](const Item& x, int buf) {
+      const int32_t* pt_row = p.page_table + int64_t(x.r) * p.stride;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int li = lane + 32 * k, lp = x.c * ppi + li;
+        if (li < ppi && lp < p.stride)
+          cp_async4(smem_u32(spg + buf * 64 + li), pt_row + lp);
+        else
+          spg[buf * 64 + li] = -1;
+      }
+      cp_async_commit();
+    };
+    if (it0 < it1) prefetch(item_at(it0, r_first), 0);
+    int u = 0, qloads = 0, rq = -1, r = r_first;
+    for (int it = it0; it < it1 && ok; ++it) {
+      const Item x = item_at(it, r);
+      r = x.r;
+      const int buf = (it - it0) & 1;
+      if (it + 1 < it1)
+        prefetch(item_at(it + 1, r), buf ^ 1);
+      else
+        cp_async_commit();  // an empty group keeps the count of groups in flight at one
+      cp_async_wait<1>();   // this item's entries have landed
+      __syncwarp();
+      if (lane == 0) {
         if (x.r != rq) {  // q and weights of the request, once the previous ones are unused
-          if (qloads > 0 && !mbar_wait(bar(X_QFREE), (qloads - 1) & 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(X_QFULL), uint32_t(N) * kIxDim + uint32_t(N) * 4u);
-          tma_load_2d(sb + uint32_t(kIxOffQ), &qmap, 0, x.r * N, bar(X_QFULL));
-          bulk_g2s(sb + uint32_t(kIxOffW), p.weights + int64_t(x.r) * N, uint32_t(N) * 4u, bar(X_QFULL));
-          ++qloads;
-          rq = x.r;
+          if (qloads > 0 && !mbar_wait(bar(X_QFREE), (qloads - 1) & 1)) ok = false;
+          if (ok) {
+            mbar_arrive_expect_tx(bar(X_QFULL), uint32_t(N) * kIxDim + uint32_t(N) * 4u);
+            tma_load_2d(sb + uint32_t(kIxOffQ), &qmap, 0, x.r * N, bar(X_QFULL));
+            bulk_g2s(sb + uint32_t(kIxOffW), p.weights + int64_t(x.r) * N, uint32_t(N) * 4u, bar(X_QFULL));
+            ++qloads;
+            rq = x.r;
+          }
         }
-        const int32_t* pt_row = p.page_table + int64_t(x.r) * p.stride;
+        const int ctx = ctx_of(x.r);
         const int nt = tiles_of(x);
-        for (int j = 0; j < nt; ++j, ++u) {
+        for (int j = 0; j < nt && ok; ++j, ++u) {
           const int st = u % kIxStages;
           if (!mbar_wait(bar(X_EMPTY + st), ((u / kIxStages) & 1) ^ 1)) { ok = false; break; }
-          const int s0 = x.c * kIxChunk + j * kIxTile;
-          const int npg = kIxTile >> p.log2_page;  // pages per tile (P <= 128)
           // pages outside the request's table or the pool are not fetched: their rows keep
           // stale bytes, which only feed logits beyond the visible range or flagged ones
           uint32_t bytes = 0, mask = 0;
-          const int ctx = ctx_of(x.r);
           for (int g = 0; g < npg; ++g) {
-            const int lp = (s0 >> p.log2_page) + g;
-            const int32_t pg = lp < p.stride ? __ldg(pt_row + lp) : -1;
+            const int li = j * npg + g;
+            const int32_t pg = spg[buf * 64 + li];
             if (pg >= 0 && pg < p.num_pages) {
               mask |= 1u << g;
               bytes += uint32_t(P) * (kIxDim + 4);
-            } else if ((lp << p.log2_page) < ctx) {  // a page the visible context needs
+            } else if (((x.c * ppi + li) << p.log2_page) < ctx) {  // a page the visible context needs
               atomicOr(p.err, SMLA_DEVERR_PAGE);
             }
           }
           mbar_arrive_expect_tx(bar(X_FULL + st), bytes);
           for (int g = 0; g < npg; ++g) {
             if (!((mask >> g) & 1u)) continue;
-            const int32_t pg = __ldg(pt_row + (s0 >> p.log2_page) + g);
+            const int32_t pg = spg[buf * 64 + j * npg + g];
             tma_load_3d(sb + uint32_t(kIxOffK + st * kIxStageK) + uint32_t(g * P * kIxDim), &kmap, 0, 0, pg,
                         bar(X_FULL + st));
             bulk_g2s(sb + uint32_t(kIxOffSc) + uint32_t(st * kIxTile * 4 + g * P * 4),
@@ -232,7 +263,14 @@ __global__ void __launch_bounds__(kIxThreads, 1)
           }
         }
       }
-      // no copy may land after the CTA has left
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      qloads = __shfl_sync(0xffffffffu, qloads, 0);
+      rq = __shfl_sync(0xffffffffu, rq, 0);
+    }
+    cp_async_wait<0>();
+    // no copy may land after the CTA has left
+    if (lane == 0) {
       for (int v = max(0, u - kIxStages); v < u; ++v)
         if (!mbar_wait(bar(X_FULL + v % kIxStages), (v / kIxStages) & 1)) break;
       if (qloads > 0) mbar_wait(bar(X_QFULL), (qloads - 1) & 1);
@@ -299,6 +337,10 @@ __global__ void __launch_bounds__(kIxThreads, 1)
         tc::fence_after();
         const int s = x.c * kIxChunk + j * kIxTile + row;
         const float sc = lds_f32(sb + uint32_t(kIxOffSc) + uint32_t(st * kIxTile + row) * 4);
+        // the scale is in a register: the stage goes back to the producer (its codes were
+        // consumed by the MMAs, whose commit is the stage's other arrival)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(X_EMPTY + st));
         for (int i = i_lo; i < i_hi; ++i) {
           float acc = 0.f;
 #pragma unroll
@@ -317,10 +359,7 @@ __global__ void __launch_bounds__(kIxThreads, 1)
         }
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(X_DEMPTY + b));
-          mbar_arrive(bar(X_EMPTY + st));
-        }
+        if (lane == 0) mbar_arrive(bar(X_DEMPTY + b));
       }
       const bool last_of_req = it + 1 >= it1 || item_at(it + 1, r).r != x.r;
       if (last_of_req && ok) {
@@ -340,7 +379,9 @@ __global__ void __launch_bounds__(kIxThreads, 1)
 
 // ------------------------------------------------------------------------------ top-k
 
-constexpr int kTkThreads = 512;
+constexpr int kTkThreads = 1024;
+constexpr int kTkWarps = kTkThreads / 32;
+constexpr int kTkUnroll = 8;  // independent loads in flight per thread
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f);
@@ -350,8 +391,7 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerArgs p) {
   __shared__ uint32_t hist[2048];
   __shared__ uint32_t s_need, s_sel;
-  __shared__ uint32_t wcount[kTkThreads / 32];
-  __shared__ uint32_t s_base_gt, s_base_eq;
+  __shared__ uint32_t wgt[kTkWarps], weq[kTkWarps];
   const int t = blockIdx.x;
   const int r = t / p.next_n;
   const int i = t - r * p.next_n;
@@ -373,15 +413,22 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
     const uint32_t hmask = pass == 0 ? 0u : (0xffffffffu << (sh + width));
     for (int k = tid; k < nb; k += kTkThreads) hist[k] = 0;
     __syncthreads();
-    for (int s = tid; s < vis; s += kTkThreads) {
-      const uint32_t key = order_key(__ldg(lg + s));
-      if ((key & hmask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
+    for (int s0 = tid; s0 < vis; s0 += kTkThreads * kTkUnroll) {
+      uint32_t key[kTkUnroll];
+#pragma unroll
+      for (int k = 0; k < kTkUnroll; ++k) {
+        const int s = s0 + k * kTkThreads;
+        key[k] = s < vis ? order_key(__ldg(lg + s)) : 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < kTkUnroll; ++k)
+        if (s0 + k * kTkThreads < vis && (key[k] & hmask) == prefix) atomicAdd(&hist[(key[k] >> sh) & (nb - 1)], 1u);
     }
     __syncthreads();
     if (warp == 0) {  // walk the bins from the top until `need` is reached
       uint32_t acc = 0;
-      int sel = -1;
-      for (int b0 = nb - 32; b0 >= 0 && sel < 0; b0 -= 32) {
+      bool found = false;
+      for (int b0 = nb - 32; b0 >= 0 && !found; b0 -= 32) {
         const uint32_t c = hist[b0 + 31 - lane];  // lane 0 holds the highest bin of the group
         uint32_t x = c;
 #pragma unroll
@@ -389,8 +436,7 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
           const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
           if (lane >= o) x += y;
         }
-        const bool reach = acc + x >= need;
-        const uint32_t m = __ballot_sync(0xffffffffu, reach);
+        const uint32_t m = __ballot_sync(0xffffffffu, acc + x >= need);
         if (m) {
           const int l = __ffs(m) - 1;
           const uint32_t before = __shfl_sync(0xffffffffu, x - c, l);
@@ -398,7 +444,7 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
             s_sel = uint32_t(b0 + 31 - l);
             s_need = need - (acc + before);
           }
-          sel = 1;
+          found = true;
         }
         acc += __shfl_sync(0xffffffffu, x, 31);
       }
@@ -409,41 +455,49 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
     __syncthreads();
   }
   // prefix is the K-th largest key; `need` keys equal to it complete the set (the lowest
-  // indices among them). One ordered pass: block-wide ranks of the "above" and "equal" flags.
-  if (tid == 0) {
-    s_base_gt = 0;
-    s_base_eq = 0;
+  // indices among them). Warp w owns the contiguous segment [w seg, (w + 1) seg): it counts
+  // its keys above and equal to the threshold, the counts are scanned across warps, and then
+  // every warp writes its selected indices in order (ballots within 32-slot chunks).
+  const int seg = (vis + kTkWarps - 1) / kTkWarps;
+  const int a0 = min(vis, warp * seg), a1 = min(vis, a0 + seg);
+  uint32_t ngt = 0, neq = 0;
+  for (int s0 = a0; s0 < a1; s0 += 32 * kTkUnroll) {
+    uint32_t key[kTkUnroll];
+#pragma unroll
+    for (int k = 0; k < kTkUnroll; ++k) {
+      const int s = s0 + 32 * k + lane;
+      key[k] = s < a1 ? order_key(__ldg(lg + s)) : 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < kTkUnroll; ++k) {
+      const bool in = s0 + 32 * k + lane < a1;
+      ngt += __popc(__ballot_sync(0xffffffffu, in && key[k] > prefix));
+      neq += __popc(__ballot_sync(0xffffffffu, in && key[k] == prefix));
+    }
+  }
+  if (lane == 0) {
+    wgt[warp] = ngt;
+    weq[warp] = neq;
   }
   __syncthreads();
-  for (int s0 = 0; s0 < vis; s0 += kTkThreads) {
-    const int s = s0 + tid;
-    const uint32_t key = s < vis ? order_key(__ldg(lg + s)) : 0u;
-    const bool gt = s < vis && key > prefix, eq = s < vis && key == prefix;
+  uint32_t bg = 0, be = 0;
+  for (int w2 = 0; w2 < warp; ++w2) {
+    bg += wgt[w2];
+    be += weq[w2];
+  }
+  const uint32_t below = (1u << lane) - 1u;
+  for (int s0 = a0; s0 < a1; s0 += 32) {
+    const int s = s0 + lane;
+    const uint32_t key = s < a1 ? order_key(__ldg(lg + s)) : 0u;
+    const bool gt = s < a1 && key > prefix, eq = s < a1 && key == prefix;
     const uint32_t mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) wcount[warp] = (__popc(mg) << 16) | __popc(me);
-    __syncthreads();
-    uint32_t bg = s_base_gt, be = s_base_eq;
-    for (int w2 = 0; w2 < warp; ++w2) {
-      bg += wcount[w2] >> 16;
-      be += wcount[w2] & 0xffffu;
-    }
-    const uint32_t below = (1u << lane) - 1u;
     const uint32_t rg = bg + __popc(mg & below), re = be + __popc(me & below);
-    // position in the output: ascending index order, "equal" keys only while the quota lasts
-    // (the rank among all selected = rank among "above" + rank among the admitted "equal")
+    // the output position: the selected keys before this one, "above" ones plus the admitted
+    // "equal" ones (the first `need` equal keys in index order are admitted)
     if (gt) out[rg + min(re, need)] = s;
     if (eq && re < need) out[rg + re] = s;
-    __syncthreads();
-    if (tid == 0) {
-      uint32_t tg = 0, te = 0;
-      for (int w2 = 0; w2 < kTkThreads / 32; ++w2) {
-        tg += wcount[w2] >> 16;
-        te += wcount[w2] & 0xffffu;
-      }
-      s_base_gt += tg;
-      s_base_eq += te;
-    }
-    __syncthreads();
+    bg += __popc(mg);
+    be += __popc(me);
   }
 }
 
