@@ -317,3 +317,62 @@ def gather_dequant(fetch_rows, kv_format: str, page_table, topk, page_size: int,
         if keep:
             out[t, keep] = dequant_rows(fetch_rows(phys), kv_format, kv_scale)
     return out
+
+
+# --------------------------------------------------------------------------- #
+# Quantise-on-write store fused with the latent's norm and the key's RoPE
+# --------------------------------------------------------------------------- #
+# The compressor's store of the vLLM PR #43827 page ("实现拆解 4-6":
+# SparseAttnCompressNormRopeStoreFullC4Kernel with store_full_kv / store_full_fp8, and the
+# fused "qnorm rope kv insert" test): normalise the latent, rotate the RoPE part, quantise and
+# store the row. The page names the steps, not their formulas; the readings are: RMSNorm over
+# the 512 latent dims with a per-dim weight, y = x / sqrt(mean(x^2) + eps) * w; the rotation
+# turns adjacent pairs (2j, 2j+1) of the 64 RoPE dims by the angle whose cosine and sine the
+# caller's table holds for the row's position; both results are rounded to bf16 (the values
+# an unfused pipeline would store), then packed exactly as pack_fp8_ds / pack_fp8_tensor /
+# pack_bf16 pack them.
+
+
+def bf16_rne(x) -> np.ndarray:
+    """float64 -> nearest bf16 value (round half to even, 8 significant bits), as float64.
+    Finite inputs of normal bf16 magnitude (the only ones used here)."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)  # x = m * 2^e, |m| in [0.5, 1)
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """bf16 values (exactly representable) -> uint16 bit patterns."""
+    return (np.asarray(x, dtype=np.float64).astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def rms_norm_bf16(latent_bits: np.ndarray, weight_bits: np.ndarray, eps: float) -> np.ndarray:
+    """[n, 512] bf16 latents (bit patterns) -> bf16 values of x / sqrt(mean(x^2) + eps) * w (float64)."""
+    x = bf16_bits_to_f64(latent_bits).reshape(-1, LATENT)
+    w = bf16_bits_to_f64(weight_bits).reshape(LATENT)
+    r = 1.0 / np.sqrt((x * x).mean(axis=1, keepdims=True) + float(np.float32(eps)))
+    return bf16_rne(x * r * w[None, :])
+
+
+def rope_bf16(rope_bits: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.ndarray:
+    """[n, 64] bf16 RoPE values -> bf16 values of the pairs (2j, 2j+1) rotated by the angle with
+    cosine cos[:, j] and sine sin[:, j] ([n, 32] each, fp32 values): (a c - b s, a s + b c)."""
+    r = bf16_bits_to_f64(rope_bits).reshape(-1, ROPE)
+    a, b = r[:, 0::2], r[:, 1::2]
+    c, s = np.asarray(cos, dtype=np.float64), np.asarray(sin, dtype=np.float64)
+    out = np.empty_like(r)
+    out[:, 0::2] = a * c - b * s
+    out[:, 1::2] = a * s + b * c
+    return bf16_rne(out)
+
+
+def store_normed_rows(latent_bits, rope_bits, weight_bits, eps, cos, sin, kv_format: str,
+                      scale_mode: int = SCALE_POW2, kv_scale: float | None = None) -> np.ndarray:
+    """Cache rows of the fused store: norm + rotation (bf16), then the format's packer."""
+    lat = f64_to_bf16_bits(rms_norm_bf16(latent_bits, weight_bits, eps))
+    rope = f64_to_bf16_bits(rope_bf16(rope_bits, cos, sin))
+    if kv_format == "bf16":
+        return pack_bf16(lat, rope)
+    if kv_format == "fp8_tensor":
+        return pack_fp8_tensor(lat, rope, kv_scale)
+    return pack_fp8_ds(lat, rope, scale_mode)

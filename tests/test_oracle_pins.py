@@ -429,3 +429,67 @@ def test_gather_dequant_rows_and_padding():
     assert (g[0, 1] == 0).all()
     np.testing.assert_array_equal(g[0, 0], O.dequant_rows(rows[[pt[0, 1] * 64 + 6]], "fp8_ds")[0])
     np.testing.assert_array_equal(g[0, 2], O.dequant_rows(rows[[pt[0, 0] * 64 + 3]], "fp8_ds")[0])
+
+
+# ----------------------------------------------------------------------------- fused store
+
+def test_bf16_rne_matches_torch_rounding():
+    x = np.random.default_rng(5).normal(size=4000) * 7.3
+    got = O.bf16_rne(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()  # torch rounds f64 -> bf16
+    assert np.array_equal(got, ref)
+    # ties to even: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7
+    assert O.bf16_rne(np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8])).tolist() == [1.0, 1 + 2 * 2.0 ** -7]
+
+
+def test_rms_norm_closed_forms():
+    # a constant row c: mean(x^2) = c^2, so y = w * c / sqrt(c^2 + eps); with eps = 0, y = w * sign(c)
+    c = np.full((1, 512), -3.0)
+    w = np.linspace(0.5, 2.0, 512)
+    y = O.rms_norm_bf16(_bits(torch.tensor(c).to(torch.bfloat16)), _bits(torch.tensor(w).to(torch.bfloat16)), 0.0)
+    wq = torch.tensor(w).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(y[0], O.bf16_rne(-wq))
+    # scaling x by any positive factor leaves the eps = 0 norm unchanged
+    g = torch.Generator().manual_seed(2)
+    x = torch.randn(3, 512, generator=g).to(torch.bfloat16)
+    wb = torch.ones(512).to(torch.bfloat16)
+    a = O.rms_norm_bf16(_bits(x), _bits(wb), 0.0)
+    b = O.rms_norm_bf16(_bits((x.double() * 4).to(torch.bfloat16)), _bits(wb), 0.0)
+    assert np.array_equal(a, b)
+
+
+def test_rms_norm_matches_torch_float64():
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(16, 512, generator=g).to(torch.bfloat16)
+    w = (1 + 0.1 * torch.randn(512, generator=g)).to(torch.bfloat16)
+    eps = 1e-6
+    ref = torch.nn.functional.rms_norm(x.double(), (512,), w.double(), eps=float(np.float32(eps)))
+    got = O.rms_norm_bf16(_bits(x), _bits(w), eps)
+    assert np.array_equal(got, O.bf16_rne(ref.numpy()))
+
+
+def test_rope_rotation_special_angles_and_complex_product():
+    g = torch.Generator().manual_seed(8)
+    r = torch.randn(4, 64, generator=g).to(torch.bfloat16)
+    rv = r.double().numpy()
+    one, zero = np.ones((4, 32)), np.zeros((4, 32))
+    assert np.array_equal(O.rope_bf16(_bits(r), one, zero), rv)            # angle 0: identity
+    quarter = O.rope_bf16(_bits(r), zero, one)                               # angle pi/2: (-b, a)
+    assert np.array_equal(quarter[:, 0::2], -rv[:, 1::2]) and np.array_equal(quarter[:, 1::2], rv[:, 0::2])
+    # general angles: the complex product (a + ib) e^{i theta}, by torch
+    th = torch.rand(4, 32, generator=g, dtype=torch.float64) * 6.28
+    cos, sin = torch.cos(th).float().double(), torch.sin(th).float().double()
+    z = torch.view_as_complex(r.double().reshape(4, 32, 2).contiguous()) * torch.complex(cos, sin)
+    ref = torch.view_as_real(z).reshape(4, 64).numpy()
+    assert np.array_equal(O.rope_bf16(_bits(r), cos.numpy(), sin.numpy()), O.bf16_rne(ref))
+
+
+def test_store_normed_rows_is_norm_rope_then_the_packer():
+    g = torch.Generator().manual_seed(9)
+    lat = torch.randn(5, 512, generator=g).to(torch.bfloat16)
+    rope = torch.randn(5, 64, generator=g).to(torch.bfloat16)
+    w = torch.ones(512).to(torch.bfloat16)
+    cos, sin = np.ones((5, 32)), np.zeros((5, 32))
+    rows = O.store_normed_rows(_bits(lat), _bits(rope), _bits(w), 0.0, cos, sin, "fp8_ds")
+    normed = O.rms_norm_bf16(_bits(lat), _bits(w), 0.0)
+    assert np.array_equal(rows, O.pack_fp8_ds(O.f64_to_bf16_bits(normed), _bits(rope)))
