@@ -99,7 +99,7 @@ const char* smla_status_string(int32_t status);
 
 /* ABI version of this header (increments on any incompatible change; 2 added kv_scale,
  * 3 added SMLA_ERR_TIMEOUT, SMLA_ERR_OPERAND_RANGE, SMLA_DEVERR_RANGE,
- * smla_noalloc_read_error and the indexer calls). */
+ * smla_noalloc_read_error, the indexer calls and smla_store_kv_normed). */
 int32_t smla_abi_version(void);
 
 /*
@@ -199,6 +199,38 @@ smla_status smla_pack_kv(int32_t kv_format, int32_t scale_mode, const void* late
 smla_status smla_pack_kv_fp8_tensor(const void* latent, const void* rope,
                                     const int64_t* slot_mapping, int64_t n, float kv_scale,
                                     void* kv_cache, int64_t num_slots, void* stream);
+
+/*
+ * The cache write fused with the latent's normalisation and the key's RoPE (the compressor's
+ * store of vLLM PR #43827, "实现拆解 4-6": SparseAttnCompressNormRopeStoreFullC4Kernel with
+ * store_full_kv / store_full_fp8, tested as a fused "qnorm rope kv insert"). The page names
+ * the steps; this library computes, for each row i with 0 <= slot_mapping[i] < num_slots:
+ *   latent' = bf16(latent[i] * r * norm_weight), r = 1 / sqrt(mean(latent[i]^2) + rms_eps),
+ *             in fp32 (sum of squares in a fixed order, correctly rounded sqrt and divide);
+ *   rope'   = bf16 of the RoPE pairs (2j, 2j+1) = (a, b) turned to (a c - b s, a s + b c), with
+ *             c = cos_sin[positions[i], j] and s = cos_sin[positions[i], 32 + j] (fp32);
+ * and stores (latent', rope') exactly as smla_pack_kv (kv_format BF16 or FP8_DS with
+ * scale_mode) or smla_pack_kv_fp8_tensor (kv_format FP8_TENSOR with kv_scale) would.
+ *   latent [n, 512] and rope [n, 64] bf16, norm_weight [512] bf16: 16-byte aligned.
+ *   positions [n] int64; cos_sin [max_position, 64] fp32; slot_mapping [n] int64.
+ *   error_word: device int32 or NULL; a row whose position is outside [0, max_position) is not
+ *   written and sets SMLA_DEVERR_INDEX.
+ */
+typedef struct smla_store_desc {
+  int32_t kv_format;    /* SMLA_KV_* */
+  int32_t scale_mode;   /* SMLA_SCALE_* (FP8_DS) */
+  float kv_scale;       /* FP8_TENSOR: the per-tensor scale (finite, > 0) */
+  float rms_eps;        /* >= 0 */
+  int64_t n;            /* rows */
+  int64_t num_slots;    /* rows of kv_cache */
+  int64_t max_position; /* rows of cos_sin (>= 1) */
+  int32_t reserved[2];  /* must be zero */
+} smla_store_desc;
+
+smla_status smla_store_kv_normed(const smla_store_desc* d, const void* latent, const void* rope,
+                                 const void* norm_weight, const int64_t* positions,
+                                 const float* cos_sin, const int64_t* slot_mapping, void* kv_cache,
+                                 int32_t* error_word, void* stream);
 
 /*
  * Test hook exposing the gather + dequantise steps of smla_decode

@@ -30,7 +30,7 @@ DEVICE_ERROR_STATUSES = (0, 7, 9, 10)  # statuses that report device error bits
 EXPORTS = ["smla_status_string", "smla_abi_version", "smla_workspace_size", "smla_decode",
            "smla_pack_kv", "smla_gather_dequant", "smla_read_error", "smla_decode_noalloc",
            "smla_set_kernel_events", "smla_pack_kv_fp8_tensor", "smla_selftest_wait_timeout",
-           "smla_noalloc_read_error", "smla_indexer_logits", "smla_indexer_topk"]
+           "smla_noalloc_read_error", "smla_indexer_logits", "smla_indexer_topk", "smla_store_kv_normed"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -56,6 +56,13 @@ class smla_indexer_desc(ctypes.Structure):
                 ("page_size", ctypes.c_int32), ("page_table_stride", ctypes.c_int32),
                 ("num_pages", ctypes.c_int64), ("logits_stride", ctypes.c_int32),
                 ("topk", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+
+
+class smla_store_desc(ctypes.Structure):
+    _fields_ = [("kv_format", ctypes.c_int32), ("scale_mode", ctypes.c_int32),
+                ("kv_scale", ctypes.c_float), ("rms_eps", ctypes.c_float), ("n", ctypes.c_int64),
+                ("num_slots", ctypes.c_int64), ("max_position", ctypes.c_int64),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 _lib = None
@@ -99,6 +106,8 @@ def lib() -> ctypes.CDLL:
         L.smla_indexer_logits.argtypes = [XD, P, P, P, P, P, P, P, P]
         L.smla_indexer_topk.restype = I32
         L.smla_indexer_topk.argtypes = [XD, P, P, P, P]
+        L.smla_store_kv_normed.restype = I32
+        L.smla_store_kv_normed.argtypes = [ctypes.POINTER(smla_store_desc), P, P, P, P, P, P, P, P, P]
         _lib = L
     return _lib
 
@@ -240,3 +249,14 @@ def indexer_topk(desc, logits, context_lens, topk, stream=None):
     """Top-k slots of every token's visible logits (smla_indexer_topk), ascending, -1 padded."""
     _check("smla_indexer_topk", lib().smla_indexer_topk(
         ctypes.byref(desc), _ptr(logits), _ptr(context_lens), _ptr(topk), _stream(stream)))
+
+
+def store_kv_normed(kv_format, latent, rope, norm_weight, eps, positions, cos_sin, slot_mapping, kv_cache,
+                    num_slots, scale_mode=SMLA_SCALE_POW2, kv_scale=1.0, error_word=None, stream=None):
+    """The cache write fused with RMSNorm and RoPE (smla_store_kv_normed)."""
+    d = smla_store_desc()
+    d.kv_format, d.scale_mode, d.kv_scale, d.rms_eps = kv_format, scale_mode, kv_scale, eps
+    d.n, d.num_slots, d.max_position = latent.shape[0], num_slots, cos_sin.shape[0]
+    _check("smla_store_kv_normed", lib().smla_store_kv_normed(
+        ctypes.byref(d), _ptr(latent), _ptr(rope), _ptr(norm_weight), _ptr(positions), _ptr(cos_sin),
+        _ptr(slot_mapping), _ptr(kv_cache), _ptr(error_word), _stream(stream)))

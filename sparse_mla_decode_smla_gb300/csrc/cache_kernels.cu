@@ -7,31 +7,83 @@
 // two block scales).
 // Per-tensor FP8 row (576 B): 576 E4M3FN codes [latent 512 | RoPE 64] of x / kv_scale,
 // one scale for the whole cache (vLLM PR #43827 "实现拆解 4": store_full_fp8).
+#include <string.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace smla {
 
+// The norm and rotation of the fused store (the compressor's store of vLLM PR #43827,
+// "实现拆解 4-6": norm, RoPE and the cache write in one kernel). Inputs and outputs are bf16.
+struct NormRope {
+  const uint4* weight;     // [512] bf16 RMSNorm weight
+  float eps;
+  const int64_t* positions;  // [n] rotary positions
+  const float* cos_sin;    // [max_position, 64] fp32: cos of the 32 pair angles, then their sin
+  int64_t max_position;
+  int32_t* err;            // rows whose position is outside [0, max_position) set SMLA_DEVERR_INDEX
+};
+
+__device__ __forceinline__ uint32_t bf16x2_pack_rn(float lo, float hi) { return pack_bf16x2(lo, hi); }
+
 // One warp per row. Lane l owns latent elements [16l, 16l+16); lanes 8b..8b+7 form block b.
-template <int FMT>
+// With NORM the row is first normalised (RMSNorm over the 512 latent dims: fp32 sum of
+// squares in a fixed order, correctly rounded sqrt and divide, x * r * w rounded to bf16) and
+// its RoPE pairs (2j, 2j+1) are rotated, (a c - b s, a s + b c) rounded to bf16.
+template <int FMT, bool NORM>
 __global__ void __launch_bounds__(256) pack_kernel(const uint4* __restrict__ latent,
                                                    const uint4* __restrict__ rope,
                                                    const int64_t* __restrict__ slot_mapping,
                                                    int64_t n, uint8_t* __restrict__ kv,
                                                    int64_t num_slots, int scale_mode,
-                                                   float kv_scale) {
+                                                   float kv_scale, const NormRope nr) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (row >= n) return;
   const int64_t slot = slot_mapping[row];
   if (slot < 0 || slot >= num_slots) return;
-  const uint4 x0 = latent[row * 64 + 2 * lane];
-  const uint4 x1 = latent[row * 64 + 2 * lane + 1];
+  uint4 x0 = latent[row * 64 + 2 * lane];
+  uint4 x1 = latent[row * 64 + 2 * lane + 1];
+  uint4 rp = lane < 8 ? rope[row * 8 + lane] : make_uint4(0, 0, 0, 0);  // RoPE dims [8 lane, +8)
+  if constexpr (NORM) {
+    const int64_t pos = nr.positions[row];
+    if (pos < 0 || pos >= nr.max_position) {  // the whole warp agrees: skip the row, flag it
+      if (lane == 0 && nr.err) atomicOr(nr.err, SMLA_DEVERR_INDEX);
+      return;
+    }
+    uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(bf16_hi(w[i]), bf16_hi(w[i]), fmaf(bf16_lo(w[i]), bf16_lo(w[i]), ss));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, float(kLatent)), nr.eps)));
+    const uint4 g0 = nr.weight[2 * lane], g1 = nr.weight[2 * lane + 1];
+    const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i] = bf16x2_pack_rn(__fmul_rn(__fmul_rn(bf16_lo(w[i]), r), bf16_lo(gw[i])),
+                            __fmul_rn(__fmul_rn(bf16_hi(w[i]), r), bf16_hi(gw[i])));
+    x0 = make_uint4(w[0], w[1], w[2], w[3]);
+    x1 = make_uint4(w[4], w[5], w[6], w[7]);
+    if (lane < 8) {  // pairs j = 4 lane .. 4 lane + 3, one per bf16 word
+      const float* cs = nr.cos_sin + pos * 64;
+      uint32_t rw[4] = {rp.x, rp.y, rp.z, rp.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float c = cs[4 * lane + k], sn = cs[32 + 4 * lane + k];
+        const float a = bf16_lo(rw[k]), b = bf16_hi(rw[k]);
+        rw[k] = bf16x2_pack_rn(__fsub_rn(__fmul_rn(a, c), __fmul_rn(b, sn)), __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, c)));
+      }
+      rp = make_uint4(rw[0], rw[1], rw[2], rw[3]);
+    }
+  }
   if (FMT == SMLA_KV_BF16) {
     uint4* dst = reinterpret_cast<uint4*>(kv + slot * kBf16RowBytes);
     dst[2 * lane] = x0;
     dst[2 * lane + 1] = x1;
-    if (lane < 8) dst[64 + lane] = rope[row * 8 + lane];
+    if (lane < 8) dst[64 + lane] = rp;
     return;
   }
   if (FMT == SMLA_KV_FP8_TENSOR) {
@@ -47,8 +99,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint4* __restrict__ lat
     }
     *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
     if (lane < 8) {  // RoPE values [8 lane, 8 lane + 8)
-      const uint4 r = rope[row * 8 + lane];
-      const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+      const uint32_t rw[4] = {rp.x, rp.y, rp.z, rp.w};
       uint32_t rc[2];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -99,27 +150,52 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint4* __restrict__ lat
   const float s2 = __shfl_sync(0xffffffffu, scale, 16);
   const float s3 = __shfl_sync(0xffffffffu, scale, 24);
   if (lane == 0) *reinterpret_cast<float4*>(dst + kScaleOff) = make_float4(scale, s1, s2, s3);
-  if (lane < 8) *reinterpret_cast<uint4*>(dst + kRopeOffFp8 + 16 * lane) = rope[row * 8 + lane];
+  if (lane < 8) *reinterpret_cast<uint4*>(dst + kRopeOffFp8 + 16 * lane) = rp;
 }
 
-cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, float kv_scale, const void* latent,
-                        const void* rope, const int64_t* slot_mapping, int64_t n, void* kv,
-                        int64_t num_slots, cudaStream_t s) {
+template <bool NORM>
+cudaError_t launch_pack_impl(int32_t kv_format, int32_t scale_mode, float kv_scale, const void* latent,
+                             const void* rope, const int64_t* slot_mapping, int64_t n, void* kv,
+                             int64_t num_slots, const NormRope& nr, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   const int64_t blocks = (n * 32 + 255) / 256;
   auto* L = static_cast<const uint4*>(latent);
   auto* R = static_cast<const uint4*>(rope);
   auto* K = static_cast<uint8_t*>(kv);
   if (kv_format == SMLA_KV_FP8_DS)
-    pack_kernel<SMLA_KV_FP8_DS><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        L, R, slot_mapping, n, K, num_slots, scale_mode, kv_scale);
+    pack_kernel<SMLA_KV_FP8_DS, NORM><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        L, R, slot_mapping, n, K, num_slots, scale_mode, kv_scale, nr);
   else if (kv_format == SMLA_KV_FP8_TENSOR)
-    pack_kernel<SMLA_KV_FP8_TENSOR><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        L, R, slot_mapping, n, K, num_slots, scale_mode, kv_scale);
+    pack_kernel<SMLA_KV_FP8_TENSOR, NORM><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        L, R, slot_mapping, n, K, num_slots, scale_mode, kv_scale, nr);
   else
-    pack_kernel<SMLA_KV_BF16><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        L, R, slot_mapping, n, K, num_slots, scale_mode, kv_scale);
+    pack_kernel<SMLA_KV_BF16, NORM><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        L, R, slot_mapping, n, K, num_slots, scale_mode, kv_scale, nr);
   return cudaGetLastError();
+}
+
+cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, float kv_scale, const void* latent,
+                        const void* rope, const int64_t* slot_mapping, int64_t n, void* kv,
+                        int64_t num_slots, cudaStream_t s) {
+  NormRope none;
+  memset(&none, 0, sizeof(none));
+  return launch_pack_impl<false>(kv_format, scale_mode, kv_scale, latent, rope, slot_mapping, n, kv, num_slots,
+                                 none, s);
+}
+
+cudaError_t launch_store_normed(int32_t kv_format, int32_t scale_mode, float kv_scale, const void* latent,
+                                const void* rope, const void* weight, float eps, const int64_t* positions,
+                                const float* cos_sin, int64_t max_position, const int64_t* slot_mapping,
+                                int64_t n, void* kv, int64_t num_slots, int32_t* err, cudaStream_t s) {
+  NormRope nr;
+  nr.weight = static_cast<const uint4*>(weight);
+  nr.eps = eps;
+  nr.positions = positions;
+  nr.cos_sin = cos_sin;
+  nr.max_position = max_position;
+  nr.err = err;
+  return launch_pack_impl<true>(kv_format, scale_mode, kv_scale, latent, rope, slot_mapping, n, kv, num_slots, nr,
+                                s);
 }
 
 // One warp per (token, top-k position). Lane l writes latent dims [16l, 16l+16) and

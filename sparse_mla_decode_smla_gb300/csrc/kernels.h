@@ -58,6 +58,11 @@ cudaError_t launch_pack(int32_t kv_format, int32_t scale_mode, float kv_scale, c
                         const void* rope, const int64_t* slot_mapping, int64_t n, void* kv,
                         int64_t num_slots, cudaStream_t s);
 cudaError_t launch_gather_dequant(const DecodeArgs& a, float* rows, cudaStream_t s);
+// The quantise-on-write store fused with the latent's RMSNorm and the RoPE rotation.
+cudaError_t launch_store_normed(int32_t kv_format, int32_t scale_mode, float kv_scale, const void* latent,
+                                const void* rope, const void* weight, float eps, const int64_t* positions,
+                                const float* cos_sin, int64_t max_position, const int64_t* slot_mapping,
+                                int64_t n, void* kv, int64_t num_slots, int32_t* err, cudaStream_t s);
 
 // ------------------------------------------------------------------------------ indexer
 

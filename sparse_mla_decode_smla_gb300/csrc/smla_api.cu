@@ -332,6 +332,37 @@ smla_status smla_pack_kv_fp8_tensor(const void* latent, const void* rope,
   return SMLA_OK;
 }
 
+smla_status smla_store_kv_normed(const smla_store_desc* d, const void* latent, const void* rope,
+                                 const void* norm_weight, const int64_t* positions, const float* cos_sin,
+                                 const int64_t* slot_mapping, void* kv_cache, int32_t* error_word,
+                                 void* stream) {
+  if (!d) return SMLA_ERR_NULL;
+  if (d->kv_format != SMLA_KV_BF16 && d->kv_format != SMLA_KV_FP8_DS && d->kv_format != SMLA_KV_FP8_TENSOR)
+    return SMLA_ERR_UNSUPPORTED;
+  if (d->kv_format == SMLA_KV_FP8_DS && d->scale_mode != SMLA_SCALE_POW2 && d->scale_mode != SMLA_SCALE_FP32)
+    return SMLA_ERR_UNSUPPORTED;
+  if (d->kv_format == SMLA_KV_FP8_TENSOR && !(isfinite(d->kv_scale) && d->kv_scale > 0.f)) return SMLA_ERR_SHAPE;
+  if (!(isfinite(d->rms_eps) && d->rms_eps >= 0.f)) return SMLA_ERR_SHAPE;
+  if (d->n < 0 || d->num_slots < 0 || d->max_position < 1 || d->n > (int64_t(1) << 36)) return SMLA_ERR_SHAPE;
+  for (int i = 0; i < 2; ++i)
+    if (d->reserved[i] != 0) return SMLA_ERR_SHAPE;
+  if (d->n == 0) return SMLA_OK;
+  if (!latent || !rope || !norm_weight || !positions || !cos_sin || !slot_mapping || !kv_cache) return SMLA_ERR_NULL;
+  if (!aligned(latent, 16) || !aligned(rope, 16) || !aligned(norm_weight, 16) || !aligned(kv_cache, 16) ||
+      !aligned(positions, 8) || !aligned(slot_mapping, 8) || !aligned(cos_sin, 4) ||
+      (error_word && !aligned(error_word, 4)))
+    return SMLA_ERR_ALIGN;
+  int sms = 0;
+  smla_status st = current_device(&sms);
+  if (st != SMLA_OK) return st;
+  if (smla::launch_store_normed(d->kv_format, d->scale_mode, d->kv_format == SMLA_KV_FP8_TENSOR ? d->kv_scale : 1.f,
+                                latent, rope, norm_weight, d->rms_eps, positions, cos_sin, d->max_position,
+                                slot_mapping, d->n, kv_cache, d->num_slots, error_word,
+                                static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
 smla_status smla_gather_dequant(const smla_desc* d, const void* kv_cache,
                                 const int32_t* page_table, const int32_t* topk,
                                 const int32_t* req_id_per_token, float* rows,

@@ -180,3 +180,27 @@ def test_indexer_desc_layout_and_host_checks(L):
     assert L.smla_indexer_logits(ctypes.byref(d), None, P(16), P(16), P(16), P(16), P(16), P(16), None) == 1
     assert L.smla_indexer_logits(ctypes.byref(d), P(8), P(16), P(16), P(16), P(16), P(16), P(16), None) == 3
     assert L.smla_indexer_topk(ctypes.byref(d), P(16), None, P(16), None) == 1
+
+
+def test_store_normed_desc_layout_and_host_checks(L):
+    assert ctypes.sizeof(smla.smla_store_desc) == 48
+    P = ctypes.c_void_p
+
+    def status(**kw):
+        d = smla.smla_store_desc()
+        d.kv_format, d.scale_mode, d.kv_scale, d.rms_eps = smla.SMLA_KV_FP8_DS, 0, 1.0, 1e-6
+        d.n, d.num_slots, d.max_position = 4, 8, 16
+        for k, v in kw.items():
+            setattr(d, k, v)
+        return L.smla_store_kv_normed(ctypes.byref(d), P(16), P(16), P(16), P(16), P(16), P(16), P(16), None, None)
+
+    assert status(kv_format=7) == 4
+    assert status(scale_mode=3) == 4
+    assert status(rms_eps=-1.0) == 2 and status(rms_eps=float("nan")) == 2
+    assert status(max_position=0) == 2
+    assert status(kv_format=smla.SMLA_KV_FP8_TENSOR, kv_scale=0.0) == 2
+    assert status(n=0) == 0  # nothing to do
+    d = smla.smla_store_desc()
+    d.kv_format, d.n, d.num_slots, d.max_position = smla.SMLA_KV_BF16, 4, 8, 16
+    assert L.smla_store_kv_normed(ctypes.byref(d), P(8), P(16), P(16), P(16), P(16), P(16), P(16), None, None) == 3
+    assert L.smla_store_kv_normed(ctypes.byref(d), None, P(16), P(16), P(16), P(16), P(16), P(16), None, None) == 1

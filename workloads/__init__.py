@@ -298,3 +298,36 @@ def make_indexer_inputs(problem: Problem, seed: int | None = None, heads: int = 
         e = torch.randint(-10, -3, (n, P), generator=g, device=dev).to(torch.float32)
         cache[p0:p0 + n, P * INDEX_DIM:] = torch.exp2(e).contiguous().view(torch.uint8).view(n, P * 4)
     return IndexerInputs(q=q, weights=weights, cache=cache, ctx=problem.ctx.to(torch.int32).to(dev), heads=heads)
+
+
+# ------------------------------------------------------------------------------ fused-store inputs
+
+
+@dataclasses.dataclass
+class StoreInputs:
+    """Inputs of the cache write fused with the latent's RMSNorm and the RoPE rotation.
+
+    latent [n, 512] and rope [n, 64] bf16 (N(0, 1) * 3 and N(0, 1)), weight [512] bf16
+    (1 + N(0, 1) / 10), positions [n] int64 uniform in [0, max_position), cos_sin
+    [max_position, 64] fp32: cos, then sin, of position * 10000^(-j / 32) for the 32 pairs
+    (the rotary table a model passes in; drawn here, not computed by the method).
+    """
+
+    latent: torch.Tensor
+    rope: torch.Tensor
+    weight: torch.Tensor
+    positions: torch.Tensor
+    cos_sin: torch.Tensor
+
+
+def make_store_inputs(n: int, seed: int, max_position: int = 4096, device="cpu") -> StoreInputs:
+    g = _gen(seed, 60, "cpu")
+    latent = (torch.randn((n, LATENT_DIM), generator=g) * 3.0).to(torch.bfloat16)
+    rope = torch.randn((n, ROPE_DIM), generator=g).to(torch.bfloat16)
+    weight = (1.0 + torch.randn((LATENT_DIM,), generator=g) / 10.0).to(torch.bfloat16)
+    positions = torch.randint(0, max_position, (n,), generator=g, dtype=torch.int64)
+    theta = torch.pow(10000.0, -torch.arange(ROPE_DIM // 2, dtype=torch.float64) / (ROPE_DIM // 2))
+    ang = torch.arange(max_position, dtype=torch.float64)[:, None] * theta[None, :]
+    cos_sin = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)
+    d = torch.device(device)
+    return StoreInputs(latent.to(d), rope.to(d), weight.to(d), positions.to(d), cos_sin.to(d))
