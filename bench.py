@@ -60,14 +60,16 @@ def measured_peaks() -> dict:
 # of that kernel's sources at capture time. A capture of an older kernel (the hash differs) is
 # not reported.
 TRAFFIC = {
-    ("fp8_mtp_T256_H128_K2048_ctx4k-128k_sink", "decode_hg_kernel"): (430947840, "9868bc305a1fc3ae"),
-    ("fp8_T128_H128_K2048_ctx64k_sink", "decode_hg_kernel"): (230827264, "9868bc305a1fc3ae"),
-    ("fp8_T32_H64_K2048_ctx1k-32k", "decode_hg_kernel"): (51818240, "9868bc305a1fc3ae"),
-    ("fp8_T256_H16_K2048_ctx8k-128k_pad20", "decode_mma_kernel"): (334121472, "4071888d224255ba"),
+    ("fp8_mtp_T256_H128_K2048_ctx4k-128k_sink", "decode_hg_kernel"): (430947840, "c40b4989cdfa8e20"),
+    ("fp8_T128_H128_K2048_ctx64k_sink", "decode_hg_kernel"): (230827264, "c40b4989cdfa8e20"),
+    ("fp8_T32_H64_K2048_ctx1k-32k", "decode_hg_kernel"): (51818240, "c40b4989cdfa8e20"),
+    ("fp8_T256_H16_K2048_ctx8k-128k_pad20", "decode_mma_kernel"): (334121472, "0896484c860414c8"),
+    ("store_fp8_ds_rows65536_P64_pos131072", "pack_kernel"): (111947008, "4dfd7199c86d8388"),
 }
 KERNEL_SOURCES = {
     "decode_hg_kernel": ("common.cuh", "kernels.h", "tcgen05.cuh", "decode_hg.cu", "tensor_maps.cu"),
     "decode_mma_kernel": ("common.cuh", "kernels.h", "decode_mma.cu"),
+    "pack_kernel": ("common.cuh", "kernels.h", "cache_kernels.cu"),
 }
 
 
@@ -542,6 +544,91 @@ def indexer_arm(args):
     return 0
 
 
+# ------------------------------------------------------------------------------ fused-store arm
+
+
+def store_work(n: int, row_bytes: int) -> dict:
+    """Algorithmic bytes of one fused store of n rows: the bf16 latent and RoPE (1152 B), the
+    position and slot (16 B) and the row's cos/sin (256 B) read, the packed row written."""
+    per_row = 2 * 576 + 16 + 64 * 4 + row_bytes
+    return {"bytes_per_row": per_row, "bytes": n * per_row + 1024, "rows": n}
+
+
+def store_arm(args):
+    """smla_store_kv_normed (RMSNorm + RoPE + quantise on write) over one prefill chunk of rows."""
+    import numpy as np
+    import sparse_mla_decode_smla_gb300 as smla
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n, P, max_pos = args.store_rows, 64, 131072
+    fmt = {"fp8_ds": (smla.SMLA_KV_FP8_DS, 656), "fp8_tensor": (smla.SMLA_KV_FP8_TENSOR, 576),
+           "bf16": (smla.SMLA_KV_BF16, 1152)}[args.store_format]
+    x = W.make_store_inputs(n, 7, max_position=max_pos, device=dev)
+    x.positions = torch.arange(n, dtype=torch.int64, device=dev)  # a chunk's consecutive positions
+    pages = -(-n // P)
+    perm = torch.randperm(pages, generator=torch.Generator().manual_seed(8)).to(dev)
+    slots = perm.repeat_interleave(P)[:n] * P + torch.arange(n, device=dev) % P
+    kv = torch.zeros((pages * P, fmt[1]), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kv_scale = 2.0 ** -4
+
+    def step():
+        smla.store_kv_normed(fmt[0], x.latent, x.rope, x.weight, 1e-6, x.positions, x.cos_sin, slots, kv,
+                             pages * P, kv_scale=kv_scale, error_word=err)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    assert err.item() == 0, f"store error word {err.item()}"
+    peaks = measured_peaks()
+    work = store_work(n, fmt[1])
+    ach = work["bytes"] / (ms * 1e-3) / 1e9
+    rl = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+          "frac": ach / peaks["hbm_gbs"], "kernel": "pack_kernel (normed)", "kernel_ms": ms,
+          "traffic": recorded_traffic(f"store_{args.store_format}_rows{n}_P{P}_pos{max_pos}", "pack_kernel"),
+          "peak_source": peaks["source"] + " hbm_gbs (burst)"}
+    line = {"metric": "fused cache-store rows/s", "value": n / (ms * 1e-3), "unit": "rows/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"store_{args.store_format}_rows{n}_P{P}_pos{max_pos}", "op": "store",
+                       "rows": n, "kv_format": args.store_format, "row_bytes": fmt[1],
+                       "positions": "consecutive from 0", "slots": "shuffled pages of 64",
+                       "l2": "flushed between timed steps (512 MiB write, outside the events)"},
+            "roofline": rl, "algorithmic": work, "gpu_launches": args.steps, "clocks": clk.summary()}
+    if args.cpu_baseline_seconds > 0:
+        import oracle as O
+        host = {k: getattr(x, k).cpu() for k in ("latent", "rope", "weight", "positions", "cos_sin")}
+        bits = {k: host[k].view(torch.int16).numpy().view(np.uint16) for k in ("latent", "rope", "weight")}
+        cs = host["cos_sin"].double().numpy()
+        done, el, chunk = 0, 0.0, 1024
+        while el < args.cpu_baseline_seconds and done < n:
+            lo, hi = done, min(n, done + chunk)
+            c = cs[host["positions"][lo:hi].numpy()]
+            t0 = time.perf_counter()
+            O.store_normed_rows(bits["latent"][lo:hi], bits["rope"][lo:hi], bits["weight"], 1e-6, c[:, :32],
+                                c[:, 32:], args.store_format, O.SCALE_POW2, kv_scale)
+            el += time.perf_counter() - t0
+            done = hi
+        line["cpu_baseline"] = {"value": done / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{done} of {n} rows, fused-store oracle, numpy float64, 1 BLAS thread, "
+                                          f"{el:.1f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -550,8 +637,11 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=[w.name for w in W.WORKLOADS + W.EXTRA_WORKLOADS])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--op", default="decode", choices=["decode", "indexer"],
-                    help="decode (the hot path, default) or the indexer that produces its top-k indices")
+    ap.add_argument("--op", default="decode", choices=["decode", "indexer", "store"],
+                    help="decode (the hot path, default), the indexer that produces its top-k indices, "
+                         "or the fused cache store (RMSNorm + RoPE + quantise on write)")
+    ap.add_argument("--store-rows", type=int, default=65536, help="--op store: rows per call")
+    ap.add_argument("--store-format", default="fp8_ds", choices=["fp8_ds", "fp8_tensor", "bf16"])
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     ap.add_argument("--ref-budget-seconds", type=float, default=60.0,
@@ -567,6 +657,8 @@ def main(argv=None):
         return reference_arm(args)
     if args.op == "indexer":
         return indexer_arm(args)
+    if args.op == "store":
+        return store_arm(args)
     return gpu_arm(args)
 
 

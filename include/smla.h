@@ -212,7 +212,7 @@ smla_status smla_pack_kv_fp8_tensor(const void* latent, const void* rope,
  * and stores (latent', rope') exactly as smla_pack_kv (kv_format BF16 or FP8_DS with
  * scale_mode) or smla_pack_kv_fp8_tensor (kv_format FP8_TENSOR with kv_scale) would.
  *   latent [n, 512] and rope [n, 64] bf16, norm_weight [512] bf16: 16-byte aligned.
- *   positions [n] int64; cos_sin [max_position, 64] fp32; slot_mapping [n] int64.
+ *   positions [n] int64; cos_sin [max_position, 64] fp32, 16-byte aligned; slot_mapping [n] int64.
  *   error_word: device int32 or NULL; a row whose position is outside [0, max_position) is not
  *   written and sets SMLA_DEVERR_INDEX.
  */

@@ -27,12 +27,40 @@ struct NormRope {
 
 __device__ __forceinline__ uint32_t bf16x2_pack_rn(float lo, float hi) { return pack_bf16x2(lo, hi); }
 
+// x / scale for the E4M3 conversion. Where scale is a power of two in [2^-126, 2^126] its
+// reciprocal is exact, so x * (1 / scale) is the same real number x / scale rounded once: the
+// same fp32 value as the correctly rounded division, for every x. Otherwise divide.
+struct ScaleDiv {
+  float scale, inv;
+  bool exact;
+  __device__ __forceinline__ explicit ScaleDiv(float sc) : scale(sc) {
+    const uint32_t b = __float_as_uint(sc);
+    exact = (b & 0x007fffffu) == 0u && sc >= 0x1p-126f && sc <= 0x1p126f;
+    inv = exact ? __frcp_rn(sc) : 0.f;
+  }
+  // E4M3 codes of x[0..2n) / scale, two per 16-bit word: one branch for the whole run
+  template <int N>
+  __device__ __forceinline__ void codes(const float* x, uint16_t* out) const {
+    if (exact) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) out[i] = f32x2_to_e4m3x2(__fmul_rn(x[2 * i], inv), __fmul_rn(x[2 * i + 1], inv));
+    } else {
+#pragma unroll
+      for (int i = 0; i < N; ++i)
+        out[i] = f32x2_to_e4m3x2(__fdiv_rn(x[2 * i], scale), __fdiv_rn(x[2 * i + 1], scale));
+    }
+  }
+};
+
 // One warp per row. Lane l owns latent elements [16l, 16l+16); lanes 8b..8b+7 form block b.
 // With NORM the row is first normalised (RMSNorm over the 512 latent dims: fp32 sum of
 // squares in a fixed order, correctly rounded sqrt and divide, x * r * w rounded to bf16) and
 // its RoPE pairs (2j, 2j+1) are rotated, (a c - b s, a s + b c) rounded to bf16.
+// The kernel waits on one memory round trip per row, so its speed follows the rows in flight:
+// the FP8 variants are held to 40 registers for six blocks per SM (measured faster than five,
+// despite a few spilled words); the bf16 one at five blocks, 48 registers.
 template <int FMT, bool NORM>
-__global__ void __launch_bounds__(256) pack_kernel(const uint4* __restrict__ latent,
+__global__ void __launch_bounds__(256, FMT == SMLA_KV_BF16 ? 5 : 6) pack_kernel(const uint4* __restrict__ latent,
                                                    const uint4* __restrict__ rope,
                                                    const int64_t* __restrict__ slot_mapping,
                                                    int64_t n, uint8_t* __restrict__ kv,
@@ -41,16 +69,26 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint4* __restrict__ lat
   const int lane = threadIdx.x & 31;
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (row >= n) return;
+  // every load of the row is issued before the first one is used (all lie inside the row's
+  // own inputs), so the warp waits for one memory round trip, not one per dependent load
   const int64_t slot = slot_mapping[row];
-  if (slot < 0 || slot >= num_slots) return;
   uint4 x0 = latent[row * 64 + 2 * lane];
   uint4 x1 = latent[row * 64 + 2 * lane + 1];
   uint4 rp = lane < 8 ? rope[row * 8 + lane] : make_uint4(0, 0, 0, 0);  // RoPE dims [8 lane, +8)
+  int64_t pos = 0;
+  if constexpr (NORM) pos = nr.positions[row];
+  if (slot < 0 || slot >= num_slots) return;
   if constexpr (NORM) {
-    const int64_t pos = nr.positions[row];
     if (pos < 0 || pos >= nr.max_position) {  // the whole warp agrees: skip the row, flag it
       if (lane == 0 && nr.err) atomicOr(nr.err, SMLA_DEVERR_INDEX);
       return;
+    }
+    const uint4 g0 = nr.weight[2 * lane], g1 = nr.weight[2 * lane + 1];
+    float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f), s4 = c4;
+    if (lane < 8) {  // cos and sin of the RoPE pairs 4 lane .. 4 lane + 3
+      const float4* cs = reinterpret_cast<const float4*>(nr.cos_sin + pos * 64);
+      c4 = cs[lane];
+      s4 = cs[8 + lane];
     }
     uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
     float ss = 0.f;
@@ -58,8 +96,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint4* __restrict__ lat
     for (int i = 0; i < 8; ++i) ss = fmaf(bf16_hi(w[i]), bf16_hi(w[i]), fmaf(bf16_lo(w[i]), bf16_lo(w[i]), ss));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, float(kLatent)), nr.eps)));
-    const uint4 g0 = nr.weight[2 * lane], g1 = nr.weight[2 * lane + 1];
+    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.f / kLatent), nr.eps)));  // 1/512: exact
     const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -68,11 +105,11 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint4* __restrict__ lat
     x0 = make_uint4(w[0], w[1], w[2], w[3]);
     x1 = make_uint4(w[4], w[5], w[6], w[7]);
     if (lane < 8) {  // pairs j = 4 lane .. 4 lane + 3, one per bf16 word
-      const float* cs = nr.cos_sin + pos * 64;
+      const float cv[4] = {c4.x, c4.y, c4.z, c4.w}, sv[4] = {s4.x, s4.y, s4.z, s4.w};
       uint32_t rw[4] = {rp.x, rp.y, rp.z, rp.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float c = cs[4 * lane + k], sn = cs[32 + 4 * lane + k];
+        const float c = cv[k], sn = sv[k];
         const float a = bf16_lo(rw[k]), b = bf16_hi(rw[k]);
         rw[k] = bf16x2_pack_rn(__fsub_rn(__fmul_rn(a, c), __fmul_rn(b, sn)), __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, c)));
       }
@@ -88,27 +125,31 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint4* __restrict__ lat
   }
   if (FMT == SMLA_KV_FP8_TENSOR) {
     uint8_t* dst = kv + slot * kFp8TensorRowBytes;
+    const ScaleDiv dv(kv_scale);
     const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-    uint32_t codes[4];
+    float v[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[2 * i]), kv_scale), __fdiv_rn(bf16_hi(w[2 * i]), kv_scale));
-      const uint16_t hi =
-          f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[2 * i + 1]), kv_scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), kv_scale));
-      codes[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = bf16_lo(w[i]);
+      v[2 * i + 1] = bf16_hi(w[i]);
     }
-    *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+    uint16_t c[8];
+    dv.codes<8>(v, c);
+    *reinterpret_cast<uint4*>(dst + 16 * lane) =
+        make_uint4(c[0] | (uint32_t(c[1]) << 16), c[2] | (uint32_t(c[3]) << 16), c[4] | (uint32_t(c[5]) << 16),
+                   c[6] | (uint32_t(c[7]) << 16));
     if (lane < 8) {  // RoPE values [8 lane, 8 lane + 8)
       const uint32_t rw[4] = {rp.x, rp.y, rp.z, rp.w};
-      uint32_t rc[2];
+      float r[8];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(rw[2 * i]), kv_scale), __fdiv_rn(bf16_hi(rw[2 * i]), kv_scale));
-        const uint16_t hi =
-            f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(rw[2 * i + 1]), kv_scale), __fdiv_rn(bf16_hi(rw[2 * i + 1]), kv_scale));
-        rc[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      for (int i = 0; i < 4; ++i) {
+        r[2 * i] = bf16_lo(rw[i]);
+        r[2 * i + 1] = bf16_hi(rw[i]);
       }
-      *reinterpret_cast<uint2*>(dst + kLatent + 8 * lane) = make_uint2(rc[0], rc[1]);
+      uint16_t rc[4];
+      dv.codes<4>(r, rc);
+      *reinterpret_cast<uint2*>(dst + kLatent + 8 * lane) =
+          make_uint2(rc[0] | (uint32_t(rc[1]) << 16), rc[2] | (uint32_t(rc[3]) << 16));
     }
     return;
   }
@@ -136,16 +177,12 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint4* __restrict__ lat
       scale = ratio;
     }
   }
-  uint32_t codes[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(v[4 * i], scale), __fdiv_rn(v[4 * i + 1], scale));
-    const uint16_t hi =
-        f32x2_to_e4m3x2(__fdiv_rn(v[4 * i + 2], scale), __fdiv_rn(v[4 * i + 3], scale));
-    codes[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-  }
+  uint16_t c[8];
+  ScaleDiv(scale).codes<8>(v, c);
   uint8_t* dst = kv + slot * kFp8RowBytes;
-  *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+  *reinterpret_cast<uint4*>(dst + 16 * lane) =
+      make_uint4(c[0] | (uint32_t(c[1]) << 16), c[2] | (uint32_t(c[3]) << 16), c[4] | (uint32_t(c[5]) << 16),
+                 c[6] | (uint32_t(c[7]) << 16));
   const float s1 = __shfl_sync(0xffffffffu, scale, 8);
   const float s2 = __shfl_sync(0xffffffffu, scale, 16);
   const float s3 = __shfl_sync(0xffffffffu, scale, 24);

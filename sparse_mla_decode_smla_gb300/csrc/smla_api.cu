@@ -349,7 +349,7 @@ smla_status smla_store_kv_normed(const smla_store_desc* d, const void* latent, c
   if (d->n == 0) return SMLA_OK;
   if (!latent || !rope || !norm_weight || !positions || !cos_sin || !slot_mapping || !kv_cache) return SMLA_ERR_NULL;
   if (!aligned(latent, 16) || !aligned(rope, 16) || !aligned(norm_weight, 16) || !aligned(kv_cache, 16) ||
-      !aligned(positions, 8) || !aligned(slot_mapping, 8) || !aligned(cos_sin, 4) ||
+      !aligned(positions, 8) || !aligned(slot_mapping, 8) || !aligned(cos_sin, 16) ||
       (error_word && !aligned(error_word, 4)))
     return SMLA_ERR_ALIGN;
   int sms = 0;

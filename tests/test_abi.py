@@ -203,4 +203,5 @@ def test_store_normed_desc_layout_and_host_checks(L):
     d = smla.smla_store_desc()
     d.kv_format, d.n, d.num_slots, d.max_position = smla.SMLA_KV_BF16, 4, 8, 16
     assert L.smla_store_kv_normed(ctypes.byref(d), P(8), P(16), P(16), P(16), P(16), P(16), P(16), None, None) == 3
+    assert L.smla_store_kv_normed(ctypes.byref(d), P(16), P(16), P(16), P(16), P(4), P(16), P(16), None, None) == 3
     assert L.smla_store_kv_normed(ctypes.byref(d), None, P(16), P(16), P(16), P(16), P(16), P(16), None, None) == 1

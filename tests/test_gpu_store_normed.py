@@ -70,13 +70,14 @@ def test_bit_exact_where_fp32_is_exact(fmt):
     assert np.array_equal(got[slots.numpy()], ref)
 
 
-@pytest.mark.parametrize("fmt,mode", [("bf16", 0), ("fp8_ds", smla.SMLA_SCALE_POW2), ("fp8_ds", smla.SMLA_SCALE_FP32),
-                                      ("fp8_tensor", 0)])
-def test_general_inputs_within_one_bf16_step(fmt, mode):
+# a power-of-two scale takes the kernel's exact reciprocal, any other one its division
+@pytest.mark.parametrize("fmt,mode,kv_scale", [("bf16", 0, 1.0), ("fp8_ds", smla.SMLA_SCALE_POW2, 1.0),
+                                               ("fp8_ds", smla.SMLA_SCALE_FP32, 1.0), ("fp8_tensor", 0, 2.0 ** -4),
+                                               ("fp8_tensor", 0, 0.0371)])
+def test_general_inputs_within_one_bf16_step(fmt, mode, kv_scale):
     n = 3000
     x = W.make_store_inputs(n, 11)
     slots = torch.randperm(4000)[:n].to(torch.int64)
-    kv_scale = 2.0 ** -4
     got = _store(fmt, x, 1e-6, slots, 4000, scale_mode=mode, kv_scale=kv_scale)[slots.numpy()]
     # the oracle's normed, rotated bf16 values
     cs = x.cos_sin.double().numpy()[x.positions.numpy()]
