@@ -273,14 +273,28 @@ def attend(q: np.ndarray, keys: np.ndarray, sm_scale: float, sink: np.ndarray | 
     return out, lse, lse0
 
 
+def q_values(q, q_format: str = "bf16", q_scale: float | None = None) -> np.ndarray:
+    """q of one token as float64 values: bf16 bit patterns, or E4M3 codes times the per-tensor
+    q_scale (the FP8-Q path of vLLM PR #43827, "关键源码片段": bmm1_scale = scale * q_scale *
+    kv_scale; the product of a 4-bit significand and an fp32 scale is exact in float64)."""
+    if q_format == "bf16":
+        return bf16_bits_to_f64(q)
+    if q_format == "e4m3":
+        if q_scale is None:
+            raise ValueError("E4M3 q needs q_scale")
+        return e4m3_decode(q) * float(np.float32(q_scale))
+    raise ValueError(q_format)
+
+
 def decode(q_bits: np.ndarray, fetch_rows: Callable[[np.ndarray], np.ndarray], kv_format: str,
            page_table: np.ndarray, topk: np.ndarray, page_size: int, num_pages: int,
            sm_scale: float, sink=None, next_n: int = 1, req_id_per_token=None, tokens=None,
-           kv_scale: float | None = None):
+           kv_scale: float | None = None, q_format: str = "bf16", q_scale: float | None = None):
     """Sparse MLA decode of the listed tokens (all by default), float64.
 
-    q_bits [T, H, 576] bf16 bit patterns; fetch_rows(phys_slots) -> [n, R] uint8
-    cache rows; page_table [B, stride]; topk [T, K] request-local indices.
+    q_bits [T, H, 576] bf16 bit patterns (q_format "bf16") or E4M3 codes (q_format "e4m3",
+    values code * q_scale); fetch_rows(phys_slots) -> [n, R] uint8 cache rows; page_table
+    [B, stride]; topk [T, K] request-local indices.
     Returns dict(out [t,H,512], lse [t,H], lse_nosink [t,H], n_invalid [t]).
     """
     q_bits = np.asarray(q_bits)
@@ -292,7 +306,7 @@ def decode(q_bits: np.ndarray, fetch_rows: Callable[[np.ndarray], np.ndarray], k
         _, phys, n_invalid = physical_slots(topk[t], page_table[r], page_size, num_pages)
         rows = fetch_rows(phys) if len(phys) else np.zeros((0, 1), dtype=np.uint8)
         keys = dequant_rows(rows, kv_format, kv_scale) if len(phys) else np.zeros((0, DIM))
-        o, l, l0 = attend(bf16_bits_to_f64(q_bits[t]), keys, sm_scale, sink)
+        o, l, l0 = attend(q_values(q_bits[t], q_format, q_scale), keys, sm_scale, sink)
         outs.append(o)
         lses.append(l)
         lse0s.append(l0)

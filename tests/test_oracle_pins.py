@@ -493,3 +493,55 @@ def test_store_normed_rows_is_norm_rope_then_the_packer():
     rows = O.store_normed_rows(_bits(lat), _bits(rope), _bits(w), 0.0, cos, sin, "fp8_ds")
     normed = O.rms_norm_bf16(_bits(lat), _bits(w), 0.0)
     assert np.array_equal(rows, O.pack_fp8_ds(O.f64_to_bf16_bits(normed), _bits(rope)))
+
+
+# ----------------------------------------------------------------------------- FP8 q
+
+def test_q_values_e4m3_matches_torch_decode_times_scale():
+    codes = np.arange(256, dtype=np.uint8)
+    finite = ~np.isin(codes, [0x7F, 0xFF])
+    for qs in (1.0, 2.0 ** -3, 0.37):
+        got = O.q_values(codes[finite], "e4m3", qs)
+        ref = torch.from_numpy(codes[finite]).view(torch.float8_e4m3fn).to(torch.float64) * float(np.float32(qs))
+        assert np.array_equal(got, ref.numpy())
+    with pytest.raises(ValueError):
+        O.q_values(codes, "e4m3", None)
+
+
+@pytest.mark.parametrize("sink", [False, True])
+def test_decode_fp8_q_equals_dense_sdpa(sink):
+    # E4M3 q (torch's cast) against the per-tensor FP8 cache: the full context as top-k equals
+    # dense float64 SDPA on q and keys decoded by torch
+    P, n_pages, H = 64, 3, 4
+    rows, q, pt, sig = _problem(n_pages, P, H, "fp8_tensor", seed=13, sink=sink)
+    qs = 2.0 ** -2
+    q8 = (q.float() / qs).to(torch.float8_e4m3fn)
+    ctx = n_pages * P
+    perm = np.random.default_rng(3).permutation(ctx).astype(np.int32)
+    sm = 1.0 / 24
+    res = O.decode(q8.view(torch.uint8).numpy(), lambda s: rows[s], "fp8_tensor", pt, perm[None, :], P, n_pages,
+                   sm, sink=sig, kv_scale=TENSOR_SCALE, q_format="e4m3", q_scale=qs)
+    logical_rows = np.concatenate([rows[p * P:(p + 1) * P] for p in pt[0]])
+    keys = _torch_tensor_keys(logical_rows, TENSOR_SCALE)
+    qf = q8[0].to(torch.float64) * qs
+    scores = sm * (qf @ keys.T)
+    if sig is not None:
+        scores = torch.cat([scores, torch.from_numpy(sig)[:, None]], 1)
+    w = torch.softmax(scores, 1)[:, :ctx]
+    np.testing.assert_allclose(res["out"][0], (w @ keys[:, :512]).numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(res["lse"][0], torch.logsumexp(scores, 1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_decode_fp8_q_scale_folds_into_the_scores():
+    # bmm1_scale = sm_scale * q_scale * kv_scale: scaling q by q_scale is scaling sm_scale by it
+    P, n_pages, H = 64, 2, 3
+    rows, q, pt, _ = _problem(n_pages, P, H, "fp8_tensor", seed=17)
+    q8 = q.float().to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    idx = np.random.default_rng(4).permutation(n_pages * P)[:100].astype(np.int32)[None, :]
+    qs = float(np.float32(0.37))
+    a = O.decode(q8, lambda s: rows[s], "fp8_tensor", pt, idx, P, n_pages, 0.05, kv_scale=TENSOR_SCALE,
+                 q_format="e4m3", q_scale=qs)
+    b = O.decode(q8, lambda s: rows[s], "fp8_tensor", pt, idx, P, n_pages, 0.05 * qs, kv_scale=TENSOR_SCALE,
+                 q_format="e4m3", q_scale=1.0)
+    np.testing.assert_allclose(a["out"], b["out"], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(a["lse"], b["lse"], rtol=0, atol=1e-12)
