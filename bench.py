@@ -108,6 +108,8 @@ def workload_config(problem, valid: int, num_splits: int, world: int) -> dict:
 
 
 def roofline(valid_bytes, flops, seconds, peaks) -> dict:
+    """The bound of whichever side takes longer at its peak; peaks["tensor"] names the tensor
+    peak used (the measured bf16 one unless an 8-bit path scales it)."""
     t_hbm = valid_bytes / (peaks["hbm_gbs"] * 1e9)
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
     if t_hbm >= t_tc:
@@ -118,7 +120,7 @@ def roofline(valid_bytes, flops, seconds, peaks) -> dict:
     achieved = flops / seconds / 1e12
     return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": achieved / peaks["bf16_tflops"], "traffic": None,
-            "peak_source": peaks["source"] + " bf16_tflops (burst)"}
+            "peak_source": peaks["source"] + " " + peaks.get("tensor", "bf16_tflops (burst)")}
 
 
 class ClockSampler:
@@ -208,7 +210,7 @@ def barrier(world: int):
 
 
 def run_oracle_sample(problem, budget_s: float, wall_limit_s: float | None = None,
-                      max_tokens: int | None = None):
+                      max_tokens: int | None = None, q_e4m3=None, q_scale=None):
     """Time the float64 oracle's decode, as it stands, on whole query tokens.
 
     The oracle's cache rows for a few requests at a time are packed first, outside the
@@ -229,7 +231,7 @@ def run_oracle_sample(problem, budget_s: float, wall_limit_s: float | None = Non
         cache = OracleCache(problem, [t // w.next_n for t in batch])
         for t in batch:
             t0 = time.perf_counter()
-            oracle_decode(problem, tokens=[t], cache=cache)
+            oracle_decode(problem, tokens=[t], cache=cache, q_e4m3=q_e4m3, q_scale=q_scale)
             el += time.perf_counter() - t0
             done += 1
             if (el >= budget_s or time.perf_counter() - wall0 >= wall_limit
@@ -295,6 +297,14 @@ def gpu_arm(args):
     w = workload_from_args(args)
     problem = W.make_problem(w, seed=W.SEED_BASE + w.seed_offset + 1000 * rank, device=dev)
     dd = DeviceDecode(problem, num_splits=args.num_splits, device=dev)
+    q8 = None
+    if args.q_fp8:  # E4M3 q with a per-tensor scale: the FP8-operand kernel
+        if w.kv_format != "fp8_tensor" or w.num_heads < 64:
+            raise SystemExit("--q-fp8 needs a per-tensor FP8 workload with 64 or more heads")
+        q8 = W.q_to_e4m3(problem.q).to(dev).contiguous()
+        dd.q = q8
+        dd.desc.q_format, dd.desc.q_scale = smla.SMLA_Q_FP8_E4M3, W.Q_SCALE_FP8
+        dd.kernel_name = "decode_hg_f8_kernel"
     valid, kv_bytes, flops = algorithmic_work(problem)
     launches_per_step = 2 if dd.workspace.numel() * 4 > 256 else 1
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -395,6 +405,11 @@ def gpu_arm(args):
             torch.distributed.destroy_process_group()
         return 0
     peaks = measured_peaks()
+    if args.q_fp8:  # E4M3 operands: the measured bf16 peak times the nominal fp8 / bf16 ratio of 2
+        peaks = dict(peaks, bf16_tflops=2 * peaks["bf16_tflops"],
+                     bf16_tflops_sustained=(2 * peaks["bf16_tflops_sustained"]
+                                            if peaks.get("bf16_tflops_sustained") else None),
+                     tensor="bf16_tflops (burst) x 2 (fp8)")
     rl = roofline(kv_bytes, flops, kernel_ms * 1e-3, peaks)
     rl["kernel"] = dd.kernel_name
     rl["kernel_ms"] = kernel_ms
@@ -403,9 +418,10 @@ def gpu_arm(args):
     line = {
         "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "data": "synthetic",
-        "config": workload_config(problem, valid, args.num_splits, world),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if args.q_fp8 else "f16", "data": "synthetic",
+        "config": dict(workload_config(problem, valid, args.num_splits, world),
+                       **({"q": "e4m3", "q_scale": W.Q_SCALE_FP8} if args.q_fp8 else {})),
         "roofline": rl,
         "roofline_step_frac": step_rl["frac"],
         "roofline_sustained_frac": (rl["achieved"] / peaks["bf16_tflops_sustained"]
@@ -420,7 +436,8 @@ def gpu_arm(args):
     }
     if args.cpu_baseline_seconds > 0 and world == 1:
         cpu_problem = problem
-        n, el = run_oracle_sample(cpu_problem, budget_s=args.cpu_baseline_seconds)
+        n, el = run_oracle_sample(cpu_problem, budget_s=args.cpu_baseline_seconds,
+                                  q_e4m3=None if q8 is None else q8.cpu(), q_scale=W.Q_SCALE_FP8)
         line["cpu_baseline"] = {"value": n / el, "unit": "query-tokens/s", "cores": 1, "kind": "oracle",
                                 "sample": f"{n} of {w.num_tokens} query tokens of {w.name}, oracle "
                                           f"decode time {el:.1f} s (cache rows packed beforehand, "
@@ -643,6 +660,8 @@ def main(argv=None):
     ap.add_argument("--store-rows", type=int, default=65536, help="--op store: rows per call")
     ap.add_argument("--store-format", default="fp8_ds", choices=["fp8_ds", "fp8_tensor", "bf16"])
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--q-fp8", action="store_true",
+                    help="E4M3 q against a per-tensor FP8 workload (the FP8-operand tensor-core kernel)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     ap.add_argument("--ref-budget-seconds", type=float, default=60.0,
                     help="reference arm: oracle decode time of all timed steps together")

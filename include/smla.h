@@ -53,9 +53,19 @@ enum {
   /* per-tensor FP8: 576 E4M3FN codes per slot, [latent 512 | RoPE 64] = 576 bytes, all
    * dequantised with the one fp32 scale smla_desc.kv_scale (the contiguous per-tensor FP8
    * cache of vLLM PR #43827 "实现拆解 4" / "关键源码片段": keys and values both carry
-   * kv_scale, bmm1_scale = scale * q_scale * kv_scale, bmm2_scale = kv_scale; q stays
-   * bf16, so q_scale = 1). */
+   * kv_scale, bmm1_scale = scale * q_scale * kv_scale, bmm2_scale = kv_scale; with
+   * bf16 q, q_scale = 1; FP8 q: SMLA_Q_FP8_E4M3). */
   SMLA_KV_FP8_TENSOR = 2
+};
+
+/* Element type of q (smla_desc.q_format). */
+enum {
+  SMLA_Q_BF16 = 0,     /* [T, H, 576] bf16 */
+  /* [T, H, 576] E4M3FN codes with one per-tensor scale smla_desc.q_scale: q = code * q_scale
+   * (the FP8-Q path of vLLM PR #43827 "关键源码片段": bmm1_scale = scale * q_scale *
+   * kv_scale, bmm2_scale = kv_scale). Served with SMLA_KV_FP8_TENSOR and 64 or more heads by
+   * the FP8 tensor-core kernel, whose probabilities enter PV as E4M3 (see smla_decode). */
+  SMLA_Q_FP8_E4M3 = 1
 };
 
 /* Block-scale rule of smla_pack_kv (amax = max |x| over the 128-dim block). */
@@ -91,7 +101,10 @@ typedef struct smla_desc {
                                 into n contiguous parts merged by log-sum-exp */
   float kv_scale;            /* SMLA_KV_FP8_TENSOR: the cache's per-tensor scale (finite,
                                 > 0); ignored by the other formats */
-  int32_t reserved[3];       /* must be zero */
+  int32_t q_format;          /* SMLA_Q_* (0: bf16) */
+  float q_scale;             /* SMLA_Q_FP8_E4M3: q's per-tensor scale (finite, > 0);
+                                ignored for bf16 q */
+  int32_t reserved[1];       /* must be zero */
 } smla_desc;
 
 /* Human-readable name of a status (static string). */
@@ -99,7 +112,8 @@ const char* smla_status_string(int32_t status);
 
 /* ABI version of this header (increments on any incompatible change; 2 added kv_scale,
  * 3 added SMLA_ERR_TIMEOUT, SMLA_ERR_OPERAND_RANGE, SMLA_DEVERR_RANGE,
- * smla_noalloc_read_error, the indexer calls and smla_store_kv_normed). */
+ * smla_noalloc_read_error, the indexer calls and smla_store_kv_normed; 4 added q_format and
+ * q_scale in place of two reserved words). */
 int32_t smla_abi_version(void);
 
 /*
@@ -114,8 +128,8 @@ smla_status smla_workspace_size(const smla_desc* d, size_t* bytes);
 
 /*
  * Sparse MLA decode (the hot path).
- *   q          [T, H, 576] bf16, 16-byte aligned; dims 0..511 pair with the latent,
- *              512..575 with the RoPE part.
+ *   q          [T, H, 576] bf16 (or E4M3 codes, q_format SMLA_Q_FP8_E4M3), 16-byte
+ *              aligned; dims 0..511 pair with the latent, 512..575 with the RoPE part.
  *   kv_cache   [num_pages, P, R] bytes, R = 656 (FP8_DS), 576 (FP8_TENSOR) or 1152 (BF16),
  *              16-byte aligned. num_pages * P must stay below 2^31 - 1 (SMLA_ERR_SHAPE
  *              otherwise): rows are gathered by 32-bit row coordinates.
@@ -151,6 +165,15 @@ smla_status smla_workspace_size(const smla_desc* d, size_t* bytes);
  * magnitude (larger ones make the outputs of their heads non-finite; nothing flags them),
  * and values below 2^-17 keep 2^-25 in absolute error. Fewer than 64 heads,
  * SMLA_KV_FP8_TENSOR and SMLA_KV_BF16 apply scales in fp32 and have neither limit.
+ *
+ * FP8 q (q_format SMLA_Q_FP8_E4M3; only with SMLA_KV_FP8_TENSOR and 64 or more heads, else
+ * SMLA_ERR_UNSUPPORTED): the codes of q and of the cache are the MMA operands (E4M3, fp32
+ * accumulation); the scores take sm_scale * q_scale * kv_scale in fp32. The probabilities
+ * enter PV as E4M3 values 2^(s - m + 7) (m within 1 of the running maximum), each within 2^-4
+ * relative of its exact value (values below 2^-16 of the maximum weight are dropped), and the
+ * output is normalised by the sum of those E4M3 values: every output is a convex combination
+ * of the selected values times kv_scale, within 2^-3 * max |v_j| * kv_scale of the exact one.
+ * The LSE uses the weights before rounding.
  */
 smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
                         const int32_t* page_table, const int32_t* topk,

@@ -44,15 +44,19 @@ class OracleCache:
         return self.rows[loc * self.P + phys % self.P]
 
 
-def oracle_decode(problem, tokens=None, scale_mode: int = O.SCALE_POW2, cache: OracleCache | None = None):
-    """Float64 decode of the listed tokens (all by default) of a seeded problem."""
+def oracle_decode(problem, tokens=None, scale_mode: int = O.SCALE_POW2, cache: OracleCache | None = None,
+                  q_e4m3: torch.Tensor | None = None, q_scale: float | None = None):
+    """Float64 decode of the listed tokens (all by default) of a seeded problem; with q_e4m3
+    ([T, H, 576] uint8 E4M3 codes) and q_scale, of that FP8 q instead of the problem's bf16 q."""
     w = problem.w
     T = w.num_tokens
     tokens = list(range(T)) if tokens is None else list(tokens)
     if cache is None:
         cache = OracleCache(problem, [t // w.next_n for t in tokens], scale_mode)
     sink = None if problem.sink is None else problem.sink.cpu().double().numpy()
-    return O.decode(_bits(problem.q), cache.fetch, w.kv_format, problem.page_table.cpu().numpy(),
+    q = _bits(problem.q) if q_e4m3 is None else q_e4m3.cpu().numpy()
+    return O.decode(q, cache.fetch, w.kv_format, problem.page_table.cpu().numpy(),
                     problem.topk.cpu().numpy(), w.page_size, problem.num_pages, w.sm_scale,
                     sink=sink, next_n=w.next_n, tokens=tokens,
-                    kv_scale=w.kv_scale if w.kv_format == "fp8_tensor" else None)
+                    kv_scale=w.kv_scale if w.kv_format == "fp8_tensor" else None,
+                    q_format="bf16" if q_e4m3 is None else "e4m3", q_scale=q_scale)

@@ -17,6 +17,8 @@ SMLA_KV_FP8_DS = 1
 SMLA_KV_FP8_TENSOR = 2
 SMLA_SCALE_POW2 = 0
 SMLA_SCALE_FP32 = 1
+SMLA_Q_BF16 = 0
+SMLA_Q_FP8_E4M3 = 1
 SMLA_DEVERR_INDEX = 1
 SMLA_DEVERR_PAGE = 2
 SMLA_DEVERR_TIMEOUT = 4
@@ -47,7 +49,8 @@ class smla_desc(ctypes.Structure):
                 ("num_pages", ctypes.c_int64), ("page_table_stride", ctypes.c_int32),
                 ("kv_format", ctypes.c_int32), ("sm_scale", ctypes.c_float),
                 ("num_splits", ctypes.c_int32), ("kv_scale", ctypes.c_float),
-                ("reserved", ctypes.c_int32 * 3)]
+                ("q_format", ctypes.c_int32), ("q_scale", ctypes.c_float),
+                ("reserved", ctypes.c_int32 * 1)]
 
 
 class smla_indexer_desc(ctypes.Structure):
@@ -133,13 +136,15 @@ def _check(fn: str, status: int):
 
 
 def make_desc(num_tokens, num_heads, topk, num_requests, page_size, num_pages, page_table_stride,
-              kv_format, sm_scale, next_n=1, num_splits=0, kv_scale=1.0) -> smla_desc:
+              kv_format, sm_scale, next_n=1, num_splits=0, kv_scale=1.0, q_format=0,
+              q_scale=1.0) -> smla_desc:
     d = smla_desc()
     d.num_tokens, d.num_heads, d.topk = num_tokens, num_heads, topk
     d.num_requests, d.next_n, d.page_size = num_requests, next_n, page_size
     d.num_pages, d.page_table_stride = num_pages, page_table_stride
     d.kv_format, d.sm_scale, d.num_splits = kv_format, sm_scale, num_splits
     d.kv_scale = kv_scale
+    d.q_format, d.q_scale = q_format, q_scale
     return d
 
 

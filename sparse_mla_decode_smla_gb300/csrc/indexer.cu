@@ -71,18 +71,6 @@ constexpr size_t kIxSmem = kIxOffBars + X_COUNT * 8 + 1024;
 static_assert(kIxOffK % 1024 == 0 && kIxStageK % 1024 == 0 && kIxOffSc % 16 == 0, "swizzle atoms, bulk copies");
 static_assert(kIxSmem <= 232448, "shared memory budget");
 
-// Instruction descriptor of kind::f8f6f4 with E4M3 A and B, fp32 accumulator, both K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
-  return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-
 // TMA load of box (x, y, z) of a 3-D tensor map into dst, counting the box bytes on bar.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
                                             uint32_t bar) {
@@ -279,7 +267,7 @@ __global__ void __launch_bounds__(kIxThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_e4m3_f32(128, N);
+      const uint32_t idesc = tc::idesc_e4m3_f32(128, N);
       int u = 0, qloads = 0, rq = -1, r = r_first;
       for (int it = it0; it < it1 && ok; ++it) {
         const Item x = item_at(it, r);
@@ -298,7 +286,7 @@ __global__ void __launch_bounds__(kIxThreads, 1)
           const uint32_t ka = sb + uint32_t(kIxOffK + st * kIxStageK);
 #pragma unroll
           for (int k = 0; k < kIxDim / 32; ++k)
-            mma_f8(tm + uint32_t(b * N), tc::sdesc_sw128(ka + 32 * k, 16, 1024),
+            tc::mma_ss_f8(tm + uint32_t(b * N), tc::sdesc_sw128(ka + 32 * k, 16, 1024),
                    tc::sdesc_sw128(sb + uint32_t(kIxOffQ) + 32 * k, 16, 1024), idesc, k > 0);
           tc::commit(bar(X_EMPTY + st));
           tc::commit(bar(X_DFULL + b));

@@ -34,6 +34,8 @@ struct DecodeArgs {
   // The split CTAs of a (token, head group) form one thread-block cluster (cluster size =
   // num_splits) and merge their partials through distributed shared memory; no o_part.
   int32_t cluster_merge;
+  int32_t q_fp8;   // q holds E4M3 codes (SMLA_Q_FP8_E4M3), times q_scale
+  float q_scale;
 };
 // Largest cluster the in-kernel split merge uses (the portable cluster size).
 constexpr int kMaxClusterMerge = 8;
@@ -42,6 +44,8 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t s);
 // One CTA per (token, split, group of 64 heads); FP8 caches.
 cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s);
+// The FP8-operand head-group kernel: E4M3 q against the per-tensor FP8 cache, 64+ heads.
+cudaError_t launch_decode_hg_f8(const DecodeArgs& a, cudaStream_t s);
 
 // Row gathers (TMA tile::gather4) address the cache by 32-bit row coordinates, and one past
 // the last slot marks a masked row: caches must hold fewer slots than this.
@@ -51,6 +55,9 @@ int kv_row_bytes(int32_t kv_format);
 cudaError_t kv_gather_map(const DecodeArgs& a, CUtensorMap* out);
 // Tensor map of q as [T H rows, 576] bf16 with [64 rows x 64 dims] boxes, 128-byte swizzle.
 cudaError_t q_tile_map(const DecodeArgs& a, CUtensorMap* out);
+// Tensor maps of E4M3 q as [T H rows, 576] bytes: [64 rows x 128 B] boxes with 128-byte
+// swizzle (latent) and [64 rows x 32 B] boxes with 32-byte swizzle (RoPE).
+cudaError_t q_e4m3_maps(const DecodeArgs& a, CUtensorMap* map128, CUtensorMap* map32);
 
 // The tensor-core head-group kernel serves the FP8 caches with at least this many heads.
 constexpr int kHgMinHeads = 64;

@@ -76,8 +76,13 @@ smla_status check_desc(const smla_desc* d) {
     return SMLA_ERR_SHAPE;
   if (d->num_splits < 0 || d->num_splits > smla::kMaxSplits) return SMLA_ERR_SHAPE;
   if (d->topk > smla::kMaxSplits * smla::kMaxSplitLen) return SMLA_ERR_SHAPE;
-  for (int i = 0; i < 3; ++i)
-    if (d->reserved[i] != 0) return SMLA_ERR_SHAPE;
+  if (d->reserved[0] != 0) return SMLA_ERR_SHAPE;
+  if (d->q_format != SMLA_Q_BF16 && d->q_format != SMLA_Q_FP8_E4M3) return SMLA_ERR_UNSUPPORTED;
+  if (d->q_format == SMLA_Q_FP8_E4M3) {
+    if (!(isfinite(d->q_scale) && d->q_scale > 0.f)) return SMLA_ERR_SHAPE;
+    // E4M3 q runs on the FP8-operand tensor-core kernel only
+    if (d->kv_format != SMLA_KV_FP8_TENSOR || d->num_heads < smla::kHgMinHeads) return SMLA_ERR_UNSUPPORTED;
+  }
   return SMLA_OK;
 }
 
@@ -163,6 +168,8 @@ smla::DecodeArgs make_args(const smla_desc* d, const void* q, const void* kv,
   a.num_pages = d->num_pages;
   a.c2 = d->sm_scale * 1.4426950408889634f;
   a.kv_scale = d->kv_format == SMLA_KV_FP8_TENSOR ? d->kv_scale : 1.f;
+  a.q_fp8 = d->q_format == SMLA_Q_FP8_E4M3 ? 1 : 0;
+  a.q_scale = a.q_fp8 ? d->q_scale : 1.f;
   return a;
 }
 
@@ -227,7 +234,7 @@ const char* smla_status_string(int32_t s) {
   }
 }
 
-int32_t smla_abi_version(void) { return 3; }
+int32_t smla_abi_version(void) { return 4; }
 
 smla_status smla_workspace_size(const smla_desc* d, size_t* bytes) {
   if (!bytes) return SMLA_ERR_NULL;
@@ -277,7 +284,9 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
   a.cluster_merge = plan.cluster_merge ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (t_ev_start && cudaEventRecord(t_ev_start, s) != cudaSuccess) return SMLA_ERR_CUDA;
-  const cudaError_t e = use_hg(d) ? smla::launch_decode_hg(a, s) : smla::launch_decode_mma(a, sms, s);
+  const cudaError_t e = a.q_fp8   ? smla::launch_decode_hg_f8(a, s)
+                        : use_hg(d) ? smla::launch_decode_hg(a, s)
+                                    : smla::launch_decode_mma(a, sms, s);
   if (e != cudaSuccess) return SMLA_ERR_CUDA;
   if (t_ev_stop && cudaEventRecord(t_ev_stop, s) != cudaSuccess) return SMLA_ERR_CUDA;
   if (plan.num_splits > 1 && !a.cluster_merge && smla::launch_merge(a, s) != cudaSuccess) return SMLA_ERR_CUDA;

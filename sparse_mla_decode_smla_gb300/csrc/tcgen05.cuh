@@ -32,6 +32,18 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t addr, uint32_t lbo, uint
   return d;
 }
 
+// Same with 32-byte swizzle: K-major tiles of 32-byte rows in 8-row atoms of 256 B
+// (sbo = 256); the atom base is 256-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= uint64_t((addr & 0x3FFFF) >> 4);
+  d |= uint64_t((lbo & 0x3FFFF) >> 4) << 16;
+  d |= uint64_t((sbo & 0x3FFFF) >> 4) << 32;
+  d |= uint64_t(1) << 46;  // descriptor version (tcgen05)
+  d |= uint64_t(6) << 61;  // SWIZZLE_32B
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn_major) << 15) |
@@ -42,6 +54,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn_major = false,
+                                                      bool b_mn_major = false) {
+  return (1u << 4) | (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
+         (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// D(tmem) (+)= A(smem desc) * B(smem desc), E4M3 operands (kind::f8f6f4, K = 32 per MMA)
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
 // D(tmem) (+)= A(smem desc) * B(smem desc)

@@ -88,6 +88,24 @@ cudaError_t q_tile_map(const DecodeArgs& a, CUtensorMap* out) {
   return cudaSuccess;
 }
 
+cudaError_t q_e4m3_maps(const DecodeArgs& a, CUtensorMap* map128, CUtensorMap* map32) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cuuint64_t(kDim), cuuint64_t(int64_t(a.T) * a.H)};
+  const cuuint64_t strides[1] = {cuuint64_t(kDim)};
+  const cuuint32_t estr[2] = {1, 1};
+  const cuuint32_t box128[2] = {128, 64};
+  CUresult r = encode(map128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.q), dims, strides, box128, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const cuuint32_t box32[2] = {32, 64};
+  r = encode(map32, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.q), dims, strides, box32, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t index_key_map(const IndexerArgs& a, CUtensorMap* out) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.smla_abi_version() == 3
+    assert L.smla_abi_version() == 4
     for s in range(11):
         assert smla.status_string(s) != "unknown status"
     assert smla.status_string(99) == "unknown status"
@@ -62,11 +62,13 @@ def test_binding_statuses_and_error_bits_match_header():
 
 
 def test_desc_layout_matches_header():
-    # int32 x6, int64, int32 x2, float, int32, float, int32[3]; natural alignment
+    # int32 x6, int64, int32 x2, float, int32, float, int32, float, int32; natural alignment
     assert ctypes.sizeof(smla.smla_desc) == 64
     assert smla.smla_desc.num_pages.offset == 24
     assert smla.smla_desc.kv_scale.offset == 48
-    assert smla.smla_desc.reserved.offset == 52
+    assert smla.smla_desc.q_format.offset == 52
+    assert smla.smla_desc.q_scale.offset == 56
+    assert smla.smla_desc.reserved.offset == 60
 
 
 def _desc(**kw):
@@ -99,10 +101,22 @@ def test_decode_rejects_null_and_misaligned_pointers(L):
     assert _decode_status(L, _desc(), topk=16 + 4) == 3
     assert _decode_status(L, _desc(), ws=256 + 16) == 3
     d = _desc()
-    d.reserved[2] = 1
+    d.reserved[0] = 1
     assert _decode_status(L, d) == 2
     # more tokens than requests * next_n without req_id_per_token
     assert _decode_status(L, _desc(num_tokens=9, num_requests=2, next_n=4)) == 2
+
+
+def test_decode_fp8_q_host_checks(L):
+    # E4M3 q is served with the per-tensor FP8 cache and 64 or more heads only; q_scale must be
+    # finite and positive; an unknown q_format is unsupported (all rejected before any launch)
+    ten = dict(kv_format=smla.SMLA_KV_FP8_TENSOR, num_heads=64, q_format=smla.SMLA_Q_FP8_E4M3, q_scale=0.5)
+    assert _decode_status(L, _desc(**{**ten, "kv_format": smla.SMLA_KV_FP8_DS})) == 4
+    assert _decode_status(L, _desc(**{**ten, "kv_format": smla.SMLA_KV_BF16})) == 4
+    assert _decode_status(L, _desc(**{**ten, "num_heads": 48})) == 4
+    assert _decode_status(L, _desc(**{**ten, "q_scale": 0.0})) == 2
+    assert _decode_status(L, _desc(**{**ten, "q_scale": float("inf")})) == 2
+    assert _decode_status(L, _desc(q_format=2)) == 4
 
 
 def test_decode_rejects_caches_beyond_32_bit_row_coordinates(L):

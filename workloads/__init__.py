@@ -112,7 +112,21 @@ WORKLOADS = [
 EXTRA_WORKLOADS = [
     Workload("fp8tensor_T32_H64_K2048_ctx1k-32k", 32, 1, 64, 2048, 64, "fp8_tensor", 1024, 32768,
              False, seed_offset=5, kv_scale=1.0),
+    # the two 128-head batches on the per-tensor cache, for FP8 q against it
+    Workload("fp8tensor_T128_H128_K2048_ctx64k_sink", 128, 1, 128, 2048, 64, "fp8_tensor", 65536, 65536,
+             True, seed_offset=6, kv_scale=1.0),
+    Workload("fp8tensor_mtp_T256_H128_K2048_ctx4k-128k_sink", 64, 4, 128, 2048, 64, "fp8_tensor", 4096,
+             131072, True, seed_offset=7, kv_scale=1.0),
 ]
+# Per-tensor scale of FP8 q in the tests and the bench: N(0, 1) q maps to |q / 2^-5| < 448.
+Q_SCALE_FP8 = 2.0 ** -5
+
+
+def q_to_e4m3(q: torch.Tensor, q_scale: float = Q_SCALE_FP8) -> torch.Tensor:
+    """The caller's FP8 q: E4M3FN codes (uint8, same shape) of q / q_scale by torch's cast,
+    clamped to +-448 first (an input of the decode, like q itself)."""
+    x = (q.float() / q_scale).clamp(-448.0, 448.0)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
 
 
