@@ -6,18 +6,18 @@
 // l's output dims [0, 256), lane 64 + l its dims [256, 512).
 //
 // What changes with 8-bit operands:
-//  * q arrives as E4M3 codes and goes by six TMA boxes straight into its A-operand layout in
-//    shared memory (two 128-byte-swizzled atoms of [128 rows x 128 dims] for the latent, rows
-//    0-63 the heads' dims [0, 256) and rows 64-127 their dims [256, 512); one 32-byte-swizzled
-//    [128 rows x 32 dims] block for RoPE). Nothing converts it.
+//  * q arrives as E4M3 codes: six TMA boxes stage it in shared memory, and the softmax warps
+//    copy each row into TMEM, the A operand of QK (lane l < 64: head l's dims [0, 256) and
+//    RoPE dims 512..543; lane 64 + l: dims [256, 512) and 544..575; four codes a column).
 //  * The gathered cache rows are the MMA operands as they are: the copy warps only move each
 //    16-byte chunk of a raw row to its place in the swizzled K tile (latent: two 16 KB pair
 //    blocks [64 slots x 128 low dims | same slots x 128 high dims]; RoPE: [64 slots x 32 |
-//    same slots x 32], 32-byte swizzle). A K tile is half the 16-bit one, so three buffers fit.
+//    same slots x 32], 32-byte swizzle). A K tile is half the 16-bit one: three buffers, and
+//    a raw ring of two tiles, fit.
 //  * QK of a 64-slot tile is 9 M128 N128 K32 MMAs, PV 4 M128 N256 K32: half the tensor-pipe
-//    time of the 16-bit kernel for the same work.
-//  * q sits in shared memory, so the tensor memory holds two score buffers (O 256 columns, S
-//    2 x 128): QK of tile i+1 runs while the softmax reads tile i.
+//    time of the 16-bit kernel for the same work. What bounds the tile is shared-memory
+//    bandwidth (gathers, the copy, the MMAs' operand reads, the score exchange), hence q in
+//    TMEM and an MMA issuer that sleeps on its barriers instead of polling them.
 //  * P is E4M3: p = 2^(s - m + 7), with the running max m moved whenever the max grows by more
 //    than 1 (log2 units), so P <= 256 < 448 and values down to 2^-16 of the max survive. The
 //    output is normalised by the sum of the E4M3 values PV accumulated (a convex combination
@@ -47,7 +47,7 @@ constexpr int kFProducers = 2;
 constexpr int kFMmaWarp = kFFirstProducer + kFProducers;
 constexpr int kFThreads = 32 * (kFMmaWarp + 1);
 constexpr int kFKBufs = 3;
-constexpr int kFRawStages = 4;                 // a whole tile
+constexpr int kFRawStages = 8;  // two tiles of gathered rows in flight
 constexpr int kFGroup = 4 * kFp8TensorRowBytes;  // four gathered rows, 2304 B (128-byte multiple)
 constexpr int kFRawStage = 4 * kFGroup;          // 16 rows
 constexpr int kFPairBlk = 2 * kFN * 128;         // [64 slots x 128 low dims | same slots x 128 high dims]
@@ -64,16 +64,21 @@ constexpr float kFRescaleThreshold = 1.f;  // log2 units: P stays below 2^(1 + k
 constexpr float kFPShift = 7.f;            // P = 2^(s - m + 7) <= 256 (E4M3 max 448)
 static_assert(kFIdxAhead <= 2 * kFAhead && kFIdxRing > kFIdxAhead && kFPageRing > kFAhead, "index and page rings");
 static_assert(kFGroup % 128 == 0, "gather destinations are 128-byte aligned");
+// the producers run at most (K buffers + raw stages / 4 + 1) tiles ahead of the softmax
+static_assert(kFMetaRing > kFKBufs + (kFRawStages + 3) / 4 + 1, "slot-mask ring");
 
 // TMEM columns (512 allocated)
 constexpr uint32_t kFTmO = 0;    // O [128 lanes x 256] fp32, lanes 64.. = high dims
-constexpr uint32_t kFTmS = 256;  // scores, two buffers of [128 lanes x 128] fp32
+constexpr uint32_t kFTmS = 256;  // scores [128 lanes x 128] fp32
+constexpr uint32_t kFTmQ = 384;  // q [128 lanes x 288 codes]: 64 latent columns, then 8 RoPE
 
 constexpr size_t kFOffK = 0;
 constexpr size_t kFOffRope = kFOffK + size_t(kFKBufs) * kFKLat;
-constexpr size_t kFOffQ = kFOffRope + size_t(kFKBufs) * kFRopeBlk;
+constexpr size_t kFOffP = kFOffRope + size_t(kFKBufs) * kFRopeBlk;  // [0 | P | 0]
+// q is staged by TMA in the K-tile area (free until the copy warps' first write), then placed in
+// TMEM: two 128-byte-swizzled latent atoms and a 32-byte-swizzled RoPE block
+constexpr size_t kFOffQ = kFOffK;
 constexpr size_t kFOffQr = kFOffQ + 2 * size_t(kFQAtom);
-constexpr size_t kFOffP = kFOffQr + kFQRope;  // [0 | P | 0]
 constexpr size_t kFOffRaw = kFOffP + 3 * size_t(kFPBlk);
 constexpr size_t kFOffXs = kFOffRaw + size_t(kFRawStages) * kFRawStage;
 constexpr size_t kFOffXm = kFOffXs + 128 * size_t(kFXRow);
@@ -87,20 +92,37 @@ enum {
   F_RAW_EMPTY = F_RAW_FULL + kFRawStages,
   F_K_FULL = F_RAW_EMPTY + kFRawStages,  // [buffer]
   F_K_FREE = F_K_FULL + kFKBufs,         // [buffer]
-  F_S_FULL = F_K_FREE + kFKBufs,         // [score buffer]
-  F_S_FREE = F_S_FULL + 2,               // [score buffer]
-  F_P_READY = F_S_FREE + 2,
-  F_PV_DONE, F_Q, F_DRAIN, F_COUNT
+  F_S_FULL = F_K_FREE + kFKBufs,
+  F_S_FREE, F_P_READY, F_PV_DONE,
+  F_Q,   // q's staging copy has landed
+  F_QP,  // q is placed in TMEM (and its staging copy read)
+  F_DRAIN, F_COUNT
 };
-static_assert(F_COUNT == 2 * kFRawStages + 2 * kFKBufs + 8, "one mbarrier per ring stage and buffer, none shared");
+static_assert(F_COUNT == 2 * kFRawStages + 2 * kFKBufs + 7, "one mbarrier per ring stage and buffer, none shared");
 constexpr size_t kSmemF8 = kFOffBars + F_COUNT * 8 + 1024;  // + alignment slack
 static_assert(kSmemF8 <= 232448, "shared memory budget");
+static_assert(kFOffQr + kFQRope <= kFOffRope, "q staging fits in the K-tile area");
 static_assert(kFOffK % 1024 == 0 && kFKLat % 1024 == 0 && kFOffQ % 1024 == 0 && kFOffRope % 256 == 0 &&
                   kFRopeBlk % 256 == 0 && kFOffQr % 256 == 0 && kFOffP % 512 == 0 && kFOffRaw % 128 == 0 &&
                   kFOffBars % 8 == 0,
               "swizzle atoms: 1024 B (128-byte swizzle), 512 B (64-byte), 256 B (32-byte)");
-// the in-cluster split merge reuses the K-tile area: 72 rows of 1024 B, LSEs, weights
-static_assert(size_t(kFKBufs) * kFKLat >= 72 * 1024 + 512 + 64 * kMaxClusterMerge * 4, "merge buffer");
+// the in-cluster split merge reuses the area below P (K tiles, RoPE blocks, q; free once every
+// MMA has completed): 72 rows of 1024 B, LSEs, weights. P holds the final row factors then.
+static_assert(kFOffP - kFOffK >= 72 * 1024 + 512 + 64 * kMaxClusterMerge * 4, "merge buffer");
+
+// Wait for the phase of `bar` with the given parity, suspended for at most about hint_ns (the
+// thread wakes as soon as the phase completes); true once it has completed. It spares the
+// shared memory the polling of a test loop.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 
 __global__ void __launch_bounds__(kFThreads, 1)
     decode_hg_f8_kernel(const DecodeArgs p, const __grid_constant__ CUtensorMap kv_map,
@@ -186,10 +208,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
         mbar_init(bar(F_K_FULL + b), kFCopyWarps);
         mbar_init(bar(F_K_FREE + b), 1);
       }
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(bar(F_S_FULL + b), 1);
-        mbar_init(bar(F_S_FREE + b), 4);
-      }
+      mbar_init(bar(F_S_FULL), 1);
+      mbar_init(bar(F_S_FREE), 4);
+      mbar_init(bar(F_QP), 4);  // the four softmax warps
       mbar_init(bar(F_P_READY), 4);
       mbar_init(bar(F_PV_DONE), 1);
       mbar_init(bar(F_Q), 1);
@@ -277,25 +298,23 @@ __global__ void __launch_bounds__(kFThreads, 1)
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t kIdQK = tc::idesc_e4m3_f32(128, 128, false, false);
       constexpr uint32_t kIdPV = tc::idesc_e4m3_f32(128, 256, false, true);
-      const uint32_t qa = sb + uint32_t(kFOffQ), qr = sb + uint32_t(kFOffQr);
-      // QK of tile i once its K tile is written and the scores of tile i-2 (same buffer)
-      // have been read
+      // QK of tile i once its K tile is written and the scores of tile i-1 have been read
       auto qk_ready = [&](int i) {
         return mbar_test_wait(bar(F_K_FULL + i % kFKBufs), (i / kFKBufs) & 1) &&
-               (i < 2 || mbar_test_wait(bar(F_S_FREE + (i & 1)), ((i - 2) >> 1) & 1));
+               (i == 0 || mbar_test_wait(bar(F_S_FREE), (i - 1) & 1));
       };
       auto qk = [&](int i) {
         tc::fence_after();
         const int b = i % kFKBufs;
         const uint32_t kt = sb + uint32_t(kFOffK) + uint32_t(b * kFKLat);
         const uint32_t kr = sb + uint32_t(kFOffRope) + uint32_t(b * kFRopeBlk);
-        const uint32_t d = tm + kFTmS + 128u * uint32_t(i & 1);
+        const uint32_t d = tm + kFTmS;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)  // 32 dims per MMA: atom j / 4, bytes 32 (j % 4) of each row
-          tc::mma_ss_f8(d, tc::sdesc_sw128(qa + (j >> 2) * kFQAtom + (j & 3) * 32, 16, 1024),
-                        tc::sdesc_sw128(kt + (j >> 2) * kFPairBlk + (j & 3) * 32, 16, 1024), kIdQK, j > 0);
-        tc::mma_ss_f8(d, tc::sdesc_sw32(qr, 16, 256), tc::sdesc_sw32(kr, 16, 256), kIdQK, 1);
-        tc::commit(bar(F_S_FULL + (i & 1)));
+        for (int j = 0; j < 8; ++j)  // 32 dims per MMA: q columns 8j.., K pair block j / 4, bytes 32 (j % 4)
+          tc::mma_ts_f8(d, tm + kFTmQ + 8 * j, tc::sdesc_sw128(kt + (j >> 2) * kFPairBlk + (j & 3) * 32, 16, 1024),
+                        kIdQK, j > 0);
+        tc::mma_ts_f8(d, tm + kFTmQ + 64, tc::sdesc_sw32(kr, 16, 256), kIdQK, 1);
+        tc::commit(bar(F_S_FULL));
       };
       auto pv = [&](int i) {
         tc::fence_after();
@@ -313,7 +332,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         tc::commit(bar(F_K_FREE + b));
         tc::commit(bar(F_PV_DONE));
       };
-      bool qok = mbar_wait(bar(F_Q), 0);
+      bool qok = mbar_wait(bar(F_QP), 0);
       if (!qok) ok = false;
       // PV of the oldest scored tile first when its P is ready, else QK of the next tile (at
       // most two tiles ahead of PV: two score buffers)
@@ -329,6 +348,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
             ok = false;
             break;
           }
+          // nothing to issue: sleep on the event that gates the next step (P of the oldest
+          // scored tile, else the next K tile) rather than polling shared memory
+          if (npv < nqk)
+            mbar_try_wait_hint(bar(F_P_READY), npv & 1, 100);
+          else if (nqk < ntiles)
+            mbar_try_wait_hint(bar(F_K_FULL + nqk % kFKBufs), (nqk / kFKBufs) & 1, 100);
           continue;
         }
         t0 = globaltimer_ns();
@@ -352,7 +377,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
       const int b = i % kFKBufs;
       const uint32_t kt = sb + uint32_t(kFOffK) + uint32_t(b * kFKLat);
       const uint32_t kr = sb + uint32_t(kFOffRope) + uint32_t(b * kFRopeBlk);
-      // the buffer is free once PV of tile i - kFKBufs is complete
+      // the first K tile overwrites q's staging copy, read once q is placed in TMEM; later
+      // ones wait for PV of tile i - kFKBufs to free their buffer
+      if (i == 0 && !mbar_wait(bar(F_QP), 0)) {
+        ok = false;
+        break;
+      }
       if (i >= kFKBufs && !mbar_wait(bar(F_K_FREE + b), ((i - kFKBufs) / kFKBufs) & 1)) {
         ok = false;
         break;
@@ -430,11 +460,50 @@ __global__ void __launch_bounds__(kFThreads, 1)
       tc::wait_st();
     };
 
+    // q placement: TMEM lane r = 32 warp + lane takes row r of the staged q (head r % 64, dims
+    // [256 (r / 64), +256) and RoPE dims [512 + 32 (r / 64), +32)), four codes a column
+    {
+      const int qrow = 32 * warp + lane;
+      bool have = ntiles > 0 && mbar_wait(bar(F_Q), 0);
+      have = __all_sync(0xffffffffu, have);  // the TMEM stores are warp-wide
+      if (ntiles > 0 && !have) {
+        good = false;
+        if (lane == 0) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
+      }
+      if (have) {
+        const uint32_t qa = sb + uint32_t(kFOffQ), qr = sb + uint32_t(kFOffQr);
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            uint32_t w[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int c = 4 * part + k;  // 16-byte chunk of the 128-byte atom row
+              const uint4 v = lds128(qa + uint32_t(a * kFQAtom + qrow * 128 + ((c ^ (qrow & 7)) << 4)));
+              w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+            }
+            tc::st16(lrow + kFTmQ + 32 * a + 16 * part, w);
+          }
+        uint32_t rw[8];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint4 v = lds128(qr + uint32_t(qrow * 32 + ((c ^ ((qrow >> 2) & 1)) << 4)));
+          rw[4 * c] = v.x; rw[4 * c + 1] = v.y; rw[4 * c + 2] = v.z; rw[4 * c + 3] = v.w;
+        }
+        tc::st8(lrow + kFTmQ + 64, rw);
+        tc::wait_st();
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(F_QP));  // also: the staging copy has been read
+    }
+
     bool loop_ok = true;
     for (int i = 0; i < ntiles; ++i) {
       float v[64];
-      const uint32_t sbuf = kFTmS + 128u * uint32_t(i & 1);  // column offset (lrow holds tm)
-      const bool got = good && mbar_wait(bar(F_S_FULL + (i & 1)), (i >> 1) & 1);
+      const uint32_t sbuf = kFTmS;  // column offset (lrow holds tm)
+      const bool got = good && mbar_wait(bar(F_S_FULL), i & 1);
       if (got) {
         tc::fence_after();
         uint32_t w0[32], w1[32];
@@ -452,7 +521,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         for (int e = 0; e < 64; ++e) v[e] = 0.f;
       }
       __syncwarp();
-      if (lane == 0 && got) mbar_arrive(bar(F_S_FREE + (i & 1)));
+      if (lane == 0 && got) mbar_arrive(bar(F_S_FREE));
       float own[32], send[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
