@@ -64,12 +64,14 @@ TRAFFIC = {
     ("fp8_T128_H128_K2048_ctx64k_sink", "decode_hg_kernel"): (230827264, "c40b4989cdfa8e20"),
     ("fp8_T32_H64_K2048_ctx1k-32k", "decode_hg_kernel"): (51818240, "c40b4989cdfa8e20"),
     ("fp8_T256_H16_K2048_ctx8k-128k_pad20", "decode_mma_kernel"): (334121472, "0896484c860414c8"),
+    ("fp8tensor_mtp_T256_H128_K2048_ctx4k-128k_sink", "decode_hg_f8_kernel"): (342332928, "3b645df95524cce1"),
     ("store_fp8_ds_rows65536_P64_pos131072", "pack_kernel"): (111947008, "4dfd7199c86d8388"),
 }
 KERNEL_SOURCES = {
     "decode_hg_kernel": ("common.cuh", "kernels.h", "tcgen05.cuh", "decode_hg.cu", "tensor_maps.cu"),
     "decode_mma_kernel": ("common.cuh", "kernels.h", "decode_mma.cu"),
     "pack_kernel": ("common.cuh", "kernels.h", "cache_kernels.cu"),
+    "decode_hg_f8_kernel": ("common.cuh", "kernels.h", "tcgen05.cuh", "decode_hg_f8.cu", "tensor_maps.cu"),
 }
 
 
