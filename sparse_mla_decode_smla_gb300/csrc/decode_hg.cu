@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kHgThreads, 1)
   // the splits of a (token, head group) are consecutive CTAs: with the in-kernel merge they
   // form one cluster, and the split is the CTA's rank in it
   const int split = blockIdx.x % p.num_splits;
-  const int item = blockIdx.x / p.num_splits;
+  const int item = p.item0 + int(blockIdx.x) / p.num_splits;
   const int g = item % G;
   const int t = item / G;
   const int r = p.req_id ? __ldg(p.req_id + t) : t / p.next_n;
@@ -1002,7 +1002,8 @@ cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e = kv_gather_map(a, &map);
   if (e == cudaSuccess) e = q_tile_map(a, &qmap);
   if (e != cudaSuccess) return e;
-  const int64_t grid = int64_t(a.T) * a.num_splits * ((a.H + 63) / 64);
+  const int64_t items = a.nitems > 0 ? a.nitems : int64_t(a.T) * ((a.H + 63) / 64);
+  const int64_t grid = items * a.num_splits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kHgThreads);

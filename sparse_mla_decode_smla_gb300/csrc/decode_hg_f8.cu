@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   const float c2 = p.c2 * p.q_scale * p.kv_scale;
   const int G = (p.H + 63) >> 6;
   const int split = blockIdx.x % p.num_splits;
-  const int item = blockIdx.x / p.num_splits;
+  const int item = p.item0 + int(blockIdx.x) / p.num_splits;
   const int g = item % G;
   const int t = item / G;
   const int r = p.req_id ? __ldg(p.req_id + t) : t / p.next_n;
@@ -834,7 +834,8 @@ cudaError_t launch_decode_hg_f8(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e = kv_gather_map(a, &map);
   if (e == cudaSuccess) e = q_e4m3_maps(a, &q128, &q32);
   if (e != cudaSuccess) return e;
-  const int64_t grid = int64_t(a.T) * a.num_splits * ((a.H + 63) / 64);
+  const int64_t items = a.nitems > 0 ? a.nitems : int64_t(a.T) * ((a.H + 63) / 64);
+  const int64_t grid = items * a.num_splits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kFThreads);

@@ -36,6 +36,9 @@ struct DecodeArgs {
   int32_t cluster_merge;
   int32_t q_fp8;   // q holds E4M3 codes (SMLA_Q_FP8_E4M3), times q_scale
   float q_scale;
+  // head-group kernels: this launch serves the (token, head group) items [item0, item0 +
+  // nitems), nitems = 0 meaning all T x ceil(H / 64) of them
+  int32_t item0, nitems;
 };
 // Largest cluster the in-kernel split merge uses (the portable cluster size).
 constexpr int kMaxClusterMerge = 8;

@@ -283,10 +283,33 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
   a.part_f16 = use_hg(d) ? 1 : 0;
   a.cluster_merge = plan.cluster_merge ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto launch = [&](const smla::DecodeArgs& x) {
+    return x.q_fp8 ? smla::launch_decode_hg_f8(x, s)
+                   : use_hg(d) ? smla::launch_decode_hg(x, s) : smla::launch_decode_mma(x, sms, s);
+  };
+  // Tail split (tensor-core kernels, library-chosen splits): when the (token, head group)
+  // items fill whole waves of one CTA per SM plus a remainder of at most half a wave, the
+  // remainder runs as a second launch with two splits an item, merged inside their cluster, so
+  // the last wave takes about half a CTA's time instead of a whole one.
+  const int units = d->num_tokens * ((d->num_heads + 63) / 64);
+  const int rem = units % sms;
+  const bool tail = use_hg(d) && d->num_splits == 0 && plan.num_splits == 1 && d->topk >= 512 && units > sms &&
+                    rem > 0 && 2 * rem <= sms;
   if (t_ev_start && cudaEventRecord(t_ev_start, s) != cudaSuccess) return SMLA_ERR_CUDA;
-  const cudaError_t e = a.q_fp8   ? smla::launch_decode_hg_f8(a, s)
-                        : use_hg(d) ? smla::launch_decode_hg(a, s)
-                                    : smla::launch_decode_mma(a, sms, s);
+  cudaError_t e;
+  if (tail) {
+    smla::DecodeArgs full = a, last = a;
+    full.nitems = units - rem;
+    last.item0 = units - rem;
+    last.nitems = rem;
+    last.num_splits = 2;
+    last.split_len = ((d->topk + 1) / 2 + smla::kTile - 1) / smla::kTile * smla::kTile;
+    last.cluster_merge = 1;
+    e = launch(full);
+    if (e == cudaSuccess) e = launch(last);
+  } else {
+    e = launch(a);
+  }
   if (e != cudaSuccess) return SMLA_ERR_CUDA;
   if (t_ev_stop && cudaEventRecord(t_ev_stop, s) != cudaSuccess) return SMLA_ERR_CUDA;
   if (plan.num_splits > 1 && !a.cluster_merge && smla::launch_merge(a, s) != cudaSuccess) return SMLA_ERR_CUDA;

@@ -482,3 +482,18 @@ def test_full_size_sampled_tokens(name):
     assert smla.read_error(dd.desc, dd.workspace) == 0
     del dd, p
     torch.cuda.empty_cache()
+
+
+def test_tail_wave_split_launch():
+    # (token, head group) items filling one wave of SMs plus 8: the library runs the last 8
+    # items as a second launch of two splits each, merged in their cluster; every token,
+    # those of the tail included, against the oracle
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = (sms + 8 + 1) // 2
+    w = W.small_variant(W.WORKLOADS[2], num_requests=T, ctx_lo=600, ctx_hi=600, topk=512)
+    p = W.make_problem(w)
+    dd = DeviceDecode(p)
+    out, lse = dd.run()
+    torch.cuda.synchronize()
+    assert int(dd.workspace[0].item()) == 0
+    assert_parity(out, lse, oracle_decode(p))
