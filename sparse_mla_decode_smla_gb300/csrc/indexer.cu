@@ -21,7 +21,8 @@
 //    tcgen05.mma kind::f8f6f4 (K = 32 each), into one of two TMEM accumulators. The next_n query
 //    rows of a request share every key tile: it is read once, not next_n times.
 //  * epilogue (warps 2-9): thread = slot; each warp pair of a TMEM lane quarter splits the
-//    request's query rows; scale, ReLU and the weighted sum over heads in fp32; coalesced
+//    request's query rows; ReLU and the weighted sum over heads in fp32 in four independent
+//    chains, the key's scale applied once (max(0, s d) = |s| max(0, sgn(s) d)); coalesced
 //    stores of the visible logits.
 // Every wait is bounded; a wait that gives up sets SMLA_DEVERR_TIMEOUT.
 //
@@ -68,8 +69,15 @@ constexpr size_t kIxOffBars = (kIxOffTm + 16 + 7) / 8 * 8;
 enum { X_FULL = 0, X_EMPTY = X_FULL + kIxStages, X_DFULL = X_EMPTY + kIxStages, X_DEMPTY = X_DFULL + 2,
        X_QFULL = X_DEMPTY + 2, X_QFREE, X_DRAIN, X_COUNT };
 constexpr size_t kIxSmem = kIxOffBars + X_COUNT * 8 + 1024;
-static_assert(kIxOffK % 1024 == 0 && kIxStageK % 1024 == 0 && kIxOffSc % 16 == 0, "swizzle atoms, bulk copies");
+static_assert(kIxOffK % 1024 == 0 && kIxStageK % 1024 == 0 && kIxOffSc % 16 == 0 && kIxOffW % 16 == 0,
+              "swizzle atoms, bulk copies, weight vectors");
 static_assert(kIxSmem <= 232448, "shared memory budget");
+
+// Four fp32 from shared memory (16-byte aligned).
+__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
+  const uint4 v = lds128(addr);
+  return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+}
 
 // TMA load of box (x, y, z) of a 3-D tensor map into dst, counting the box bytes on bar.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
@@ -306,8 +314,9 @@ __global__ void __launch_bounds__(kIxThreads, 1)
     const int quarter = warp & 3, half = ew >> 2;
     const int row = 32 * quarter + lane;  // slot within the tile
     const uint32_t lrow = tm + (uint32_t(32 * quarter) << 16);
+    // the two warps of a lane quarter split the request's query rows
     const int nn = p.next_n, i_lo = half ? (nn + 1) / 2 : 0, i_hi = half ? nn : (nn + 1) / 2;
-    const float* wsm = reinterpret_cast<const float*>(sm + kIxOffW);
+    const uint32_t wsm = sb + uint32_t(kIxOffW);
     int u = 0, r = r_first, rq = -1, qloads = 0;
     for (int it = it0; it < it1 && ok; ++it) {
       const Item x = item_at(it, r);
@@ -329,21 +338,40 @@ __global__ void __launch_bounds__(kIxThreads, 1)
         // consumed by the MMAs, whose commit is the stage's other arrival)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(X_EMPTY + st));
+        // max(0, sc * d) = |sc| * max(0, sgn * d), sgn the sign of sc: the scale leaves the sum,
+        // and with every lane's scale non-negative (quantisation scales) the sign does too
+        const bool pos = __all_sync(0xffffffffu, !(sc < 0.f));
+        const float sgn = sc < 0.f ? -1.f : 1.f, asc = fabsf(sc);
         for (int i = i_lo; i < i_hi; ++i) {
-          float acc = 0.f;
+          uint32_t v[64];  // the row's 64 (or 32) head scores, both loads before one wait
+          tc::ld32(lrow + uint32_t(b * N + i * p.H), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          if (p.H > 32) tc::ld32(lrow + uint32_t(b * N + i * p.H + 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tc::wait_ld();
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // four independent chains
+          if (pos) {
 #pragma unroll
-          for (int h0 = 0; h0 < 64; h0 += 32) {
-            if (h0 >= p.H) break;
-            uint32_t v[32];
-            tc::ld32(lrow + uint32_t(b * N + i * p.H + h0), v);
-            tc::wait_ld();
+            for (int e = 0; e < 64; e += 4) {
+              if (e >= p.H) break;
+              const float4 w4 = lds_f32x4(wsm + uint32_t(i * p.H + e) * 4u);
+              a0 = fmaf(w4.x, fmaxf(0.f, __uint_as_float(v[e])), a0);
+              a1 = fmaf(w4.y, fmaxf(0.f, __uint_as_float(v[e + 1])), a1);
+              a2 = fmaf(w4.z, fmaxf(0.f, __uint_as_float(v[e + 2])), a2);
+              a3 = fmaf(w4.w, fmaxf(0.f, __uint_as_float(v[e + 3])), a3);
+            }
+          } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              acc = fmaf(wsm[i * p.H + h0 + e], fmaxf(0.f, __uint_as_float(v[e]) * sc), acc);
+            for (int e = 0; e < 64; e += 4) {
+              if (e >= p.H) break;
+              const float4 w4 = lds_f32x4(wsm + uint32_t(i * p.H + e) * 4u);
+              a0 = fmaf(w4.x, fmaxf(0.f, sgn * __uint_as_float(v[e])), a0);
+              a1 = fmaf(w4.y, fmaxf(0.f, sgn * __uint_as_float(v[e + 1])), a1);
+              a2 = fmaf(w4.z, fmaxf(0.f, sgn * __uint_as_float(v[e + 2])), a2);
+              a3 = fmaf(w4.w, fmaxf(0.f, sgn * __uint_as_float(v[e + 3])), a3);
+            }
           }
           const int vis = ctx - nn + 1 + i;
           const int t = x.r * nn + i;
-          if (s < vis) p.logits[int64_t(t) * p.logits_stride + s] = acc;
+          if (s < vis) p.logits[int64_t(t) * p.logits_stride + s] = asc * ((a0 + a1) + (a2 + a3));
         }
         tc::fence_before();
         __syncwarp();
