@@ -79,6 +79,25 @@ __device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
   return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
 }
 
+// sum_h w[h] * max(0, sgn * d[h]) over H heads (d: the row's TMEM words), in four independent
+// chains. H is a compile-time constant so the weight loads (shared memory, the same address in
+// every lane) are all issued before the first is used.
+template <int H, bool POS>
+__device__ __forceinline__ float head_sum(const uint32_t (&d)[64], uint32_t w_row, float sgn) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int e = 0; e < H; e += 4) {
+    const float4 w4 = lds_f32x4(w_row + uint32_t(e) * 4u);
+    const float x0 = __uint_as_float(d[e]), x1 = __uint_as_float(d[e + 1]);
+    const float x2 = __uint_as_float(d[e + 2]), x3 = __uint_as_float(d[e + 3]);
+    a0 = fmaf(w4.x, fmaxf(0.f, POS ? x0 : sgn * x0), a0);
+    a1 = fmaf(w4.y, fmaxf(0.f, POS ? x1 : sgn * x1), a1);
+    a2 = fmaf(w4.z, fmaxf(0.f, POS ? x2 : sgn * x2), a2);
+    a3 = fmaf(w4.w, fmaxf(0.f, POS ? x3 : sgn * x3), a3);
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
 // TMA load of box (x, y, z) of a 3-D tensor map into dst, counting the box bytes on bar.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
                                             uint32_t bar) {
@@ -218,51 +237,47 @@ __global__ void __launch_bounds__(kIxThreads, 1)
         cp_async_commit();  // an empty group keeps the count of groups in flight at one
       cp_async_wait<1>();   // this item's entries have landed
       __syncwarp();
-      if (lane == 0) {
-        if (x.r != rq) {  // q and weights of the request, once the previous ones are unused
-          if (qloads > 0 && !mbar_wait(bar(X_QFREE), (qloads - 1) & 1)) ok = false;
-          if (ok) {
-            mbar_arrive_expect_tx(bar(X_QFULL), uint32_t(N) * kIxDim + uint32_t(N) * 4u);
-            tma_load_2d(sb + uint32_t(kIxOffQ), &qmap, 0, x.r * N, bar(X_QFULL));
-            bulk_g2s(sb + uint32_t(kIxOffW), p.weights + int64_t(x.r) * N, uint32_t(N) * 4u, bar(X_QFULL));
-            ++qloads;
-            rq = x.r;
-          }
-        }
-        const int ctx = ctx_of(x.r);
-        const int nt = tiles_of(x);
-        for (int j = 0; j < nt && ok; ++j, ++u) {
-          const int st = u % kIxStages;
-          if (!mbar_wait(bar(X_EMPTY + st), ((u / kIxStages) & 1) ^ 1)) { ok = false; break; }
-          // pages outside the request's table or the pool are not fetched: their rows keep
-          // stale bytes, which only feed logits beyond the visible range or flagged ones
-          uint32_t bytes = 0, mask = 0;
-          for (int g = 0; g < npg; ++g) {
-            const int li = j * npg + g;
-            const int32_t pg = spg[buf * 64 + li];
-            if (pg >= 0 && pg < p.num_pages) {
-              mask |= 1u << g;
-              bytes += uint32_t(P) * (kIxDim + 4);
-            } else if (((x.c * ppi + li) << p.log2_page) < ctx) {  // a page the visible context needs
-              atomicOr(p.err, SMLA_DEVERR_PAGE);
-            }
-          }
-          mbar_arrive_expect_tx(bar(X_FULL + st), bytes);
-          for (int g = 0; g < npg; ++g) {
-            if (!((mask >> g) & 1u)) continue;
-            const int32_t pg = spg[buf * 64 + j * npg + g];
-            tma_load_3d(sb + uint32_t(kIxOffK + st * kIxStageK) + uint32_t(g * P * kIxDim), &kmap, 0, 0, pg,
-                        bar(X_FULL + st));
-            bulk_g2s(sb + uint32_t(kIxOffSc) + uint32_t(st * kIxTile * 4 + g * P * 4),
-                     p.cache + int64_t(pg) * P * (kIxDim + 4) + int64_t(P) * kIxDim, uint32_t(P) * 4u,
-                     bar(X_FULL + st));
-          }
+      if (lane == 0 && x.r != rq) {  // q and weights of the request, once the previous ones are unused
+        if (qloads > 0 && !mbar_wait(bar(X_QFREE), (qloads - 1) & 1)) ok = false;
+        if (ok) {
+          mbar_arrive_expect_tx(bar(X_QFULL), uint32_t(N) * kIxDim + uint32_t(N) * 4u);
+          tma_load_2d(sb + uint32_t(kIxOffQ), &qmap, 0, x.r * N, bar(X_QFULL));
+          bulk_g2s(sb + uint32_t(kIxOffW), p.weights + int64_t(x.r) * N, uint32_t(N) * 4u, bar(X_QFULL));
+          ++qloads;
+          rq = x.r;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      u = __shfl_sync(0xffffffffu, u, 0);
       qloads = __shfl_sync(0xffffffffu, qloads, 0);
       rq = __shfl_sync(0xffffffffu, rq, 0);
+      // The whole warp issues a tile's copies: lane g checks page g of the tile and, when it is
+      // valid, issues its 3-D load and its scales' copy, all in one instruction each.
+      const int ctx = ctx_of(x.r);
+      const int nt = tiles_of(x);
+      for (int j = 0; j < nt && ok; ++j, ++u) {
+        const int st = u % kIxStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(X_EMPTY + st), ((u / kIxStages) & 1) ^ 1))) {
+          ok = false;
+          break;
+        }
+        // pages outside the request's table or the pool are not fetched: their rows keep
+        // stale bytes, which only feed logits beyond the visible range or flagged ones
+        const int li = j * npg + lane;
+        const int32_t pg = lane < npg ? spg[buf * 64 + li] : -1;
+        const bool valid = lane < npg && pg >= 0 && pg < p.num_pages;
+        if (lane < npg && !valid && ((x.c * ppi + li) << p.log2_page) < ctx)  // a page the visible context needs
+          atomicOr(p.err, SMLA_DEVERR_PAGE);
+        const uint32_t mask = __ballot_sync(0xffffffffu, valid);
+        if (lane == 0) mbar_arrive_expect_tx(bar(X_FULL + st), uint32_t(__popc(mask)) * uint32_t(P) * (kIxDim + 4));
+        __syncwarp();
+        if (valid) {
+          tma_load_3d(sb + uint32_t(kIxOffK + st * kIxStageK) + uint32_t(lane * P * kIxDim), &kmap, 0, 0, pg,
+                      bar(X_FULL + st));
+          bulk_g2s(sb + uint32_t(kIxOffSc) + uint32_t(st * kIxTile * 4 + lane * P * 4),
+                   p.cache + int64_t(pg) * P * (kIxDim + 4) + int64_t(P) * kIxDim, uint32_t(P) * 4u,
+                   bar(X_FULL + st));
+        }
+      }
     }
     cp_async_wait<0>();
     // no copy may land after the CTA has left
@@ -347,31 +362,12 @@ __global__ void __launch_bounds__(kIxThreads, 1)
           tc::ld32(lrow + uint32_t(b * N + i * p.H), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
           if (p.H > 32) tc::ld32(lrow + uint32_t(b * N + i * p.H + 32), *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           tc::wait_ld();
-          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // four independent chains
-          if (pos) {
-#pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-              if (e >= p.H) break;
-              const float4 w4 = lds_f32x4(wsm + uint32_t(i * p.H + e) * 4u);
-              a0 = fmaf(w4.x, fmaxf(0.f, __uint_as_float(v[e])), a0);
-              a1 = fmaf(w4.y, fmaxf(0.f, __uint_as_float(v[e + 1])), a1);
-              a2 = fmaf(w4.z, fmaxf(0.f, __uint_as_float(v[e + 2])), a2);
-              a3 = fmaf(w4.w, fmaxf(0.f, __uint_as_float(v[e + 3])), a3);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-              if (e >= p.H) break;
-              const float4 w4 = lds_f32x4(wsm + uint32_t(i * p.H + e) * 4u);
-              a0 = fmaf(w4.x, fmaxf(0.f, sgn * __uint_as_float(v[e])), a0);
-              a1 = fmaf(w4.y, fmaxf(0.f, sgn * __uint_as_float(v[e + 1])), a1);
-              a2 = fmaf(w4.z, fmaxf(0.f, sgn * __uint_as_float(v[e + 2])), a2);
-              a3 = fmaf(w4.w, fmaxf(0.f, sgn * __uint_as_float(v[e + 3])), a3);
-            }
-          }
+          const uint32_t w_row = wsm + uint32_t(i * p.H) * 4u;
+          const float hs = p.H == 64 ? (pos ? head_sum<64, true>(v, w_row, sgn) : head_sum<64, false>(v, w_row, sgn))
+                                     : (pos ? head_sum<32, true>(v, w_row, sgn) : head_sum<32, false>(v, w_row, sgn));
           const int vis = ctx - nn + 1 + i;
           const int t = x.r * nn + i;
-          if (s < vis) p.logits[int64_t(t) * p.logits_stride + s] = asc * ((a0 + a1) + (a2 + a3));
+          if (s < vis) p.logits[int64_t(t) * p.logits_stride + s] = asc * hs;
         }
         tc::fence_before();
         __syncwarp();
