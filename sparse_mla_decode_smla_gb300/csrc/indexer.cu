@@ -27,15 +27,22 @@
 // Every wait is bounded; a wait that gives up sets SMLA_DEVERR_TIMEOUT.
 //
 // indexer_topk_kernel: one CTA of 1024 threads per token, radix select over the token's visible
-// logits (keys made order-preserving as unsigned 32-bit integers; three passes of 11, 11 and
-// 10 bits with shared-memory histograms, eight loads in flight per thread) to the K-th largest
-// value; then each warp counts the keys above and equal to it in its contiguous segment, the
-// counts are scanned across warps, and each warp writes every index above the threshold and,
-// among indices equal to it, the lowest ones up to K: the top-k set in ascending index order.
+// logits (keys made order-preserving as unsigned 32-bit integers) to the K-th largest value:
+//  * pass 0 histograms bits [31:20] of every key (eight loads in flight per thread) and finds
+//    the bin holding the K-th largest;
+//  * pass 1 has each warp read its contiguous segment: it counts the keys above that bin and
+//    gathers the bin's keys, with their indices, into shared memory;
+//  * bits [19:10] and [9:0] are then selected among the gathered keys, whose counts above and
+//    equal to the threshold join their segments' counts (when the bin holds more keys than the
+//    buffer, these two passes and the counts read global memory instead);
+//  * the counts are scanned across warps, and each warp writes every index above the threshold
+//    and, among indices equal to it, the lowest ones up to K: the top-k set in ascending index
+//    order.
+// Three passes over a token's logits, not five.
 //
 // The producer warp prefetches the next item's page-table entries into shared memory by
-// cp.async while lane 0 issues the current item's copies, and the epilogue hands a stage back
-// as soon as it has read the stage's key scales.
+// cp.async and issues each tile's copies with one lane per page, and the epilogue hands a
+// stage back as soon as it has read the stage's key scales.
 #include <math_constants.h>
 #include <string.h>
 
@@ -394,6 +401,8 @@ __global__ void __launch_bounds__(kIxThreads, 1)
 constexpr int kTkThreads = 1024;
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kTkUnroll = 8;  // independent loads in flight per thread
+constexpr int kTkCand = 12288;  // keys of the threshold bin held in shared memory (with their indices)
+constexpr size_t kTkSmem = size_t(kTkCand) * 8;  // dynamic shared memory of the top-k kernel
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f);
@@ -401,9 +410,12 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerArgs p) {
-  __shared__ uint32_t hist[2048];
-  __shared__ uint32_t s_need, s_sel;
+  __shared__ uint32_t hist[4096];
+  __shared__ uint32_t s_need, s_sel, s_ncand;
   __shared__ uint32_t wgt[kTkWarps], weq[kTkWarps];
+  extern __shared__ uint32_t tk_dyn[];
+  uint32_t* cand_key = tk_dyn;                                     // [kTkCand]
+  int32_t* cand_idx = reinterpret_cast<int32_t*>(tk_dyn + kTkCand);  // [kTkCand]
   const int t = blockIdx.x;
   const int r = t / p.next_n;
   const int i = t - r * p.next_n;
@@ -416,25 +428,24 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
     for (int j = tid; j < p.K; j += kTkThreads) out[j] = j < vis ? j : -1;
     return;
   }
-  // radix select of the K-th largest key: bits [31:21], [20:10], [9:0]
-  uint32_t prefix = 0, need = uint32_t(p.K);
-#pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int width = pass == 2 ? 10 : 11;
-    const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0), nb = 1 << width;
-    const uint32_t hmask = pass == 0 ? 0u : (0xffffffffu << (sh + width));
+  // Histogram of the keys' bits [sh, sh + width) among those whose higher bits equal prefix,
+  // then the bin holding the need-th largest key: s_sel, and s_need = how many keys of that bin
+  // complete the set. `key_at(j)` gives key j of `count`.
+  auto select = [&](auto key_at, int count, uint32_t prefix, int sh, int width, uint32_t need) {
+    const int nb = 1 << width;
+    const uint32_t hmask = sh + width >= 32 ? 0u : (0xffffffffu << (sh + width));
     for (int k = tid; k < nb; k += kTkThreads) hist[k] = 0;
     __syncthreads();
-    for (int s0 = tid; s0 < vis; s0 += kTkThreads * kTkUnroll) {
+    for (int s0 = tid; s0 < count; s0 += kTkThreads * kTkUnroll) {
       uint32_t key[kTkUnroll];
 #pragma unroll
       for (int k = 0; k < kTkUnroll; ++k) {
         const int s = s0 + k * kTkThreads;
-        key[k] = s < vis ? order_key(__ldg(lg + s)) : 0u;
+        key[k] = s < count ? key_at(s) : 0u;
       }
 #pragma unroll
       for (int k = 0; k < kTkUnroll; ++k)
-        if (s0 + k * kTkThreads < vis && (key[k] & hmask) == prefix) atomicAdd(&hist[(key[k] >> sh) & (nb - 1)], 1u);
+        if (s0 + k * kTkThreads < count && (key[k] & hmask) == prefix) atomicAdd(&hist[(key[k] >> sh) & (nb - 1)], 1u);
     }
     __syncthreads();
     if (warp == 0) {  // walk the bins from the top until `need` is reached
@@ -462,31 +473,98 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
       }
     }
     __syncthreads();
-    prefix |= s_sel << sh;
-    need = s_need;
-    __syncthreads();
-  }
-  // prefix is the K-th largest key; `need` keys equal to it complete the set (the lowest
-  // indices among them). Warp w owns the contiguous segment [w seg, (w + 1) seg): it counts
-  // its keys above and equal to the threshold, the counts are scanned across warps, and then
-  // every warp writes its selected indices in order (ballots within 32-slot chunks).
+  };
+  auto global_key = [&](int s) { return order_key(__ldg(lg + s)); };
+
+  // pass 0: bits [31:20] of every visible key
+  select(global_key, vis, 0u, 20, 12, uint32_t(p.K));
+  const uint32_t sel0 = s_sel;
+  uint32_t need = s_need;
+  // pass 1 over each warp's contiguous segment [w seg, (w + 1) seg): count the keys above the
+  // threshold bin, and gather the bin's keys (and their indices) into shared memory
   const int seg = (vis + kTkWarps - 1) / kTkWarps;
   const int a0 = min(vis, warp * seg), a1 = min(vis, a0 + seg);
-  uint32_t ngt = 0, neq = 0;
+  if (tid == 0) s_ncand = 0;
+  __syncthreads();
+  uint32_t ngt = 0;
   for (int s0 = a0; s0 < a1; s0 += 32 * kTkUnroll) {
     uint32_t key[kTkUnroll];
 #pragma unroll
     for (int k = 0; k < kTkUnroll; ++k) {
       const int s = s0 + 32 * k + lane;
-      key[k] = s < a1 ? order_key(__ldg(lg + s)) : 0u;
+      key[k] = s < a1 ? global_key(s) : 0u;
     }
 #pragma unroll
     for (int k = 0; k < kTkUnroll; ++k) {
-      const bool in = s0 + 32 * k + lane < a1;
-      ngt += __popc(__ballot_sync(0xffffffffu, in && key[k] > prefix));
-      neq += __popc(__ballot_sync(0xffffffffu, in && key[k] == prefix));
+      const int s = s0 + 32 * k + lane;
+      const bool in = s < a1;
+      ngt += __popc(__ballot_sync(0xffffffffu, in && (key[k] >> 20) > sel0));
+      if (in && (key[k] >> 20) == sel0) {
+        const uint32_t c = atomicAdd(&s_ncand, 1u);
+        if (c < uint32_t(kTkCand)) {
+          cand_key[c] = key[k];
+          cand_idx[c] = s;
+        }
+      }
     }
   }
+  __syncthreads();
+  const int ncand = int(s_ncand);
+  uint32_t prefix = sel0 << 20;
+  uint32_t neq = 0;
+  if (ncand <= kTkCand) {
+    // passes 2 and 3 on the gathered keys of the bin
+    auto cand_key_at = [&](int c) { return cand_key[c]; };
+    select(cand_key_at, ncand, prefix, 10, 10, need);
+    prefix |= s_sel << 10;
+    need = s_need;
+    select(cand_key_at, ncand, prefix, 0, 10, need);
+    prefix |= s_sel;
+    need = s_need;
+    // the bin's keys above and equal to the threshold, into their warp segment's counts
+    if (tid < kTkWarps) {
+      wgt[tid] = 0;
+      weq[tid] = 0;
+    }
+    __syncthreads();
+    for (int c = tid; c < ncand; c += kTkThreads) {
+      const uint32_t key = cand_key[c];
+      const int owner = cand_idx[c] / seg;
+      if (key > prefix) atomicAdd(&wgt[owner], 1u);
+      else if (key == prefix) atomicAdd(&weq[owner], 1u);
+    }
+    __syncthreads();
+    ngt += wgt[warp];
+    neq = weq[warp];
+    __syncthreads();
+  } else {
+    // more keys in the bin than the buffer holds: passes 2 and 3 over global memory, then the
+    // segments' counts
+    select(global_key, vis, prefix, 10, 10, need);
+    prefix |= s_sel << 10;
+    need = s_need;
+    select(global_key, vis, prefix, 0, 10, need);
+    prefix |= s_sel;
+    need = s_need;
+    ngt = 0;
+    for (int s0 = a0; s0 < a1; s0 += 32 * kTkUnroll) {
+      uint32_t key[kTkUnroll];
+#pragma unroll
+      for (int k = 0; k < kTkUnroll; ++k) {
+        const int s = s0 + 32 * k + lane;
+        key[k] = s < a1 ? global_key(s) : 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < kTkUnroll; ++k) {
+        const bool in = s0 + 32 * k + lane < a1;
+        ngt += __popc(__ballot_sync(0xffffffffu, in && key[k] > prefix));
+        neq += __popc(__ballot_sync(0xffffffffu, in && key[k] == prefix));
+      }
+    }
+  }
+  // prefix is the K-th largest key; `need` keys equal to it complete the set (the lowest
+  // indices among them). The segments' counts are scanned across warps, and then every warp
+  // writes its selected indices in order (ballots within 32-slot chunks).
   if (lane == 0) {
     wgt[warp] = ngt;
     weq[warp] = neq;
@@ -498,18 +576,26 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
     be += weq[w2];
   }
   const uint32_t below = (1u << lane) - 1u;
-  for (int s0 = a0; s0 < a1; s0 += 32) {
-    const int s = s0 + lane;
-    const uint32_t key = s < a1 ? order_key(__ldg(lg + s)) : 0u;
-    const bool gt = s < a1 && key > prefix, eq = s < a1 && key == prefix;
-    const uint32_t mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
-    const uint32_t rg = bg + __popc(mg & below), re = be + __popc(me & below);
-    // the output position: the selected keys before this one, "above" ones plus the admitted
-    // "equal" ones (the first `need` equal keys in index order are admitted)
-    if (gt) out[rg + min(re, need)] = s;
-    if (eq && re < need) out[rg + re] = s;
-    bg += __popc(mg);
-    be += __popc(me);
+  for (int s1 = a0; s1 < a1; s1 += 32 * kTkUnroll) {
+    uint32_t keys[kTkUnroll];  // eight 32-key chunks in flight, then taken in order
+#pragma unroll
+    for (int k = 0; k < kTkUnroll; ++k) {
+      const int s = s1 + 32 * k + lane;
+      keys[k] = s < a1 ? order_key(__ldg(lg + s)) : 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < kTkUnroll; ++k) {
+      const int s = s1 + 32 * k + lane;
+      const bool gt = s < a1 && keys[k] > prefix, eq = s < a1 && keys[k] == prefix;
+      const uint32_t mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
+      const uint32_t rg = bg + __popc(mg & below), re = be + __popc(me & below);
+      // the output position: the selected keys before this one, "above" ones plus the admitted
+      // "equal" ones (the first `need` equal keys in index order are admitted)
+      if (gt) out[rg + min(re, need)] = s;
+      if (eq && re < need) out[rg + re] = s;
+      bg += __popc(mg);
+      be += __popc(me);
+    }
   }
 }
 
@@ -536,7 +622,17 @@ cudaError_t launch_indexer_logits(const IndexerArgs& a, int num_sms, cudaStream_
 }
 
 cudaError_t launch_indexer_topk(const IndexerArgs& a, cudaStream_t s) {
-  indexer_topk_kernel<<<a.T, kTkThreads, 0, s>>>(a);
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (!(configured.load(std::memory_order_acquire) & bit) || !bit) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(indexer_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTkSmem));
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_release);
+  }
+  indexer_topk_kernel<<<a.T, kTkThreads, kTkSmem, s>>>(a);
   return cudaGetLastError();
 }
 
