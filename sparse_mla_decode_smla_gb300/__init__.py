@@ -127,7 +127,7 @@ def _stream(stream):
     if stream is None:
         import torch
         return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    return ctypes.c_void_p(int(stream))
+    return ctypes.c_void_p(int(getattr(stream, "cuda_stream", stream)))  # a torch stream or a handle
 
 
 def _check(fn: str, status: int):

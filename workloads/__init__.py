@@ -345,3 +345,24 @@ def make_store_inputs(n: int, seed: int, max_position: int = 4096, device="cpu")
     cos_sin = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)
     d = torch.device(device)
     return StoreInputs(latent.to(d), rope.to(d), weight.to(d), positions.to(d), cos_sin.to(d))
+
+
+def make_topk_variants(problem: Problem, n: int) -> list[torch.Tensor]:
+    """n further index sets of a problem [T, K] int32 (same contexts, pages and padding recipe as
+    its own: distinct request-local slots drawn uniformly from each token's visible prefix, in
+    random order, -1 tail), each from its own seeded generator: consecutive end-to-end steps
+    then gather different rows."""
+    w = problem.w
+    T, K = w.num_tokens, w.topk
+    out = []
+    for v in range(n):
+        g = _gen(problem.seed, 300 + v, problem.device)
+        topk = torch.full((T, K), -1, dtype=torch.int32)
+        for t in range(T):
+            r, i = divmod(t, w.next_n)
+            visible = int(problem.ctx[r]) - (w.next_n - 1) + i
+            nvalid = min(visible, K - w.tail_pad)
+            idx = torch.randperm(visible, generator=g, device=problem.device)[:nvalid]
+            topk[t, :nvalid] = idx.to(torch.int32).cpu()
+        out.append(topk)
+    return out
