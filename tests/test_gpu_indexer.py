@@ -217,3 +217,35 @@ def test_indexer_topk_feeds_the_decode():
     o = out.double().cpu().numpy()
     assert np.abs(o - ref["out"]).max() <= 1e-2
     assert np.abs(lse.double().cpu().numpy() - ref["lse"]).max() <= 1e-3
+
+
+def test_topk_threshold_bin_at_and_over_the_shared_buffer():
+    # 20,003 visible slots a token. The kernel gathers the keys of the threshold's 12-bit bin into
+    # a shared-memory buffer of 12,288; with more, its last two radix passes read global memory.
+    # Token 0: every key in one bin (values in [1, 1.125): one sign, exponent and top three
+    # mantissa bits). Token 1: exactly 12,288 keys in that bin, the rest below it. Token 2: one
+    # more. Given fp32 logits, each index set must equal the oracle's bit for bit.
+    w = W.small_variant(W.WORKLOADS[3], num_requests=3, ctx_lo=20003, ctx_hi=20003, topk=2048).replace(next_n=1)
+    p = W.make_problem(w)
+    ix = Indexer(p)
+    g = torch.Generator().manual_seed(11)
+    n = ix.stride
+    vals = 1.0 + torch.randint(0, 1 << 20, (w.num_tokens, n), generator=g).float() * 2.0 ** -23
+    vals[:, ::7] = 1.0  # ties at the bottom of the bin
+    vals[1, 12288:] = 0.25
+    vals[2, 12289:] = 0.25
+    ix.logits.copy_(vals.cuda())
+    smla.indexer_topk(ix.desc, ix.logits, ix.ix.ctx, ix.topk)
+    torch.cuda.synchronize()
+    ctx = ix.ix.ctx.cpu().numpy()
+    for t in range(w.num_tokens):
+        vis = IX.visible_len(ctx[t], 1, 0)
+        assert vis == 20003
+        ref = IX.topk_set(vals[t, :vis].double().numpy(), ix.K)
+        assert np.array_equal(ix.topk[t].cpu().numpy(), ref), t
+    # all keys equal (more than the buffer holds): the lowest K indices
+    ix.logits.fill_(2.5)
+    smla.indexer_topk(ix.desc, ix.logits, ix.ix.ctx, ix.topk)
+    torch.cuda.synchronize()
+    for t in range(w.num_tokens):
+        assert np.array_equal(ix.topk[t].cpu().numpy(), np.arange(ix.K)), t
