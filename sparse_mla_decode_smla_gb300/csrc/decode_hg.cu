@@ -525,8 +525,34 @@ __global__ void __launch_bounds__(kHgThreads, 1)
     auto raw_row = [&](uint32_t stage, int slot) -> uint32_t {
       return stage + uint32_t((slot >> 2) * kHgGroup + (slot & 3) * rstride);
     };
-    // RoPE jobs: dims [8rc, 8rc+8) of slot 16q + rslot, q = rq0 + k for k = 0, 1
-    const int rslot = dtid & 15, rc = (dtid >> 4) & 7, rq0 = 2 * (dtid >> 7);
+    // Jobs are placed so that every access phase of a warp (8 lanes for 16-byte accesses, 16 for
+    // 8-byte ones) meets distinct bank groups. Gathered rows sit four to a 128-byte aligned group
+    // at a 656- or 576-byte pitch, so a slot's bank offset is 16 (slot & 3) or 64 (slot & 1) bytes.
+    // Latent jobs: bytes [16ch, 16ch+16) of a slot, two per thread (k = 0, 1).
+    //  fp8_ds: slot lslot, ch = lch + k. A phase takes four slots whose slot & 3 and
+    //  (slot & 7) >> 1 both differ ({0,3,5,6} or {1,2,4,7}, + 8), each with two chunks 64 bytes
+    //  apart. The lanes of the upper chunk (hi) store their two 16-byte halves in the other
+    //  order, so the swizzled K-tile stores stay distinct as well. Both chunks of a thread lie in
+    //  one 128-dim block: one scale load.
+    //  per-tensor: slot lslot + 8k, ch = lch. A phase takes two slots of opposite parity, each
+    //  with four consecutive chunks.
+    // RoPE jobs: dims [8rc, 8rc+8) of slot 16q + rslot, q = rq0 + k for k = 0, 1, placed the same
+    // way for their loads (16 or 8 bytes) and their stores into the 64-byte swizzled RoPE block.
+    int lslot, lch, hi = 0, rslot, rc;
+    if constexpr (tens) {
+      lslot = 2 * (lane >> 3) + ((lane >> 2) & 1);
+      lch = 4 * (dtid >> 5) + (lane & 3);
+      rslot = 2 * ((dtid >> 4) & 7) + ((dtid >> 2) & 1);
+      rc = (dtid & 3) + 4 * ((dtid >> 3) & 1);
+    } else {
+      const int dw = dtid >> 5, ph = lane >> 3, jj = lane & 3;
+      hi = (lane >> 2) & 1;
+      lslot = 8 * (ph >> 1) + (((jj << 1) | (__popc(jj) & 1)) ^ (ph & 1));
+      lch = 8 * (dw >> 1) + 2 * (dw & 1) + 4 * hi;
+      rslot = dtid & 15;
+      rc = ((dtid >> 4) & 3) + 4 * (((dtid >> 2) ^ (dtid >> 6)) & 1);
+    }
+    const int rq0 = 2 * (dtid >> 7);
     for (int i = 0; i < ntiles && ok; ++i) {
       const int b = i & 1;
       const uint32_t kt = sb + uint32_t(kHgOffK) + uint32_t(b * kHgKLat);
@@ -539,15 +565,14 @@ __global__ void __launch_bounds__(kHgThreads, 1)
         // producers at once, and only the stores wait for PV(i-2) to release the K rows
         const uint32_t raw = sb + uint32_t(kHgOffRaw) + uint32_t(st * kHgRawStage);
         uint32_t o[2][8];
+        const float sc = tens ? 1.f : lds_f32(raw_row(raw, lslot) + kScaleOff + 4 * (lch >> 3));
+        const __half2 s2 = __float2half2_rn(sc);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          const int id = dtid + kHgDequantThreads * k;
-          const int slot = id & 15, ch = id >> 4;  // latent bytes [16ch, 16ch+16) of the stage's row
-          const uint32_t rrow = raw_row(raw, slot);
-          const uint4 v = lds128(rrow + 16 * ch);
-          const float sc = tens ? 1.f : lds_f32(rrow + kScaleOff + 4 * (ch >> 3));
+          const int slot = tens ? lslot + 8 * k : lslot, ch = tens ? lch : lch + k;
+          uint4 v = lds128(raw_row(raw, slot) + 16 * ch);
+          if (hi) v = make_uint4(v.z, v.w, v.x, v.y);  // o[k][0..3] then holds the upper half
           const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-          const __half2 s2 = __float2half2_rn(sc);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             uint32_t lo, hi;
@@ -587,17 +612,16 @@ __global__ void __launch_bounds__(kHgThreads, 1)
         if (i >= 2 && !mbar_wait(bar(H_K_FREE + 4 * b + q), ((i - 2) >> 1) & 1)) { ok = false; break; }
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          const int id = dtid + kHgDequantThreads * k;
-          const int slot = id & 15, ch = id >> 4;
+          const int slot = tens ? lslot + 8 * k : lslot, ch = tens ? lch : lch + k;
           // dims [16ch, 16ch+16): block ch/4 mod 4, low rows for ch < 16, high rows after
           const int rr = kHgN * (ch >> 4) + kHgSub * q + slot;
           const uint32_t row = kt + ((ch >> 2) & 3) * kHgPairBlk + rr * 128;
           const int c0 = 2 * (ch & 3);
           const uint32_t sw = rr & 7;
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + ((c0 ^ sw) << 4)), "r"(o[k][0]),
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + (((c0 + hi) ^ sw) << 4)), "r"(o[k][0]),
                        "r"(o[k][1]), "r"(o[k][2]), "r"(o[k][3]) : "memory");
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + (((c0 + 1) ^ sw) << 4)), "r"(o[k][4]),
-                       "r"(o[k][5]), "r"(o[k][6]), "r"(o[k][7]) : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + (((c0 + 1 - hi) ^ sw) << 4)),
+                       "r"(o[k][4]), "r"(o[k][5]), "r"(o[k][6]), "r"(o[k][7]) : "memory");
         }
       }
       if (!ok) break;
