@@ -400,7 +400,8 @@ __global__ void __launch_bounds__(kIxThreads, 1)
 
 constexpr int kTkThreads = 1024;
 constexpr int kTkWarps = kTkThreads / 32;
-constexpr int kTkUnroll = 8;  // independent loads in flight per thread
+constexpr int kTkUnroll = 8;  // independent 4-byte loads in flight per thread (global fallback passes)
+constexpr int kTkVec = 4;     // independent 16-byte loads in flight per thread
 constexpr int kTkCand = 12288;  // keys of the threshold bin held in shared memory (with their indices)
 constexpr size_t kTkSmem = size_t(kTkCand) * 8;  // dynamic shared memory of the top-k kernel
 
@@ -412,7 +413,7 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerArgs p) {
   __shared__ uint32_t hist[4096];
   __shared__ uint32_t s_need, s_sel, s_ncand;
-  __shared__ uint32_t wgt[kTkWarps], weq[kTkWarps];
+  __shared__ uint32_t wgt[kTkWarps], weq[kTkWarps], wsum[kTkWarps];
   extern __shared__ uint32_t tk_dyn[];
   uint32_t* cand_key = tk_dyn;                                     // [kTkCand]
   int32_t* cand_idx = reinterpret_cast<int32_t*>(tk_dyn + kTkCand);  // [kTkCand]
@@ -428,9 +429,65 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
     for (int j = tid; j < p.K; j += kTkThreads) out[j] = j < vis ? j : -1;
     return;
   }
+  // The visible row in three parts: `head` keys before the first 16-byte boundary, `nv` groups
+  // of four read as one 16-byte load each, and the tail after them. Warp w's segment is the
+  // contiguous index range [seg_lo(w), seg_lo(w + 1)): body groups [w gs, (w + 1) gs), with the
+  // head in warp 0's segment and the tail in the last warp's.
+  const int head = min(vis, int(((16u - (uint32_t(reinterpret_cast<uintptr_t>(lg)) & 15u)) & 15u) >> 2));
+  const int nv = (vis - head) >> 2;
+  const int body_end = head + 4 * nv;
+  const int gs = max(1, (nv + kTkWarps - 1) / kTkWarps);
+  const float4* lgv = reinterpret_cast<const float4*>(lg + head);
+  auto seg_lo = [&](int w) { return w == 0 ? 0 : (w >= kTkWarps ? vis : head + 4 * min(nv, w * gs)); };
+  auto owner = [&](int s) {
+    return s < head ? 0 : (s >= body_end ? kTkWarps - 1 : min(kTkWarps - 1, ((s - head) >> 2) / gs));
+  };
+  const int v_lo = min(nv, warp * gs), v_hi = min(nv, (warp + 1) * gs);  // my body groups
+
+  // The bin of hist[0, nb) holding the need-th largest key, counted from the top: s_sel, and
+  // s_need = how many keys of that bin complete the set. Thread j sums the nb / 1024 bins
+  // just below nb - (nb / 1024) j, the sums are scanned across the block in thread order, and
+  // the one thread whose bins hold the need-th key walks them.
+  auto find_bin = [&](int nb, uint32_t need) {
+    const int per = nb / kTkThreads;
+    const int top = nb - 1 - per * tid;
+    uint32_t c = 0;
+    for (int k = 0; k < per; ++k) c += hist[top - k];
+    uint32_t x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t v = wsum[lane];
+      uint32_t z = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, z, o);
+        if (lane >= o) z += y;
+      }
+      wsum[lane] = z - v;  // the warps before, exclusive
+    }
+    __syncthreads();
+    uint32_t acc = wsum[warp] + (x - c);
+    if (acc < need && acc + c >= need) {
+      for (int k = 0; k < per; ++k) {
+        const uint32_t h = hist[top - k];
+        if (acc + h >= need) {
+          s_sel = uint32_t(top - k);
+          s_need = need - acc;
+          break;
+        }
+        acc += h;
+      }
+    }
+    __syncthreads();
+  };
   // Histogram of the keys' bits [sh, sh + width) among those whose higher bits equal prefix,
-  // then the bin holding the need-th largest key: s_sel, and s_need = how many keys of that bin
-  // complete the set. `key_at(j)` gives key j of `count`.
+  // then find_bin. `key_at(j)` gives key j of `count`.
   auto select = [&](auto key_at, int count, uint32_t prefix, int sh, int width, uint32_t need) {
     const int nb = 1 << width;
     const uint32_t hmask = sh + width >= 32 ? 0u : (0xffffffffu << (sh + width));
@@ -448,65 +505,72 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
         if (s0 + k * kTkThreads < count && (key[k] & hmask) == prefix) atomicAdd(&hist[(key[k] >> sh) & (nb - 1)], 1u);
     }
     __syncthreads();
-    if (warp == 0) {  // walk the bins from the top until `need` is reached
-      uint32_t acc = 0;
-      bool found = false;
-      for (int b0 = nb - 32; b0 >= 0 && !found; b0 -= 32) {
-        const uint32_t c = hist[b0 + 31 - lane];  // lane 0 holds the highest bin of the group
-        uint32_t x = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        const uint32_t m = __ballot_sync(0xffffffffu, acc + x >= need);
-        if (m) {
-          const int l = __ffs(m) - 1;
-          const uint32_t before = __shfl_sync(0xffffffffu, x - c, l);
-          if (lane == 0) {
-            s_sel = uint32_t(b0 + 31 - l);
-            s_need = need - (acc + before);
-          }
-          found = true;
-        }
-        acc += __shfl_sync(0xffffffffu, x, 31);
-      }
-    }
-    __syncthreads();
+    find_bin(nb, need);
   };
   auto global_key = [&](int s) { return order_key(__ldg(lg + s)); };
 
   // pass 0: bits [31:20] of every visible key
-  select(global_key, vis, 0u, 20, 12, uint32_t(p.K));
+  for (int k = tid; k < 4096; k += kTkThreads) hist[k] = 0;
+  __syncthreads();
+  for (int v0 = tid; v0 < nv; v0 += kTkThreads * kTkVec) {
+    float4 f[kTkVec];
+#pragma unroll
+    for (int k = 0; k < kTkVec; ++k) {
+      const int v = v0 + k * kTkThreads;
+      f[k] = v < nv ? __ldg(lgv + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < kTkVec; ++k)
+      if (v0 + k * kTkThreads < nv) {
+        atomicAdd(&hist[order_key(f[k].x) >> 20], 1u);
+        atomicAdd(&hist[order_key(f[k].y) >> 20], 1u);
+        atomicAdd(&hist[order_key(f[k].z) >> 20], 1u);
+        atomicAdd(&hist[order_key(f[k].w) >> 20], 1u);
+      }
+  }
+  if (tid < head) atomicAdd(&hist[global_key(tid) >> 20], 1u);
+  if (tid < vis - body_end) atomicAdd(&hist[global_key(body_end + tid) >> 20], 1u);
+  __syncthreads();
+  find_bin(4096, uint32_t(p.K));
   const uint32_t sel0 = s_sel;
   uint32_t need = s_need;
-  // pass 1 over each warp's contiguous segment [w seg, (w + 1) seg): count the keys above the
-  // threshold bin, and gather the bin's keys (and their indices) into shared memory
-  const int seg = (vis + kTkWarps - 1) / kTkWarps;
-  const int a0 = min(vis, warp * seg), a1 = min(vis, a0 + seg);
+  // pass 1 over each warp's segment: count the keys above the threshold bin, and gather the
+  // bin's keys (and their indices) into shared memory
   if (tid == 0) s_ncand = 0;
   __syncthreads();
   uint32_t ngt = 0;
-  for (int s0 = a0; s0 < a1; s0 += 32 * kTkUnroll) {
-    uint32_t key[kTkUnroll];
-#pragma unroll
-    for (int k = 0; k < kTkUnroll; ++k) {
-      const int s = s0 + 32 * k + lane;
-      key[k] = s < a1 ? global_key(s) : 0u;
-    }
-#pragma unroll
-    for (int k = 0; k < kTkUnroll; ++k) {
-      const int s = s0 + 32 * k + lane;
-      const bool in = s < a1;
-      ngt += __popc(__ballot_sync(0xffffffffu, in && (key[k] >> 20) > sel0));
-      if (in && (key[k] >> 20) == sel0) {
-        const uint32_t c = atomicAdd(&s_ncand, 1u);
-        if (c < uint32_t(kTkCand)) {
-          cand_key[c] = key[k];
-          cand_idx[c] = s;
-        }
+  auto visit1 = [&](uint32_t key, int s, bool in) {  // warp-uniform call
+    ngt += __popc(__ballot_sync(0xffffffffu, in && (key >> 20) > sel0));
+    if (in && (key >> 20) == sel0) {
+      const uint32_t c = atomicAdd(&s_ncand, 1u);
+      if (c < uint32_t(kTkCand)) {
+        cand_key[c] = key;
+        cand_idx[c] = s;
       }
     }
+  };
+  if (warp == 0) visit1(lane < head ? global_key(lane) : 0u, lane, lane < head);
+  for (int g0 = v_lo; g0 < v_hi; g0 += 32 * kTkVec) {
+    float4 f[kTkVec];
+#pragma unroll
+    for (int k = 0; k < kTkVec; ++k) {
+      const int g = g0 + 32 * k + lane;
+      f[k] = g < v_hi ? __ldg(lgv + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < kTkVec; ++k) {
+      const int g = g0 + 32 * k + lane;
+      const bool in = g < v_hi;
+      const int s = head + 4 * g;
+      visit1(order_key(f[k].x), s, in);
+      visit1(order_key(f[k].y), s + 1, in);
+      visit1(order_key(f[k].z), s + 2, in);
+      visit1(order_key(f[k].w), s + 3, in);
+    }
+  }
+  if (warp == kTkWarps - 1) {
+    const int s = body_end + lane;
+    visit1(s < vis ? global_key(s) : 0u, s, s < vis);
   }
   __syncthreads();
   const int ncand = int(s_ncand);
@@ -529,9 +593,9 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
     __syncthreads();
     for (int c = tid; c < ncand; c += kTkThreads) {
       const uint32_t key = cand_key[c];
-      const int owner = cand_idx[c] / seg;
-      if (key > prefix) atomicAdd(&wgt[owner], 1u);
-      else if (key == prefix) atomicAdd(&weq[owner], 1u);
+      const int w = owner(cand_idx[c]);
+      if (key > prefix) atomicAdd(&wgt[w], 1u);
+      else if (key == prefix) atomicAdd(&weq[w], 1u);
     }
     __syncthreads();
     ngt += wgt[warp];
@@ -547,6 +611,7 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
     prefix |= s_sel;
     need = s_need;
     ngt = 0;
+    const int a0 = seg_lo(warp), a1 = seg_lo(warp + 1);
     for (int s0 = a0; s0 < a1; s0 += 32 * kTkUnroll) {
       uint32_t key[kTkUnroll];
 #pragma unroll
@@ -564,7 +629,7 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
   }
   // prefix is the K-th largest key; `need` keys equal to it complete the set (the lowest
   // indices among them). The segments' counts are scanned across warps, and then every warp
-  // writes its selected indices in order (ballots within 32-slot chunks).
+  // writes its selected indices in order (ballots within each chunk of 32 lanes).
   if (lane == 0) {
     wgt[warp] = ngt;
     weq[warp] = neq;
@@ -576,29 +641,61 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
     be += weq[w2];
   }
   const uint32_t below = (1u << lane) - 1u;
-  for (int s1 = a0; s1 < a1; s1 += 32 * kTkUnroll) {
-    uint32_t keys[kTkUnroll];  // eight 32-key chunks in flight, then taken in order
+  // one key a lane (the head and the tail): "above" keys go after the admitted "equal" ones
+  // before them; the first `need` equal keys in index order are admitted
+  auto emit1 = [&](uint32_t key, int s, bool in) {
+    const bool gt = in && key > prefix, eq = in && key == prefix;
+    const uint32_t mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
+    const uint32_t rg = bg + __popc(mg & below), re = be + __popc(me & below);
+    if (gt) out[rg + min(re, need)] = s;
+    if (eq && re < need) out[rg + re] = s;
+    bg += __popc(mg);
+    be += __popc(me);
+  };
+  if (warp == 0) emit1(lane < head ? global_key(lane) : 0u, lane, lane < head);
+  for (int g0 = v_lo; g0 < v_hi; g0 += 32 * kTkVec) {
+    float4 f[kTkVec];
 #pragma unroll
-    for (int k = 0; k < kTkUnroll; ++k) {
-      const int s = s1 + 32 * k + lane;
-      keys[k] = s < a1 ? order_key(__ldg(lg + s)) : 0u;
+    for (int k = 0; k < kTkVec; ++k) {
+      const int g = g0 + 32 * k + lane;
+      f[k] = g < v_hi ? __ldg(lgv + g) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int k = 0; k < kTkUnroll; ++k) {
-      const int s = s1 + 32 * k + lane;
-      const bool gt = s < a1 && keys[k] > prefix, eq = s < a1 && keys[k] == prefix;
-      const uint32_t mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
-      const uint32_t rg = bg + __popc(mg & below), re = be + __popc(me & below);
-      // the output position: the selected keys before this one, "above" ones plus the admitted
-      // "equal" ones (the first `need` equal keys in index order are admitted)
-      if (gt) out[rg + min(re, need)] = s;
-      if (eq && re < need) out[rg + re] = s;
-      bg += __popc(mg);
-      be += __popc(me);
+    for (int k = 0; k < kTkVec; ++k) {
+      // four keys a lane, lane-major: the keys before (lane, j) are every key of the lanes
+      // below and this lane's keys before j
+      const int g = g0 + 32 * k + lane;
+      const bool in = g < v_hi;
+      const uint32_t key[4] = {order_key(f[k].x), order_key(f[k].y), order_key(f[k].z), order_key(f[k].w)};
+      bool gt[4], eq[4];
+      uint32_t rg = bg, re = be, tg = 0, te = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        gt[j] = in && key[j] > prefix;
+        eq[j] = in && key[j] == prefix;
+        const uint32_t mg = __ballot_sync(0xffffffffu, gt[j]), me = __ballot_sync(0xffffffffu, eq[j]);
+        rg += __popc(mg & below);
+        re += __popc(me & below);
+        tg += __popc(mg);
+        te += __popc(me);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int s = head + 4 * g + j;
+        if (gt[j]) out[rg + min(re, need)] = s;
+        if (eq[j] && re < need) out[rg + re] = s;
+        rg += gt[j] ? 1u : 0u;
+        re += eq[j] ? 1u : 0u;
+      }
+      bg += tg;
+      be += te;
     }
   }
+  if (warp == kTkWarps - 1) {
+    const int s = body_end + lane;
+    emit1(s < vis ? global_key(s) : 0u, s, s < vis);
+  }
 }
-
 }  // namespace
 
 cudaError_t launch_indexer_logits(const IndexerArgs& a, int num_sms, cudaStream_t s) {

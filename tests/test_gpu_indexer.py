@@ -249,3 +249,29 @@ def test_topk_threshold_bin_at_and_over_the_shared_buffer():
     torch.cuda.synchronize()
     for t in range(w.num_tokens):
         assert np.array_equal(ix.topk[t].cpu().numpy(), np.arange(ix.K)), t
+
+
+@pytest.mark.parametrize("extra", [1, 3])
+def test_topk_rows_at_every_alignment(extra):
+    # a logits row stride that is not a multiple of four floats puts successive rows at each
+    # 4-byte offset from a 16-byte boundary (the kernel reads the aligned body 16 bytes at a time
+    # and the ends one key at a time); given fp32 logits the index sets must equal the oracle's
+    w = W.small_variant(W.WORKLOADS[3], num_requests=3, ctx_lo=2500, ctx_hi=9000, topk=512)
+    p = W.make_problem(w)
+    ix = Indexer(p, logits_stride=w.page_table_stride * w.page_size + extra)
+    g = torch.Generator().manual_seed(5)
+    vals = torch.randint(-30, 30, (w.num_tokens, ix.stride), generator=g).float() / 8  # ties
+    vals[1::3] = torch.randn(ix.stride, generator=g)                                   # distinct values
+    ix.logits.copy_(vals.cuda())
+    smla.indexer_topk(ix.desc, ix.logits, ix.ix.ctx, ix.topk)
+    torch.cuda.synchronize()
+    ctx = ix.ix.ctx.cpu().numpy()
+    offsets = set()
+    for t in range(w.num_tokens):
+        r, i = divmod(t, w.next_n)
+        n = IX.visible_len(ctx[r], w.next_n, i)
+        offsets.add((t * ix.stride) % 4)
+        ref = IX.topk_set(vals[t, :n].double().numpy(), ix.K)
+        want = np.concatenate([ref, -np.ones(ix.K - len(ref), dtype=np.int64)])
+        assert np.array_equal(ix.topk[t].cpu().numpy(), want), t
+    assert offsets == {0, 1, 2, 3}
