@@ -27,9 +27,10 @@
 // Every wait is bounded; a wait that gives up sets SMLA_DEVERR_TIMEOUT.
 //
 // indexer_topk_kernel: one CTA of 1024 threads per token, radix select over the token's visible
-// logits (keys made order-preserving as unsigned 32-bit integers) to the K-th largest value:
-//  * pass 0 histograms bits [31:20] of every key (eight loads in flight per thread) and finds
-//    the bin holding the K-th largest;
+// logits (keys made order-preserving as unsigned 32-bit integers, -0 equal to +0) to the K-th
+// largest value. The row is read 16 bytes at a time, but for up to three keys at each end:
+//  * pass 0 histograms bits [31:20] of every key and finds the bin holding the K-th largest by
+//    a scan across the whole block;
 //  * pass 1 has each warp read its contiguous segment: it counts the keys above that bin and
 //    gathers the bin's keys, with their indices, into shared memory;
 //  * bits [19:10] and [9:0] are then selected among the gathered keys, whose counts above and
@@ -37,7 +38,7 @@
 //    buffer, these two passes and the counts read global memory instead);
 //  * the counts are scanned across warps, and each warp writes every index above the threshold
 //    and, among indices equal to it, the lowest ones up to K: the top-k set in ascending index
-//    order.
+//    order (when no tie is cut, simply every key at or above the threshold).
 // Three passes over a token's logits, not five.
 //
 // The producer warp prefetches the next item's page-table entries into shared memory by
@@ -405,9 +406,12 @@ constexpr int kTkVec = 4;     // independent 16-byte loads in flight per thread
 constexpr int kTkCand = 12288;  // keys of the threshold bin held in shared memory (with their indices)
 constexpr size_t kTkSmem = size_t(kTkCand) * 8;  // dynamic shared memory of the top-k kernel
 
+// Order-preserving unsigned key of a float: the sign bit set for positive values, every bit
+// flipped for negative ones. -0 is taken as +0 first (x + 0 rounds -0 to +0 and changes no other
+// value), so equal values have equal keys.
 __device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  const uint32_t u = __float_as_uint(__fadd_rn(f, 0.f));
+  return u ^ (uint32_t(int32_t(u) >> 31) | 0x80000000u);
 }
 
 __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerArgs p) {
@@ -538,10 +542,11 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
   // bin's keys (and their indices) into shared memory
   if (tid == 0) s_ncand = 0;
   __syncthreads();
-  uint32_t ngt = 0;
-  auto visit1 = [&](uint32_t key, int s, bool in) {  // warp-uniform call
-    ngt += __popc(__ballot_sync(0xffffffffu, in && (key >> 20) > sel0));
-    if (in && (key >> 20) == sel0) {
+  const uint32_t bin_lo = sel0 << 20, bin_hi = bin_lo | 0xfffffu;
+  uint32_t ngt = 0;  // this lane's keys above the bin, summed over the warp after the pass
+  auto visit1 = [&](uint32_t key, int s, bool in) {
+    ngt += (in && key > bin_hi) ? 1u : 0u;
+    if (in && key - bin_lo <= 0xfffffu) {
       const uint32_t c = atomicAdd(&s_ncand, 1u);
       if (c < uint32_t(kTkCand)) {
         cand_key[c] = key;
@@ -572,6 +577,7 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
     const int s = body_end + lane;
     visit1(s < vis ? global_key(s) : 0u, s, s < vis);
   }
+  ngt = __reduce_add_sync(0xffffffffu, ngt);
   __syncthreads();
   const int ncand = int(s_ncand);
   uint32_t prefix = sel0 << 20;
@@ -635,12 +641,59 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
     weq[warp] = neq;
   }
   __syncthreads();
-  uint32_t bg = 0, be = 0;
-  for (int w2 = 0; w2 < warp; ++w2) {
-    bg += wgt[w2];
-    be += weq[w2];
+  uint32_t bg = 0, be = 0, eq_all = 0;
+  for (int w2 = 0; w2 < kTkWarps; ++w2) {
+    if (w2 < warp) {
+      bg += wgt[w2];
+      be += weq[w2];
+    }
+    eq_all += weq[w2];
   }
   const uint32_t below = (1u << lane) - 1u;
+  if (eq_all == need) {
+    // every key equal to the threshold is admitted (no tie is cut): the set is the keys at or
+    // above it. A lane's count of selected keys (0 to 4) is spread over three ballots, one a
+    // bit, so the lanes below are counted with three popcounts.
+    uint32_t base = bg + be;
+    if (warp == 0) {
+      const bool sel = lane < head && global_key(lane) >= prefix;
+      const uint32_t m = __ballot_sync(0xffffffffu, sel);
+      if (sel) out[base + __popc(m & below)] = lane;
+      base += __popc(m);
+    }
+    for (int g0 = v_lo; g0 < v_hi; g0 += 32 * kTkVec) {
+      float4 f[kTkVec];
+#pragma unroll
+      for (int k = 0; k < kTkVec; ++k) {
+        const int g = g0 + 32 * k + lane;
+        f[k] = g < v_hi ? __ldg(lgv + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < kTkVec; ++k) {
+        const int g = g0 + 32 * k + lane;
+        const bool in = g < v_hi;
+        const bool s0 = in && order_key(f[k].x) >= prefix, s1 = in && order_key(f[k].y) >= prefix;
+        const bool s2 = in && order_key(f[k].z) >= prefix, s3 = in && order_key(f[k].w) >= prefix;
+        const uint32_t c = uint32_t(s0) + uint32_t(s1) + uint32_t(s2) + uint32_t(s3);
+        const uint32_t b0 = __ballot_sync(0xffffffffu, c & 1u), b1 = __ballot_sync(0xffffffffu, c & 2u);
+        const uint32_t b2 = __ballot_sync(0xffffffffu, c & 4u);
+        uint32_t pos = base + __popc(b0 & below) + 2u * __popc(b1 & below) + 4u * __popc(b2 & below);
+        const int s = head + 4 * g;
+        if (s0) out[pos++] = s;
+        if (s1) out[pos++] = s + 1;
+        if (s2) out[pos++] = s + 2;
+        if (s3) out[pos] = s + 3;
+        base += __popc(b0) + 2u * __popc(b1) + 4u * __popc(b2);
+      }
+    }
+    if (warp == kTkWarps - 1) {
+      const int s = body_end + lane;
+      const bool sel = s < vis && global_key(s) >= prefix;
+      const uint32_t m = __ballot_sync(0xffffffffu, sel);
+      if (sel) out[base + __popc(m & below)] = s;
+    }
+    return;
+  }
   // one key a lane (the head and the tail): "above" keys go after the admitted "equal" ones
   // before them; the first `need` equal keys in index order are admitted
   auto emit1 = [&](uint32_t key, int s, bool in) {

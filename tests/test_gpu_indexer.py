@@ -275,3 +275,27 @@ def test_topk_rows_at_every_alignment(extra):
         want = np.concatenate([ref, -np.ones(ix.K - len(ref), dtype=np.int64)])
         assert np.array_equal(ix.topk[t].cpu().numpy(), want), t
     assert offsets == {0, 1, 2, 3}
+
+
+def test_topk_signed_zeros_are_one_value():
+    # -0.0 and +0.0 are the same value: where the K-th largest logit is zero, the zeros of either
+    # sign tie and the lowest indices are taken (the oracle's stable sort on values)
+    w = W.small_variant(W.WORKLOADS[3], num_requests=2, ctx_lo=1500, ctx_hi=4000, topk=300)
+    p = W.make_problem(w)
+    ix = Indexer(p)
+    g = torch.Generator().manual_seed(9)
+    shape = (w.num_tokens, ix.stride)
+    zeros = torch.where(torch.rand(shape, generator=g) < 0.5, torch.tensor(-0.0), torch.tensor(0.0))
+    vals = torch.where(torch.rand(shape, generator=g) < 0.03, torch.tensor(1.0), zeros)
+    vals[:, 7] = -1.0
+    assert (torch.signbit(vals) & (vals == 0)).any()
+    ix.logits.copy_(vals.cuda())
+    smla.indexer_topk(ix.desc, ix.logits, ix.ix.ctx, ix.topk)
+    torch.cuda.synchronize()
+    ctx = ix.ix.ctx.cpu().numpy()
+    for t in range(w.num_tokens):
+        r, i = divmod(t, w.next_n)
+        n = IX.visible_len(ctx[r], w.next_n, i)
+        ref = IX.topk_set(vals[t, :n].double().numpy(), ix.K)
+        assert (vals[t, :n] == 1.0).sum() < ix.K  # the threshold is zero
+        assert np.array_equal(ix.topk[t].cpu().numpy(), ref), t
