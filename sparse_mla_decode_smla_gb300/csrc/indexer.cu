@@ -421,14 +421,37 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const IndexerA
   extern __shared__ uint32_t tk_dyn[];
   uint32_t* cand_key = tk_dyn;                                     // [kTkCand]
   int32_t* cand_idx = reinterpret_cast<int32_t*>(tk_dyn + kTkCand);  // [kTkCand]
-  const int t = blockIdx.x;
-  const int r = t / p.next_n;
-  const int i = t - r * p.next_n;
-  int32_t* out = p.topk + int64_t(t) * p.K;
-  const int ctx = min(__ldg(p.ctx + r), min(p.stride << p.log2_page, p.logits_stride));
-  const int vis = max(0, ctx - p.next_n + 1 + i);
-  const float* lg = p.logits + int64_t(t) * p.logits_stride;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cap = min(p.stride << p.log2_page, p.logits_stride);
+  auto visible = [&](int tt) {
+    const int rr = tt / p.next_n;
+    return max(0, min(__ldg(p.ctx + rr), cap) - p.next_n + 1 + (tt - rr * p.next_n));
+  };
+  // Longest rows first (when the tokens take more than one wave of CTAs): CTA b takes the
+  // token whose visible length ranks b-th (ties by index), so the rows that take longest start
+  // in the first wave and the short ones fill in behind them. Each CTA ranks the lengths in the
+  // shared memory the candidate buffer uses later.
+  int t = blockIdx.x;
+  if (p.longest_first && p.T <= kTkRankMax) {
+    int* len = reinterpret_cast<int*>(tk_dyn);
+    for (int k = tid; k < p.T; k += kTkThreads) len[k] = visible(k);
+    __syncthreads();
+    for (int k = tid; k < p.T; k += kTkThreads) {
+      const int lk = len[k];
+      int rank = 0;
+      for (int j = 0; j < p.T; ++j) {
+        const int lj = len[j];
+        rank += (lj > lk || (lj == lk && j < k)) ? 1 : 0;
+      }
+      if (rank == int(blockIdx.x)) s_sel = uint32_t(k);
+    }
+    __syncthreads();
+    t = int(s_sel);
+    __syncthreads();  // s_sel is reused below
+  }
+  const int vis = visible(t);
+  int32_t* out = p.topk + int64_t(t) * p.K;
+  const float* lg = p.logits + int64_t(t) * p.logits_stride;
   if (vis <= p.K) {  // every visible slot, then padding
     for (int j = tid; j < p.K; j += kTkThreads) out[j] = j < vis ? j : -1;
     return;

@@ -91,6 +91,9 @@ struct IndexerArgs {
   int32_t* err;             // device error word
   int32_t T, H, B, next_n, stride, log2_page, logits_stride, K;
   int64_t num_pages;
+  // top-k: CTA b takes the token with the b-th longest visible row (ties by index) instead of
+  // token b; worth it when the tokens take more than one wave of CTAs
+  int32_t longest_first;
 };
 // Tensor map of the index-key cache as [num_pages][P][128] bytes with [1 x P x 128] boxes,
 // 128-byte swizzle; of q as [T H rows, 128] bytes with [H next_n x 128] boxes, 128-byte swizzle.
@@ -98,6 +101,9 @@ cudaError_t index_key_map(const IndexerArgs& a, CUtensorMap* out);
 cudaError_t index_q_map(const IndexerArgs& a, CUtensorMap* out);
 cudaError_t launch_indexer_logits(const IndexerArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_indexer_topk(const IndexerArgs& a, cudaStream_t s);
+// Batches up to this many tokens may take the top-k's longest-row-first order (each CTA ranks
+// every row's length, so the cost grows with the square of the batch).
+constexpr int kTkRankMax = 512;
 cudaError_t launch_selftest_wait(int32_t* err, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace smla

@@ -452,6 +452,8 @@ smla_status smla_indexer_topk(const smla_indexer_desc* d, const float* logits, c
   smla::IndexerArgs a = make_indexer_args(d, context_lens);
   a.logits = const_cast<float*>(logits);
   a.topk = topk;
+  // one CTA a token and an SM: with more tokens than SMs, the longest rows go first
+  a.longest_first = d->num_tokens > sms && d->num_tokens <= smla::kTkRankMax ? 1 : 0;
   if (smla::launch_indexer_topk(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;
 }

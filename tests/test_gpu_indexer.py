@@ -299,3 +299,26 @@ def test_topk_signed_zeros_are_one_value():
         ref = IX.topk_set(vals[t, :n].double().numpy(), ix.K)
         assert (vals[t, :n] == 1.0).sum() < ix.K  # the threshold is zero
         assert np.array_equal(ix.topk[t].cpu().numpy(), ref), t
+
+
+def test_topk_more_tokens_than_sms_longest_first():
+    # more tokens than SMs: the kernel takes the longest rows first (CTA b serves the token with
+    # the b-th longest row); every token's index set must still equal the oracle's, given the
+    # same fp32 logits
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    w = W.small_variant(W.WORKLOADS[3], num_requests=sms + 48, ctx_lo=2100, ctx_hi=9000, topk=2048).replace(next_n=1)
+    p = W.make_problem(w)
+    ix = Indexer(p)
+    g = torch.Generator().manual_seed(13)
+    vals = torch.randint(-200, 200, (w.num_tokens, ix.stride), generator=g).float() / 16  # ties
+    ix.logits.copy_(vals.cuda())
+    smla.indexer_topk(ix.desc, ix.logits, ix.ix.ctx, ix.topk)
+    torch.cuda.synchronize()
+    ctx = ix.ix.ctx.cpu().numpy()
+    assert w.num_tokens > sms and len(set(ctx.tolist())) > 1
+    got = ix.topk.cpu().numpy()
+    for t in range(w.num_tokens):
+        n = IX.visible_len(ctx[t], 1, 0)
+        ref = IX.topk_set(vals[t, :n].double().numpy(), ix.K)
+        want = np.concatenate([ref, -np.ones(ix.K - len(ref), dtype=np.int64)])
+        assert np.array_equal(got[t], want), t
