@@ -50,11 +50,41 @@
 #include <atomic>
 
 #include "common.cuh"
-#include "kernels.h"
+#include "indexer.h"
 #include "tcgen05.cuh"
 
 namespace smla {
 namespace {
+
+// Tensor map of the index-key cache as [num_pages][P][128] bytes with [1 x P x 128] boxes,
+// 128-byte swizzle; of q as [T H rows, 128] bytes with [H next_n x 128] boxes, 128-byte swizzle.
+cudaError_t index_key_map(const IndexerArgs& a, CUtensorMap* out) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (tensor_map_encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
+  const cuuint64_t P = cuuint64_t(1) << a.log2_page;
+  const cuuint64_t dims[3] = {128, P, cuuint64_t(a.num_pages)};
+  const cuuint64_t strides[2] = {128, P * 132};
+  const cuuint32_t box[3] = {128, cuuint32_t(P), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.cache), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t index_q_map(const IndexerArgs& a, CUtensorMap* out) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (tensor_map_encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {128, cuuint64_t(a.T) * a.H};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, cuuint32_t(a.H * a.next_n)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.q), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 
 constexpr int kIxDim = 128;              // index dims (bytes of E4M3 per key or q row)
 constexpr int kIxTile = 128;             // slots per tile (the MMA's M)

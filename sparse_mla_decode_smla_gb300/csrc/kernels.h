@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -54,6 +55,8 @@ cudaError_t launch_decode_hg_f8(const DecodeArgs& a, cudaStream_t s);
 // the last slot marks a masked row: caches must hold fewer slots than this.
 constexpr int64_t kMaxGatherSlots = (int64_t(1) << 31) - 1;
 int kv_row_bytes(int32_t kv_format);
+// The driver's cuTensorMapEncodeTiled, looked up once (no link against the driver library).
+cudaError_t tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* out);
 // Tensor map of the cache as [slots, row bytes / 8] 8-byte words with one-row boxes.
 cudaError_t kv_gather_map(const DecodeArgs& a, CUtensorMap* out);
 // Tensor map of q as [T H rows, 576] bf16 with [64 rows x 64 dims] boxes, 128-byte swizzle.
@@ -74,36 +77,6 @@ cudaError_t launch_store_normed(int32_t kv_format, int32_t scale_mode, float kv_
                                 const float* cos_sin, int64_t max_position, const int64_t* slot_mapping,
                                 int64_t n, void* kv, int64_t num_slots, int32_t* err, cudaStream_t s);
 
-// ------------------------------------------------------------------------------ indexer
-
-// Requests an indexer call may hold (the logits kernel keeps their schedule prefix in
-// shared memory).
-constexpr int kIxMaxRequests = 8192;
-
-struct IndexerArgs {
-  const uint8_t* q;         // [T, H, 128] E4M3 codes
-  const float* weights;     // [T, H] fp32
-  const uint8_t* cache;     // [num_pages, P * 132]: P x 128 E4M3 codes, then P fp32 scales
-  const int32_t* page_table;
-  const int32_t* ctx;       // [B] context lengths
-  float* logits;            // [T, logits_stride] fp32
-  int32_t* topk;            // [T, K] int32
-  int32_t* err;             // device error word
-  int32_t T, H, B, next_n, stride, log2_page, logits_stride, K;
-  int64_t num_pages;
-  // top-k: CTA b takes the token with the b-th longest visible row (ties by index) instead of
-  // token b; worth it when the tokens take more than one wave of CTAs
-  int32_t longest_first;
-};
-// Tensor map of the index-key cache as [num_pages][P][128] bytes with [1 x P x 128] boxes,
-// 128-byte swizzle; of q as [T H rows, 128] bytes with [H next_n x 128] boxes, 128-byte swizzle.
-cudaError_t index_key_map(const IndexerArgs& a, CUtensorMap* out);
-cudaError_t index_q_map(const IndexerArgs& a, CUtensorMap* out);
-cudaError_t launch_indexer_logits(const IndexerArgs& a, int num_sms, cudaStream_t s);
-cudaError_t launch_indexer_topk(const IndexerArgs& a, cudaStream_t s);
-// Batches up to this many tokens may take the top-k's longest-row-first order (each CTA ranks
-// every row's length, so the cost grows with the square of the batch).
-constexpr int kTkRankMax = 512;
 cudaError_t launch_selftest_wait(int32_t* err, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace smla

@@ -8,6 +8,7 @@
 #include <atomic>
 
 #include "../../include/smla.h"
+#include "indexer.h"
 #include "kernels.h"
 
 namespace {

@@ -8,9 +8,8 @@
 #include "kernels.h"
 
 namespace smla {
-namespace {
 
-cudaError_t encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
+cudaError_t tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -25,8 +24,6 @@ cudaError_t encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
   return cudaSuccess;
 }
 
-}  // namespace
-
 int kv_row_bytes(int32_t kv_format) {
   return kv_format == SMLA_KV_FP8_TENSOR ? kFp8TensorRowBytes
                                          : (kv_format == SMLA_KV_FP8_DS ? kFp8RowBytes : kBf16RowBytes);
@@ -34,7 +31,7 @@ int kv_row_bytes(int32_t kv_format) {
 
 cudaError_t kv_gather_map(const DecodeArgs& a, CUtensorMap* out) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
+  if (tensor_map_encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
   thread_local const void* last_kv = nullptr;
   thread_local int64_t last_slots = -1;
   thread_local int32_t last_fmt = -1;
@@ -65,7 +62,7 @@ cudaError_t kv_gather_map(const DecodeArgs& a, CUtensorMap* out) {
 
 cudaError_t q_tile_map(const DecodeArgs& a, CUtensorMap* out) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
+  if (tensor_map_encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
   thread_local const void* last_q = nullptr;
   thread_local int64_t last_rows = -1;
   thread_local CUtensorMap last_map;
@@ -90,7 +87,7 @@ cudaError_t q_tile_map(const DecodeArgs& a, CUtensorMap* out) {
 
 cudaError_t q_e4m3_maps(const DecodeArgs& a, CUtensorMap* map128, CUtensorMap* map32) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
+  if (tensor_map_encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {cuuint64_t(kDim), cuuint64_t(int64_t(a.T) * a.H)};
   const cuuint64_t strides[1] = {cuuint64_t(kDim)};
   const cuuint32_t estr[2] = {1, 1};
@@ -103,33 +100,6 @@ cudaError_t q_e4m3_maps(const DecodeArgs& a, CUtensorMap* map128, CUtensorMap* m
   r = encode(map32, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.q), dims, strides, box32, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-cudaError_t index_key_map(const IndexerArgs& a, CUtensorMap* out) {
-  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
-  const cuuint64_t P = cuuint64_t(1) << a.log2_page;
-  const cuuint64_t dims[3] = {128, P, cuuint64_t(a.num_pages)};
-  const cuuint64_t strides[2] = {128, P * 132};
-  const cuuint32_t box[3] = {128, cuuint32_t(P), 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.cache), dims, strides, box,
-                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-cudaError_t index_q_map(const IndexerArgs& a, CUtensorMap* out) {
-  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (encoder(&encode) != cudaSuccess) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {128, cuuint64_t(a.T) * a.H};
-  const cuuint64_t strides[1] = {128};
-  const cuuint32_t box[2] = {128, cuuint32_t(a.H * a.next_n)};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.q), dims, strides, box,
-                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
