@@ -339,8 +339,8 @@ smla_status smla_indexer_logits(const smla_indexer_desc* d, const void* q, const
 /*
  * Top-k of the indexer logits: topk [T, K] int32 receives, for token t, the request-local
  * indices of its K largest visible logits in ascending index order; at a tie on the K-th
- * value the lowest indices are taken. With fewer than K visible slots the row is 0, 1, ...,
- * visible - 1, then -1 padding: the topk_indices argument of smla_decode.
+ * value the lowest indices are taken (-0 and +0 are one value). With fewer than K visible slots
+ * the row is 0, 1, ..., visible - 1, then -1 padding: the topk_indices argument of smla_decode.
  *   logits [T, logits_stride] fp32 as smla_indexer_logits wrote them (only the visible
  *   part of each row is read); context_lens [B] int32 as given to that call.
  */
