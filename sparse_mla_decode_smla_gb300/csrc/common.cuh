@@ -201,6 +201,10 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // programmatic-serialization attribute) may start once every CTA of this grid has called
 // pdl_trigger or exited; it calls pdl_wait before touching this grid's results, which
 // returns once this grid has completed and its memory operations are visible.
+// Fetch a TMA descriptor (a kernel parameter) ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const void* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

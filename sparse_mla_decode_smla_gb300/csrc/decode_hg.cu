@@ -162,6 +162,9 @@ __global__ void __launch_bounds__(kHgThreads, 1)
   };
   const uint32_t mlse = sb + uint32_t(kHgOffK) + 72u * 1024u;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the two TMA descriptors, fetched before their first use (q's load, the first row gathers)
+  if (tid == 0) prefetch_tensormap(&q_map);
+  if (tid == 32 * kHgFirstProducer) prefetch_tensormap(&kv_map);
 
   // Per-tensor FP8 codes go into the K tile unscaled (exact in f16); kv_scale is applied in
   // fp32 to the scores (bmm1_scale = sm_scale * kv_scale) and to O (bmm2_scale = kv_scale),
@@ -1033,15 +1036,22 @@ cudaError_t launch_decode_hg(const DecodeArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(kHgThreads);
   cfg.dynamicSmemBytes = kSmemHg;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
   if (a.cluster_merge) {  // the splits of a (token, head group) share one cluster
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(a.num_splits);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = static_cast<unsigned>(a.num_splits);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
+  if (a.overlap_prev) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = na;
   if (a.kv_format == SMLA_KV_FP8_TENSOR) return cudaLaunchKernelEx(&cfg, decode_hg_kernel<true>, a, map, qmap);
   return cudaLaunchKernelEx(&cfg, decode_hg_kernel<false>, a, map, qmap);
 }

@@ -137,6 +137,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
   };
   const uint32_t mlse = sb + uint32_t(kFOffK) + 72u * 1024u;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the TMA descriptors, fetched before their first use (q's loads, the first row gathers)
+  if (tid == 0) {
+    prefetch_tensormap(&q_map128);
+    prefetch_tensormap(&q_map32);
+  }
+  if (tid == 32 * kFFirstProducer) prefetch_tensormap(&kv_map);
 
   // the codes' dot products take bmm1_scale = sm_scale * q_scale * kv_scale (times log2 e)
   const float c2 = p.c2 * p.q_scale * p.kv_scale;
@@ -841,15 +847,22 @@ cudaError_t launch_decode_hg_f8(const DecodeArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(kFThreads);
   cfg.dynamicSmemBytes = kSmemF8;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
   if (a.cluster_merge) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(a.num_splits);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = static_cast<unsigned>(a.num_splits);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
+  if (a.overlap_prev) {  // may start while the previous kernel drains (it reads none of its results)
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, decode_hg_f8_kernel, a, map, q128, q32);
 }
 

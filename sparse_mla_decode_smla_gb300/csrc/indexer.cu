@@ -159,6 +159,10 @@ __global__ void __launch_bounds__(kIxThreads, 1)
   auto bar = [&](int k) -> uint32_t { return sb + uint32_t(kIxOffBars) + 8u * k; };
   int32_t* pre = reinterpret_cast<int32_t*>(sm + kIxOffPre);  // pre[r] = items of requests < r
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {  // the TMA descriptors, fetched before their first use
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&qmap);
+  }
   const int N = p.H * p.next_n;
   const int P = 1 << p.log2_page;
 

@@ -40,6 +40,9 @@ struct DecodeArgs {
   // head-group kernels: this launch serves the (token, head group) items [item0, item0 +
   // nitems), nitems = 0 meaning all T x ceil(H / 64) of them
   int32_t item0, nitems;
+  // launched with programmatic stream serialisation: its CTAs may start while the previous
+  // kernel on the stream drains (nothing here reads what that kernel writes)
+  int32_t overlap_prev;
 };
 // Largest cluster the in-kernel split merge uses (the portable cluster size).
 constexpr int kMaxClusterMerge = 8;

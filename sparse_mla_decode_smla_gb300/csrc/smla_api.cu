@@ -306,6 +306,9 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
     last.num_splits = 2;
     last.split_len = ((d->topk + 1) / 2 + smla::kTile - 1) / smla::kTile * smla::kTile;
     last.cluster_merge = 1;
+    // the remainder's items are independent of the whole waves': its CTAs take SMs as the last
+    // wave's CTAs leave, with no launch gap in between
+    last.overlap_prev = 1;
     e = launch(full);
     if (e == cudaSuccess) e = launch(last);
   } else {
