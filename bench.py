@@ -61,12 +61,12 @@ def measured_peaks() -> dict:
 # saved or replayed), with the SHA-256 (first 16 hex digits) of that kernel's sources at capture
 # time. A capture of an older kernel (the hash differs) is not reported.
 TRAFFIC = {
-    ("fp8_mtp_T256_H128_K2048_ctx4k-128k_sink", "decode_hg_kernel"): (429982976, "b0d7a81a9cde63fb"),
-    ("fp8_T128_H128_K2048_ctx64k_sink", "decode_hg_kernel"): (231027200, "b0d7a81a9cde63fb"),
-    ("fp8_T32_H64_K2048_ctx1k-32k", "decode_hg_kernel"): (51804928, "b0d7a81a9cde63fb"),
-    ("fp8_T256_H16_K2048_ctx8k-128k_pad20", "decode_mma_kernel"): (334046976, "617676d8cfdce9e8"),
-    ("fp8tensor_mtp_T256_H128_K2048_ctx4k-128k_sink", "decode_hg_f8_kernel"): (341206016, "9480f86640d1b0ac"),
-    ("store_fp8_ds_rows65536_P64_pos131072", "pack_kernel"): (111881216, "9ba987719dc8967c"),
+    ("fp8_mtp_T256_H128_K2048_ctx4k-128k_sink", "decode_hg_kernel"): (430178560, "712d98fd6bd0621b"),
+    ("fp8_T128_H128_K2048_ctx64k_sink", "decode_hg_kernel"): (231365120, "712d98fd6bd0621b"),
+    ("fp8_T32_H64_K2048_ctx1k-32k", "decode_hg_kernel"): (51809536, "712d98fd6bd0621b"),
+    ("fp8_T256_H16_K2048_ctx8k-128k_pad20", "decode_mma_kernel"): (333995520, "8d7176b8a678685a"),
+    ("fp8tensor_mtp_T256_H128_K2048_ctx4k-128k_sink", "decode_hg_f8_kernel"): (340960512, "b4d9ea4a34fbf1e7"),
+    ("store_fp8_ds_rows65536_P64_pos131072", "pack_kernel"): (111933184, "e75a497c2046fc9b"),
 }
 KERNEL_SOURCES = {
     "decode_hg_kernel": ("common.cuh", "kernels.h", "tcgen05.cuh", "decode_hg.cu", "tensor_maps.cu"),
