@@ -4,23 +4,29 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace smla {
 
 cudaError_t tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (!encode) {
+  // looked up once; host threads that make their first call together look it up twice and
+  // store the same value
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> encode{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 f = encode.load(std::memory_order_acquire);
+  if (!f) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
             cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !fn)
       return cudaErrorNotSupported;
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    encode.store(f, std::memory_order_release);
   }
-  *out = encode;
+  *out = f;
   return cudaSuccess;
 }
 
