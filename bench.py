@@ -61,11 +61,11 @@ def measured_peaks() -> dict:
 # saved or replayed), with the SHA-256 (first 16 hex digits) of that kernel's sources at capture
 # time. A capture of an older kernel (the hash differs) is not reported.
 TRAFFIC = {
-    ("fp8_mtp_T256_H128_K2048_ctx4k-128k_sink", "decode_hg_kernel"): (430178560, "712d98fd6bd0621b"),
-    ("fp8_T128_H128_K2048_ctx64k_sink", "decode_hg_kernel"): (231365120, "712d98fd6bd0621b"),
-    ("fp8_T32_H64_K2048_ctx1k-32k", "decode_hg_kernel"): (51809536, "712d98fd6bd0621b"),
+    ("fp8_mtp_T256_H128_K2048_ctx4k-128k_sink", "decode_hg_kernel"): (429726464, "4f0b0b30b45adc0e"),
+    ("fp8_T128_H128_K2048_ctx64k_sink", "decode_hg_kernel"): (231280128, "4f0b0b30b45adc0e"),
+    ("fp8_T32_H64_K2048_ctx1k-32k", "decode_hg_kernel"): (51805440, "4f0b0b30b45adc0e"),
     ("fp8_T256_H16_K2048_ctx8k-128k_pad20", "decode_mma_kernel"): (333995520, "8d7176b8a678685a"),
-    ("fp8tensor_mtp_T256_H128_K2048_ctx4k-128k_sink", "decode_hg_f8_kernel"): (340960512, "b4d9ea4a34fbf1e7"),
+    ("fp8tensor_mtp_T256_H128_K2048_ctx4k-128k_sink", "decode_hg_f8_kernel"): (341052160, "0889268099627afb"),
     ("store_fp8_ds_rows65536_P64_pos131072", "pack_kernel"): (111933184, "e75a497c2046fc9b"),
 }
 KERNEL_SOURCES = {
