@@ -497,3 +497,18 @@ def test_tail_wave_split_launch():
     torch.cuda.synchronize()
     assert int(dd.workspace[0].item()) == 0
     assert_parity(out, lse, oracle_decode(p))
+    # the second launch may start while the first drains: calls back to back on one stream, with
+    # another batch's call in between into other buffers, give the same bits
+    ref_out, ref_lse = out.clone(), lse.clone()
+    w2 = W.small_variant(W.WORKLOADS[2], num_requests=T, ctx_lo=900, ctx_hi=900, topk=512)
+    dd2 = DeviceDecode(W.make_problem(w2))
+    for _ in range(3):
+        dd.run()
+        dd2.run()
+    torch.cuda.synchronize()
+    assert torch.equal(dd.out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(dd.lse, ref_lse)
+    out2, lse2 = dd2.out.clone(), dd2.lse.clone()
+    dd2.run()
+    torch.cuda.synchronize()
+    assert torch.equal(dd2.out.view(torch.int16), out2.view(torch.int16)) and torch.equal(dd2.lse, lse2)
