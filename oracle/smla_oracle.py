@@ -57,7 +57,10 @@ SCALE_FP32 = 1
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns (uint16) -> exact float64 values (bf16 is the top half of fp32)."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
-    return b.view(np.float32).astype(np.float64)
+    # Widening a signalling-NaN pattern quietens it, which NumPy reports as an
+    # invalid-value warning; the value stays NaN either way.
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
 
 
 def e4m3_decode(codes: np.ndarray) -> np.ndarray:
