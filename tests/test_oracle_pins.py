@@ -244,6 +244,9 @@ def test_physical_slots_invalid_entries_dropped_and_counted():
     keep, phys, bad = O.physical_slots(np.array([-5, 12, 4, 0, -1]), np.array([2, -1, 1]), 4, 3)
     # -5: negative non-padding; 12: beyond stride*P; 4: page entry -1; 0: page 2 -> slot 8
     assert keep == [3] and phys.tolist() == [8] and bad == 3
+    # a page entry equal to num_pages is one past the pool: 13 -> page entry 3 of a 3-page pool
+    keep, phys, bad = O.physical_slots(np.array([13, 9]), np.array([2, -1, 1, 3]), 4, 3)
+    assert keep == [1] and phys.tolist() == [5] and bad == 1
 
 
 # ----------------------------------------------------------------------------- attention
@@ -456,16 +459,20 @@ def test_rms_norm_closed_forms():
     a = O.rms_norm_bf16(_bits(x), _bits(wb), 0.0)
     b = O.rms_norm_bf16(_bits((x.double() * 4).to(torch.bfloat16)), _bits(wb), 0.0)
     assert np.array_equal(a, b)
+    # eps counts: a row of ones with eps = 3 gives y = w / sqrt(1 + 3) = w / 2, exactly
+    ones = np.ones((1, 512))
+    y = O.rms_norm_bf16(_bits(torch.tensor(ones).to(torch.bfloat16)), _bits(torch.tensor(w).to(torch.bfloat16)), 3.0)
+    assert np.array_equal(y[0], wq / 2)
 
 
 def test_rms_norm_matches_torch_float64():
     g = torch.Generator().manual_seed(7)
     x = torch.randn(16, 512, generator=g).to(torch.bfloat16)
     w = (1 + 0.1 * torch.randn(512, generator=g)).to(torch.bfloat16)
-    eps = 1e-6
-    ref = torch.nn.functional.rms_norm(x.double(), (512,), w.double(), eps=float(np.float32(eps)))
-    got = O.rms_norm_bf16(_bits(x), _bits(w), eps)
-    assert np.array_equal(got, O.bf16_rne(ref.numpy()))
+    for eps in (1e-6, 0.5):  # the second is of the order of mean(x^2), so it moves every output
+        ref = torch.nn.functional.rms_norm(x.double(), (512,), w.double(), eps=float(np.float32(eps)))
+        got = O.rms_norm_bf16(_bits(x), _bits(w), eps)
+        assert np.array_equal(got, O.bf16_rne(ref.numpy()))
 
 
 def test_rope_rotation_special_angles_and_complex_product():
@@ -488,11 +495,17 @@ def test_store_normed_rows_is_norm_rope_then_the_packer():
     g = torch.Generator().manual_seed(9)
     lat = torch.randn(5, 512, generator=g).to(torch.bfloat16)
     rope = torch.randn(5, 64, generator=g).to(torch.bfloat16)
-    w = torch.ones(512).to(torch.bfloat16)
-    cos, sin = np.ones((5, 32)), np.zeros((5, 32))
-    rows = O.store_normed_rows(_bits(lat), _bits(rope), _bits(w), 0.0, cos, sin, "fp8_ds")
-    normed = O.rms_norm_bf16(_bits(lat), _bits(w), 0.0)
-    assert np.array_equal(rows, O.pack_fp8_ds(O.f64_to_bf16_bits(normed), _bits(rope)))
+    w = (1 + 0.1 * torch.randn(512, generator=g)).to(torch.bfloat16)
+    eps = 0.25
+    # the norm by torch in float64, rounded to bf16 by torch
+    normed = torch.nn.functional.rms_norm(lat.double(), (512,), w.double(), eps=eps).to(torch.bfloat16)
+    # a quarter turn maps each pair (a, b) to (-b, a), exactly
+    turned = torch.stack([-rope[:, 1::2], rope[:, 0::2]], dim=2).reshape(5, 64)
+    cos, sin = np.zeros((5, 32)), np.ones((5, 32))
+    rows = O.store_normed_rows(_bits(lat), _bits(rope), _bits(w), eps, cos, sin, "fp8_ds")
+    assert np.array_equal(rows, O.pack_fp8_ds(_bits(normed), _bits(turned)))
+    rows = O.store_normed_rows(_bits(lat), _bits(rope), _bits(w), eps, cos, sin, "bf16")
+    assert np.array_equal(rows, O.pack_bf16(_bits(normed), _bits(turned)))
 
 
 # ----------------------------------------------------------------------------- FP8 q
