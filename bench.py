@@ -286,18 +286,12 @@ def reference_arm(args):
 # ------------------------------------------------------------------------------ GPU arm
 
 
-def decode_launches(w, dd, num_splits, num_sms) -> int:
-    """Kernel launches of one smla_decode call: the decode kernel; the merge kernel when the
-    workspace holds split partials; a second head-group launch when the library runs the last
-    partial wave's items as two splits each (library-chosen splits, one CTA per (token, 64
-    heads) filling whole waves plus at most half a wave, index rows of 512 or more)."""
-    n = 2 if dd.workspace.numel() * 4 > 256 else 1
-    units = w.num_tokens * ((w.num_heads + 63) // 64)
-    hg = w.kv_format in ("fp8_ds", "fp8_tensor") and w.num_heads >= 64
-    rem = units % num_sms
-    if hg and num_splits == 0 and w.topk >= 512 and units > num_sms and 0 < rem and 2 * rem <= num_sms:
-        n += 1
-    return n
+def decode_launches(smla, desc, num_sms) -> int:
+    """Kernel launches of one smla_decode call, from the library's own plan: one or two
+    decode launches (the second when the last partial wave runs as two splits per item),
+    plus the merge kernel when the split partials go through the workspace."""
+    p = smla.plan_launches(desc, num_sms)
+    return p.num_launches + (1 if p.merge == smla.SMLA_MERGE_KERNEL else 0)
 
 
 def gpu_arm(args):
@@ -323,7 +317,7 @@ def gpu_arm(args):
         dd.desc.q_format, dd.desc.q_scale = smla.SMLA_Q_FP8_E4M3, W.Q_SCALE_FP8
         dd.kernel_name = "decode_hg_f8_kernel"
     valid, kv_bytes, flops = algorithmic_work(problem)
-    launches_per_step = decode_launches(w, dd, args.num_splits, torch.cuda.get_device_properties(dev).multi_processor_count)
+    launches_per_step = decode_launches(smla, dd.desc, torch.cuda.get_device_properties(dev).multi_processor_count)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 

@@ -113,7 +113,7 @@ const char* smla_status_string(int32_t status);
 /* ABI version of this header (increments on any incompatible change; 2 added kv_scale,
  * 3 added SMLA_ERR_TIMEOUT, SMLA_ERR_OPERAND_RANGE, SMLA_DEVERR_RANGE,
  * smla_noalloc_read_error, the indexer calls and smla_store_kv_normed; 4 added q_format and
- * q_scale in place of two reserved words). */
+ * q_scale in place of two reserved words; 5 added smla_plan_launches). */
 int32_t smla_abi_version(void);
 
 /*
@@ -125,6 +125,46 @@ int32_t smla_abi_version(void);
  * Writes 0 into *bytes on error.
  */
 smla_status smla_workspace_size(const smla_desc* d, size_t* bytes);
+
+/* Decode kernels (smla_launch_plan.kernel). */
+enum {
+  SMLA_KERNEL_HEAD_GROUP = 1,      /* tcgen05, 16-bit operands: FP8 caches, 64-128 heads */
+  SMLA_KERNEL_HEAD_GROUP_FP8 = 2,  /* tcgen05, E4M3 operands: SMLA_Q_FP8_E4M3 */
+  SMLA_KERNEL_MMA = 3              /* mma.sync: 16-48 heads, or the bf16 cache */
+};
+
+/* How the split partials of one work item are merged (smla_launch_plan.merge). */
+enum {
+  SMLA_MERGE_NONE = 0,     /* one split: the decode kernel writes the output */
+  SMLA_MERGE_CLUSTER = 1,  /* inside the decode kernel, across its thread-block cluster */
+  SMLA_MERGE_KERNEL = 2    /* partials in the workspace, then a separate merge kernel */
+};
+
+typedef struct smla_launch_plan {
+  int32_t kernel;           /* SMLA_KERNEL_* */
+  int32_t num_splits;       /* top-k splits of each work item in the first launch */
+  int32_t split_len;        /* index entries a split covers (a multiple of 64; the last
+                               split of an item takes what is left) */
+  int32_t merge;            /* SMLA_MERGE_* of the first launch */
+  int32_t num_launches;     /* decode launches: 1, or 2 when the last partial wave runs apart */
+  int32_t ctas[2];          /* CTAs of each decode launch (ctas[1] = 0 with one launch) */
+  int32_t tail_items;       /* work items of the second launch, two splits each, merged
+                               across their cluster (0 with one launch) */
+  uint64_t workspace_bytes; /* the value smla_workspace_size gives on such a device */
+} smla_launch_plan;
+
+/*
+ * The launches smla_decode makes for `d` on a device with `num_sms` SMs (152 on GB300):
+ * which kernel, how the top-k list is split, and the CTAs of each launch. A work item is
+ * (token, group of 64 heads) for the head-group kernels and (token, 16 heads) for the
+ * mma.sync kernel; a CTA takes one split of one item. When the head-group items with one
+ * split fill whole waves of one CTA per SM plus a last wave at most half full, that last
+ * wave runs as a second launch with two splits per item, so it takes about half a CTA's
+ * time. Host-only: touches no device, launches nothing, and can be called without a GPU.
+ * Status: SMLA_ERR_NULL for a NULL argument, SMLA_ERR_SHAPE for num_sms < 1, else the
+ * status smla_decode's checks of `d` give; *plan is zeroed on error.
+ */
+smla_status smla_plan_launches(const smla_desc* d, int32_t num_sms, smla_launch_plan* plan);
 
 /*
  * Sparse MLA decode (the hot path).

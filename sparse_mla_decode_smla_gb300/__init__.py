@@ -23,6 +23,12 @@ SMLA_DEVERR_INDEX = 1
 SMLA_DEVERR_PAGE = 2
 SMLA_DEVERR_TIMEOUT = 4
 SMLA_DEVERR_RANGE = 8
+SMLA_KERNEL_HEAD_GROUP = 1
+SMLA_KERNEL_HEAD_GROUP_FP8 = 2
+SMLA_KERNEL_MMA = 3
+SMLA_MERGE_NONE = 0
+SMLA_MERGE_CLUSTER = 1
+SMLA_MERGE_KERNEL = 2
 
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_NULL", 2: "SMLA_ERR_SHAPE", 3: "SMLA_ERR_ALIGN",
           4: "SMLA_ERR_UNSUPPORTED", 5: "SMLA_ERR_WORKSPACE", 6: "SMLA_ERR_CUDA",
@@ -32,7 +38,8 @@ DEVICE_ERROR_STATUSES = (0, 7, 9, 10)  # statuses that report device error bits
 EXPORTS = ["smla_status_string", "smla_abi_version", "smla_workspace_size", "smla_decode",
            "smla_pack_kv", "smla_gather_dequant", "smla_read_error", "smla_decode_noalloc",
            "smla_set_kernel_events", "smla_pack_kv_fp8_tensor", "smla_selftest_wait_timeout",
-           "smla_noalloc_read_error", "smla_indexer_logits", "smla_indexer_topk", "smla_store_kv_normed"]
+           "smla_noalloc_read_error", "smla_indexer_logits", "smla_indexer_topk", "smla_store_kv_normed",
+           "smla_plan_launches"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -51,6 +58,13 @@ class smla_desc(ctypes.Structure):
                 ("num_splits", ctypes.c_int32), ("kv_scale", ctypes.c_float),
                 ("q_format", ctypes.c_int32), ("q_scale", ctypes.c_float),
                 ("reserved", ctypes.c_int32 * 1)]
+
+
+class smla_launch_plan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+                ("split_len", ctypes.c_int32), ("merge", ctypes.c_int32),
+                ("num_launches", ctypes.c_int32), ("ctas", ctypes.c_int32 * 2),
+                ("tail_items", ctypes.c_int32), ("workspace_bytes", ctypes.c_uint64)]
 
 
 class smla_indexer_desc(ctypes.Structure):
@@ -86,6 +100,8 @@ def lib() -> ctypes.CDLL:
         L.smla_abi_version.argtypes = []
         L.smla_workspace_size.restype = I32
         L.smla_workspace_size.argtypes = [D, ctypes.POINTER(SZ)]
+        L.smla_plan_launches.restype = I32
+        L.smla_plan_launches.argtypes = [D, I32, ctypes.POINTER(smla_launch_plan)]
         L.smla_decode.restype = I32
         L.smla_decode.argtypes = [D, P, P, P, P, P, P, P, P, P, SZ, P]
         L.smla_pack_kv.restype = I32
@@ -152,6 +168,13 @@ def workspace_size(desc: smla_desc) -> int:
     n = ctypes.c_size_t(0)
     _check("smla_workspace_size", lib().smla_workspace_size(ctypes.byref(desc), ctypes.byref(n)))
     return n.value
+
+
+def plan_launches(desc: smla_desc, num_sms: int) -> smla_launch_plan:
+    """The launches smla_decode makes for desc on a device with num_sms SMs (host-only)."""
+    p = smla_launch_plan()
+    _check("smla_plan_launches", lib().smla_plan_launches(ctypes.byref(desc), int(num_sms), ctypes.byref(p)))
+    return p
 
 
 def decode(desc, q, kv_cache, page_table, topk, req_id_per_token, sink, out, lse, workspace,

@@ -141,6 +141,27 @@ Plan make_plan(const smla_desc* d, int num_sms) {
   return p;
 }
 
+// Tail split (head-group kernels, library-chosen splits): when the (token, head group) items
+// fill whole waves of one CTA per SM plus a remainder of at most half a wave, the remainder
+// runs as a second launch with two splits an item, merged inside their cluster, so the last
+// wave takes about half a CTA's time instead of a whole one.
+struct Tail {
+  bool on;
+  int units;     // (token, head group) items
+  int rem;       // items of the second launch
+  int split_len; // index entries per split of the second launch
+};
+
+Tail plan_tail(const smla_desc* d, const Plan& plan, int num_sms) {
+  Tail t;
+  t.units = d->num_tokens * ((d->num_heads + 63) / 64);
+  t.rem = t.units % num_sms;
+  t.on = use_hg(d) && d->num_splits == 0 && plan.num_splits == 1 && d->topk >= 512 && t.units > num_sms &&
+         t.rem > 0 && 2 * t.rem <= num_sms;
+  t.split_len = ((d->topk + 1) / 2 + smla::kTile - 1) / smla::kTile * smla::kTile;
+  return t;
+}
+
 int ilog2(int x) {
   int l = 0;
   while ((1 << l) < x) ++l;
@@ -235,7 +256,7 @@ const char* smla_status_string(int32_t s) {
   }
 }
 
-int32_t smla_abi_version(void) { return 4; }
+int32_t smla_abi_version(void) { return 5; }
 
 smla_status smla_workspace_size(const smla_desc* d, size_t* bytes) {
   if (!bytes) return SMLA_ERR_NULL;
@@ -246,6 +267,36 @@ smla_status smla_workspace_size(const smla_desc* d, size_t* bytes) {
   st = current_device(&sms);
   if (st != SMLA_OK) return st;
   *bytes = make_plan(d, sms).bytes;
+  return SMLA_OK;
+}
+
+smla_status smla_plan_launches(const smla_desc* d, int32_t num_sms, smla_launch_plan* p) {
+  if (!p) return SMLA_ERR_NULL;
+  memset(p, 0, sizeof(*p));
+  smla_status st = check_desc(d);
+  if (st != SMLA_OK) return st;
+  if (num_sms < 1) return SMLA_ERR_SHAPE;
+  const Plan plan = make_plan(d, num_sms);
+  const Tail tail = plan_tail(d, plan, num_sms);
+  p->kernel = d->q_format == SMLA_Q_FP8_E4M3 ? SMLA_KERNEL_HEAD_GROUP_FP8
+              : use_hg(d)                    ? SMLA_KERNEL_HEAD_GROUP
+                                             : SMLA_KERNEL_MMA;
+  p->num_splits = plan.num_splits;
+  p->split_len = plan.split_len;
+  p->merge = plan.num_splits == 1 ? SMLA_MERGE_NONE : plan.cluster_merge ? SMLA_MERGE_CLUSTER : SMLA_MERGE_KERNEL;
+  if (!use_hg(d)) {
+    p->num_launches = 1;
+    p->ctas[0] = d->num_tokens * plan.num_splits * (d->num_heads / 16);
+  } else if (tail.on) {
+    p->num_launches = 2;
+    p->ctas[0] = (tail.units - tail.rem) * plan.num_splits;
+    p->ctas[1] = tail.rem * 2;
+    p->tail_items = tail.rem;
+  } else {
+    p->num_launches = 1;
+    p->ctas[0] = tail.units * plan.num_splits;
+  }
+  p->workspace_bytes = plan.bytes;
   return SMLA_OK;
 }
 
@@ -288,23 +339,16 @@ smla_status smla_decode(const smla_desc* d, const void* q, const void* kv_cache,
     return x.q_fp8 ? smla::launch_decode_hg_f8(x, s)
                    : use_hg(d) ? smla::launch_decode_hg(x, s) : smla::launch_decode_mma(x, sms, s);
   };
-  // Tail split (tensor-core kernels, library-chosen splits): when the (token, head group)
-  // items fill whole waves of one CTA per SM plus a remainder of at most half a wave, the
-  // remainder runs as a second launch with two splits an item, merged inside their cluster, so
-  // the last wave takes about half a CTA's time instead of a whole one.
-  const int units = d->num_tokens * ((d->num_heads + 63) / 64);
-  const int rem = units % sms;
-  const bool tail = use_hg(d) && d->num_splits == 0 && plan.num_splits == 1 && d->topk >= 512 && units > sms &&
-                    rem > 0 && 2 * rem <= sms;
+  const Tail tail = plan_tail(d, plan, sms);
   if (t_ev_start && cudaEventRecord(t_ev_start, s) != cudaSuccess) return SMLA_ERR_CUDA;
   cudaError_t e;
-  if (tail) {
+  if (tail.on) {
     smla::DecodeArgs full = a, last = a;
-    full.nitems = units - rem;
-    last.item0 = units - rem;
-    last.nitems = rem;
+    full.nitems = tail.units - tail.rem;
+    last.item0 = tail.units - tail.rem;
+    last.nitems = tail.rem;
     last.num_splits = 2;
-    last.split_len = ((d->topk + 1) / 2 + smla::kTile - 1) / smla::kTile * smla::kTile;
+    last.split_len = tail.split_len;
     last.cluster_merge = 1;
     // the remainder's items are independent of the whole waves': its CTAs take SMs as the last
     // wave's CTAs leave, with no launch gap in between

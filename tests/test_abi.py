@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.smla_abi_version() == 4
+    assert L.smla_abi_version() == 5
     for s in range(11):
         assert smla.status_string(s) != "unknown status"
     assert smla.status_string(99) == "unknown status"
@@ -219,3 +219,125 @@ def test_store_normed_desc_layout_and_host_checks(L):
     assert L.smla_store_kv_normed(ctypes.byref(d), P(8), P(16), P(16), P(16), P(16), P(16), P(16), None, None) == 3
     assert L.smla_store_kv_normed(ctypes.byref(d), P(16), P(16), P(16), P(16), P(4), P(16), P(16), None, None) == 3
     assert L.smla_store_kv_normed(ctypes.byref(d), None, P(16), P(16), P(16), P(16), P(16), P(16), None, None) == 1
+
+
+def _plan(L, d, sms=152):
+    p = smla.smla_launch_plan()
+    st = L.smla_plan_launches(ctypes.byref(d), sms, ctypes.byref(p))
+    return st, p
+
+
+def test_launch_plan_layout_matches_header():
+    # int32 x8 (ctas is two of them), then one uint64 at its natural alignment
+    assert ctypes.sizeof(smla.smla_launch_plan) == 40
+    assert smla.smla_launch_plan.ctas.offset == 20
+    assert smla.smla_launch_plan.workspace_bytes.offset == 32
+    assert _header_enum("SMLA_KERNEL_") == {"SMLA_KERNEL_HEAD_GROUP": smla.SMLA_KERNEL_HEAD_GROUP,
+                                            "SMLA_KERNEL_HEAD_GROUP_FP8": smla.SMLA_KERNEL_HEAD_GROUP_FP8,
+                                            "SMLA_KERNEL_MMA": smla.SMLA_KERNEL_MMA}
+    assert _header_enum("SMLA_MERGE_") == {"SMLA_MERGE_NONE": smla.SMLA_MERGE_NONE,
+                                           "SMLA_MERGE_CLUSTER": smla.SMLA_MERGE_CLUSTER,
+                                           "SMLA_MERGE_KERNEL": smla.SMLA_MERGE_KERNEL}
+
+
+def _wl_desc(tokens, heads, fmt=smla.SMLA_KV_FP8_DS, topk=2048, next_n=1, **kw):
+    d = smla.make_desc(tokens, heads, topk, tokens // next_n, 64, 4096, 2048, fmt, 1 / 24, next_n=next_n)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("name,desc,expect", [
+    # 64 requests x 4 MTP rows x 2 head groups = 512 items = 3 waves of 152 + 56: the last 56
+    # run as a second launch with two splits each
+    ("mtp 256 x 128 heads", _wl_desc(256, 128, next_n=4),
+     dict(kernel=1, num_splits=1, split_len=2048, merge=0, num_launches=2, ctas=(456, 112), tail_items=56,
+          workspace_bytes=256)),
+    ("mtp, E4M3 q, per-tensor cache", _wl_desc(256, 128, smla.SMLA_KV_FP8_TENSOR, next_n=4, q_format=1, q_scale=1.0),
+     dict(kernel=2, num_splits=1, split_len=2048, merge=0, num_launches=2, ctas=(456, 112), tail_items=56,
+          workspace_bytes=256)),
+    # 256 items = 152 + 104: a last wave more than half full stays in the one launch
+    ("128 x 128 heads", _wl_desc(128, 128),
+     dict(kernel=1, num_splits=1, split_len=2048, merge=0, num_launches=1, ctas=(256, 0), tail_items=0,
+          workspace_bytes=256)),
+    # 32 items: four splits of 512 fill 128 SMs, merged inside the cluster
+    ("32 x 64 heads", _wl_desc(32, 64),
+     dict(kernel=1, num_splits=4, split_len=512, merge=1, num_launches=1, ctas=(128, 0), tail_items=0,
+          workspace_bytes=256)),
+    # 16 heads: the mma.sync kernel, one CTA per (token, 16 heads), 256 >= 152 so one split
+    ("256 x 16 heads", _wl_desc(256, 16),
+     dict(kernel=3, num_splits=1, split_len=2048, merge=0, num_launches=1, ctas=(256, 0), tail_items=0,
+          workspace_bytes=256)),
+    # 4 x 16 heads: about two CTAs an SM wants 76 splits, capped at 2048 / 256 = 8; fp32
+    # partials of 4 x 8 x 16 rows for the merge kernel: 256 + 2048 B of LSE, 512 x 512 x 4 B
+    ("4 x 16 heads", _wl_desc(4, 16),
+     dict(kernel=3, num_splits=8, split_len=256, merge=2, num_launches=1, ctas=(32, 0), tail_items=0,
+          workspace_bytes=2304 + 512 * 512 * 4)),
+    # 12 splits asked: 2048 / 12 rounds up to 192 entries, hence 11 splits, beyond a cluster's 8:
+    # f16 partials of 2 x 11 x 64 rows through the merge kernel: 256 + 5632 B of LSE, 1408 x 512 x 2 B
+    ("2 x 64 heads, 12 splits asked", _wl_desc(2, 64, num_splits=12),
+     dict(kernel=1, num_splits=11, split_len=192, merge=2, num_launches=1, ctas=(22, 0), tail_items=0,
+          workspace_bytes=5888 + 1408 * 512 * 2)),
+    # the bf16 cache takes the mma.sync kernel at any head count
+    ("bf16 cache, 64 x 128 heads", _wl_desc(64, 128, smla.SMLA_KV_BF16),
+     dict(kernel=3, num_splits=1, split_len=2048, merge=0, num_launches=1, ctas=(512, 0), tail_items=0,
+          workspace_bytes=256)),
+])
+def test_plan_launches_of_the_benchmarked_shapes(L, name, desc, expect):
+    st, p = _plan(L, desc)
+    assert st == 0, name
+    got = {k: getattr(p, k) for k in expect}
+    got["ctas"] = tuple(p.ctas)
+    assert got == expect, name
+
+
+def test_plan_tail_split_boundaries(L):
+    # items = tokens x 2 head groups; the second launch appears exactly when the remainder
+    # over whole waves is at most half the SMs, and only with library-chosen splits
+    for sms in (152, 148, 132):
+        for tokens in range(sms // 2 + 1, 3 * sms):
+            st, p = _plan(L, _wl_desc(tokens, 128), sms)
+            assert st == 0
+            items = 2 * tokens
+            rem = items % sms
+            tail = items > sms and 0 < rem and 2 * rem <= sms
+            assert p.num_launches == (2 if tail else 1), (sms, tokens)
+            total = p.ctas[0] + p.ctas[1]
+            if tail:
+                assert p.ctas[0] == items - rem and p.ctas[1] == 2 * rem and p.tail_items == rem
+            elif items >= sms:
+                assert p.num_splits == 1 and total == items
+    st, p = _plan(L, _wl_desc(256, 128, next_n=4, num_splits=1))
+    assert st == 0 and p.num_launches == 1 and tuple(p.ctas) == (512, 0)
+    # short index rows keep one launch
+    st, p = _plan(L, _wl_desc(256, 128, topk=256, next_n=4))
+    assert st == 0 and p.num_launches == 1
+
+
+def test_plan_splits_cover_the_index_row(L):
+    for heads in (16, 32, 64, 128):
+        for topk in (4, 64, 252, 256, 2048, 4096, 8192, 2048 * 64):
+            for tokens in (1, 3, 40, 300):
+                for splits in (0, 1, 5, 64):
+                    st, p = _plan(L, _wl_desc(tokens, heads, topk=topk, num_splits=splits))
+                    assert st == 0
+                    S, n = p.num_splits, p.split_len
+                    assert n % 64 == 0 and n <= 2048 and 1 <= S <= 64
+                    assert (S - 1) * n < topk <= S * n, (heads, topk, tokens, splits, S, n)
+                    if S == 1:
+                        assert p.merge == smla.SMLA_MERGE_NONE
+                    elif heads >= 64 and S <= 8:
+                        assert p.merge == smla.SMLA_MERGE_CLUSTER and p.workspace_bytes == 256
+                    else:
+                        assert p.merge == smla.SMLA_MERGE_KERNEL and p.workspace_bytes > 256
+
+
+def test_plan_launches_host_checks(L):
+    p = smla.smla_launch_plan()
+    assert L.smla_plan_launches(None, 152, ctypes.byref(p)) == 1
+    assert L.smla_plan_launches(ctypes.byref(_desc()), 152, None) == 1
+    assert L.smla_plan_launches(ctypes.byref(_desc()), 0, ctypes.byref(p)) == 2
+    p.kernel = 7
+    assert L.smla_plan_launches(ctypes.byref(_desc(num_heads=8)), 152, ctypes.byref(p)) == 2
+    assert p.kernel == 0  # zeroed on error
+    assert smla.plan_launches(_desc(), 152).kernel == smla.SMLA_KERNEL_MMA

@@ -458,6 +458,18 @@ def test_workspace_holds_partials_at_their_element_size(heads, fmt, elem):
     assert smla.workspace_size(d) == 256 + (rows * 4 + 255) // 256 * 256 + rows * 512 * elem
 
 
+def test_plan_query_agrees_with_the_device_workspace():
+    # the host-only plan query, given this device's SM count, asks for the workspace the
+    # device-side query asks for
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for w in list(W.WORKLOADS) + list(W.EXTRA_WORKLOADS):
+        fmt = {"bf16": smla.SMLA_KV_BF16, "fp8_ds": smla.SMLA_KV_FP8_DS, "fp8_tensor": smla.SMLA_KV_FP8_TENSOR}[w.kv_format]
+        for splits in (0, 3, 12):
+            d = smla.make_desc(w.num_tokens, w.num_heads, w.topk, w.num_requests, w.page_size, 1024, 64, fmt,
+                               1 / 24, next_n=w.next_n, num_splits=splits)
+            assert smla.plan_launches(d, sms).workspace_bytes == smla.workspace_size(d), (w.name, splits)
+
+
 # ------------------------------------------------------------------ full-size, sampled
 
 
