@@ -395,6 +395,37 @@ def test_decode_long_index_rows(wi, splits):
     assert_parity(*DeviceDecode(p, num_splits=splits).run(), oracle_decode(p))
 
 
+@pytest.mark.parametrize("wi", [1, 2, 4])  # 64 and 128 heads (tensor-core kernel), 16 heads
+@pytest.mark.parametrize("topk", [4, 60, 68])
+def test_decode_index_rows_shorter_than_a_tile(wi, topk):
+    # fewer entries than one 64-slot tile, and one tile plus a ragged 4; a 40-slot context
+    # leaves some rows shorter still, padded with -1
+    w = W.small_variant(W.WORKLOADS[wi], num_requests=3, ctx_lo=40, ctx_hi=500, topk=topk)
+    p = W.make_problem(w)
+    ref = oracle_decode(p)
+    for splits in (0, 2):
+        assert_parity(*DeviceDecode(p, num_splits=splits).run(), ref)
+
+
+@pytest.mark.parametrize("wi", [1, 4])
+def test_decode_longest_index_row(wi):
+    # the largest top-k the library takes, 64 splits of 2048 entries: every split lane of the
+    # merge kernel (f16 partials from the tensor-core kernel, fp32 from the mma.sync one)
+    w = W.small_variant(W.WORKLOADS[wi], num_requests=1, ctx_lo=131072, ctx_hi=131072, topk=131072)
+    p = W.make_problem(w)
+    dd = DeviceDecode(p)
+    assert smla.plan_launches(dd.desc, 152).num_splits == 64
+    assert_parity(*dd.run(), oracle_decode(p))
+    assert smla.read_error(dd.desc, dd.workspace) == 0
+
+
+def test_decode_largest_page_size():
+    w = W.small_variant(W.WORKLOADS[2], num_requests=2, ctx_lo=5000, ctx_hi=9000, topk=320).replace(
+        page_size=4096, name="fp8_P4096")
+    p = W.make_problem(w)
+    assert_parity(*DeviceDecode(p).run(), oracle_decode(p))
+
+
 @pytest.mark.parametrize("heads", [64, 128])
 def test_decode_bf16_cache_many_heads(heads):
     w = W.WORKLOADS[0].replace(num_heads=heads, name=f"bf16_H{heads}")
