@@ -73,3 +73,19 @@ def test_both_arms_share_one_config():
     assert line["impl"] == "reference" and line["config"] == cfg
     assert line["metric"] == bench.METRIC and line["unit"] == "query-tokens/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_launch_count_comes_from_the_library_plan():
+    # gpu_launches counts the decode launches of the library's own plan, plus its merge kernel
+    smla = pytest.importorskip("sparse_mla_decode_smla_gb300")
+    if not os.path.exists(smla.LIB_PATH):
+        pytest.skip("libsmla.so is not built")
+
+    def desc(tokens, heads, next_n=1):
+        return smla.make_desc(tokens, heads, 2048, tokens // next_n, 64, 4096, 2048, smla.SMLA_KV_FP8_DS,
+                              1 / 24, next_n=next_n)
+
+    assert bench.decode_launches(smla, desc(256, 128, next_n=4), 152) == 2  # whole waves + the tail
+    assert bench.decode_launches(smla, desc(32, 64), 152) == 1   # splits merged in the cluster
+    assert bench.decode_launches(smla, desc(128, 128), 152) == 1
+    assert bench.decode_launches(smla, desc(4, 16), 152) == 2    # mma.sync splits + the merge kernel
