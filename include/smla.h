@@ -245,6 +245,9 @@ smla_status smla_set_kernel_events(void* start, void* stop);
  *   BF16:   the 576 values are stored as given (scale_mode ignored).
  *   latent [n, 512] bf16 and rope [n, 64] bf16, 16-byte aligned; slot_mapping [n] int64;
  *   kv_cache holds num_slots rows. Entries of slot_mapping >= num_slots are skipped.
+ * Status (all found before any launch): SMLA_ERR_UNSUPPORTED for another kv_format or
+ * scale_mode, SMLA_ERR_SHAPE for n < 0, num_slots < 0 or n > 2^36, SMLA_ERR_NULL or
+ * SMLA_ERR_ALIGN for a pointer (slot_mapping 8-byte aligned); n == 0 launches nothing.
  */
 smla_status smla_pack_kv(int32_t kv_format, int32_t scale_mode, const void* latent,
                          const void* rope, const int64_t* slot_mapping, int64_t n,
@@ -258,6 +261,7 @@ smla_status smla_pack_kv(int32_t kv_format, int32_t scale_mode, const void* late
  * store_full_fp8 path of the compressor in vLLM PR #43827 "实现拆解 4-5".
  *   latent [n, 512] bf16 and rope [n, 64] bf16, 16-byte aligned; slot_mapping [n] int64;
  *   kv_scale finite and > 0 (SMLA_ERR_SHAPE otherwise).
+ * Status: as smla_pack_kv; n == 0 launches nothing.
  */
 smla_status smla_pack_kv_fp8_tensor(const void* latent, const void* rope,
                                     const int64_t* slot_mapping, int64_t n, float kv_scale,
@@ -278,6 +282,9 @@ smla_status smla_pack_kv_fp8_tensor(const void* latent, const void* rope,
  *   positions [n] int64; cos_sin [max_position, 64] fp32, 16-byte aligned; slot_mapping [n] int64.
  *   error_word: device int32 or NULL; a row whose position is outside [0, max_position) is not
  *   written and sets SMLA_DEVERR_INDEX.
+ * Status (before any launch): SMLA_ERR_UNSUPPORTED for another kv_format or scale_mode,
+ * SMLA_ERR_SHAPE for a bad kv_scale, rms_eps, n, num_slots or max_position or a non-zero
+ * reserved word, SMLA_ERR_NULL or SMLA_ERR_ALIGN for a pointer; n == 0 launches nothing.
  */
 typedef struct smla_store_desc {
   int32_t kv_format;    /* SMLA_KV_* */
@@ -302,6 +309,7 @@ smla_status smla_store_kv_normed(const smla_store_desc* d, const void* latent, c
  * slot topk[t, j] selects: latent element d = fl32(e4m3(code_d) * scale[d/128]) for
  * FP8_DS, the bf16 value otherwise; RoPE as bf16 values. Padding and invalid entries
  * give a zero row. error_word (device int32, may be NULL) receives SMLA_DEVERR_* bits.
+ * The descriptor is checked as smla_decode checks it; kv_cache and rows 16-byte aligned.
  */
 smla_status smla_gather_dequant(const smla_desc* d, const void* kv_cache,
                                 const int32_t* page_table, const int32_t* topk,
