@@ -261,6 +261,45 @@ def test_unselected_rows_are_never_read(small_cases, wi):
     assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
 
 
+@pytest.mark.parametrize("wi", [1, 2, 4])
+def test_index_order_does_not_change_the_result(small_cases, wi):
+    # the result depends on the selected entries, not their order: permuting every token's
+    # top-k row changes only the order of the sums
+    p, ref = small_cases[SMALL[wi].name]
+    dd = DeviceDecode(p)
+    out0, lse0 = [x.clone() for x in dd.run()]
+    g = torch.Generator().manual_seed(11)
+    perm = torch.stack([torch.randperm(p.w.topk, generator=g) for _ in range(p.w.num_tokens)])
+    dd.topk = torch.gather(p.topk.cpu().to(torch.int64), 1, perm).to(torch.int32).to(dd.topk.device).contiguous()
+    out1, lse1 = dd.run()
+    assert_parity(out1, lse1, ref)
+    assert (out1.float() - out0.float()).abs().max().item() <= OUT_ATOL
+    fin = torch.isfinite(lse0)
+    assert torch.equal(fin, torch.isfinite(lse1))
+    assert (lse1[fin] - lse0[fin]).abs().max().item() <= 1e-4
+
+
+@pytest.mark.parametrize("wi,topk,splits", [(1, 320, 1), (2, 448, 3), (1, 1024, 16), (4, 320, 0), (4, 320, 3)])
+def test_outputs_stay_inside_their_buffers(wi, topk, splits):
+    # out and lse lie between guard bands of a sentinel pattern: the decode writes nothing
+    # outside its [T, H, 512] and [T, H] elements, with one split, splits merged inside the
+    # cluster, splits through the merge kernel (16 of 64 entries), and the mma.sync kernel
+    w = W.small_variant(W.WORKLOADS[wi], num_requests=2, ctx_lo=topk + 100, ctx_hi=topk + 400, topk=topk)
+    p = W.make_problem(w)
+    dd = DeviceDecode(p, num_splits=splits)
+    want_out, want_lse = [x.clone() for x in dd.run()]
+    T, H, G = w.num_tokens, w.num_heads, 4096  # G guard elements on each side (16-byte multiples)
+    ob = torch.full((G + T * H * 512 + G,), 0x3039, dtype=torch.int16, device="cuda")
+    lb = torch.full((G + T * H + G,), -7.0, dtype=torch.float32, device="cuda")
+    dd.out = ob[G:G + T * H * 512].view(torch.bfloat16).view(T, H, 512)
+    dd.lse = lb[G:G + T * H].view(T, H)
+    out, lse = dd.run()
+    torch.cuda.synchronize()
+    assert (ob[:G] == 0x3039).all() and (ob[G + T * H * 512:] == 0x3039).all()
+    assert (lb[:G] == -7.0).all() and (lb[G + T * H:] == -7.0).all()
+    assert torch.equal(out, want_out) and torch.equal(lse, want_lse)
+
+
 def test_page_relabel_is_bitwise_invariant(small_cases):
     p, _ = small_cases[SMALL[1].name]
     dd = DeviceDecode(p, num_splits=1)
