@@ -65,9 +65,15 @@ def test_bit_exact_where_fp32_is_exact(fmt):
     n = 700
     x = _exact_inputs(n, 3)
     slots = torch.randperm(900)[:n].to(torch.int64)
+    slots[7] = -1    # not stored
+    slots[8] = 905   # beyond the cache's 900 rows: not stored
     got = _store(fmt, x, 0.0, slots, 900, kv_scale=2.0 ** -3)
     ref = _oracle(fmt, x, 0.0, kv_scale=2.0 ** -3)
-    assert np.array_equal(got[slots.numpy()], ref)
+    m = slots.numpy()
+    ok = (m >= 0) & (m < 900)
+    assert np.array_equal(got[m[ok]], ref[ok])
+    # every other row of the cache keeps its bytes
+    assert (got[np.setdiff1d(np.arange(900), m[ok])] == 0xAB).all()
 
 
 # a power-of-two scale takes the kernel's exact reciprocal, any other one its division
