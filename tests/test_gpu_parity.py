@@ -594,3 +594,38 @@ def test_tail_wave_split_launch():
     dd2.run()
     torch.cuda.synchronize()
     assert torch.equal(dd2.out.view(torch.int16), out2.view(torch.int16)) and torch.equal(dd2.lse, lse2)
+
+
+@pytest.mark.parametrize("wi,topk,splits", [(1, 320, 1), (2, 448, 3), (1, 1024, 16), (4, 320, 3)])
+def test_lse_is_optional(wi, topk, splits):
+    # lse = NULL: the output is the same, bit for bit, with one split, splits merged in the
+    # cluster, splits through the merge kernel, and the mma.sync kernel
+    w = W.small_variant(W.WORKLOADS[wi], num_requests=2, ctx_lo=topk + 100, ctx_hi=topk + 400, topk=topk)
+    p = W.make_problem(w)
+    want = DeviceDecode(p, num_splits=splits).run()[0].clone()
+    dd = DeviceDecode(p, num_splits=splits, with_lse=False)
+    out, lse = dd.run()
+    torch.cuda.synchronize()
+    assert lse is None and torch.equal(out.view(torch.int16), want.view(torch.int16))
+    assert smla.read_error(dd.desc, dd.workspace) == 0
+
+
+def test_decode_on_a_side_stream():
+    # the library launches on the caller's stream: on a non-default stream, with the whole-wave
+    # and tail launches of the head-group kernel, the result equals the default stream's
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = (sms + 8 + 1) // 2
+    w = W.small_variant(W.WORKLOADS[2], num_requests=T, ctx_lo=600, ctx_hi=600, topk=512)
+    p = W.make_problem(w)
+    dd = DeviceDecode(p)
+    assert smla.plan_launches(dd.desc, sms).num_launches == 2
+    ref_out, ref_lse = [x.clone() for x in dd.run()]
+    torch.cuda.synchronize()
+    dd.out.zero_()
+    dd.lse.zero_()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        dd.run(side)
+    side.synchronize()
+    assert torch.equal(dd.out.view(torch.int16), ref_out.view(torch.int16)) and torch.equal(dd.lse, ref_lse)
