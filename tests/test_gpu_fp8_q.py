@@ -155,3 +155,30 @@ def test_fp8_q_full_size_mtp_sampled():
     ref = oracle_decode(p, tokens=tokens, q_e4m3=q8, q_scale=QS)
     vmax = 6.0  # N(0, 1) values in E4M3 at kv_scale 1 stay below this over any sample of the pool
     assert_fp8_parity(out, lse, ref, vmax, tokens=tokens)
+
+
+@pytest.mark.parametrize("splits", [1, 3, 16])
+def test_fp8_q_outputs_stay_inside_their_buffers(splits):
+    # out and lse between guard bands: one split, splits merged in the cluster, and splits
+    # through the merge kernel (16 of 64 entries); lse = NULL gives the same output bits
+    w = SMALL[0].replace(num_heads=128, topk=1024, ctx_lo=1500, ctx_hi=1500)
+    p = W.make_problem(w)
+    dd = DeviceDecode(p, num_splits=splits)
+    dd.q = W.q_to_e4m3(p.q, QS).cuda().contiguous()
+    dd.desc.q_format, dd.desc.q_scale = smla.SMLA_Q_FP8_E4M3, QS
+    want_out, want_lse = [x.clone() for x in dd.run()]
+    T, H, G = w.num_tokens, w.num_heads, 4096
+    ob = torch.full((G + T * H * 512 + G,), 0x3039, dtype=torch.int16, device="cuda")
+    lb = torch.full((G + T * H + G,), -7.0, dtype=torch.float32, device="cuda")
+    dd.out = ob[G:G + T * H * 512].view(torch.bfloat16).view(T, H, 512)
+    dd.lse = lb[G:G + T * H].view(T, H)
+    out, lse = dd.run()
+    torch.cuda.synchronize()
+    assert (ob[:G] == 0x3039).all() and (ob[G + T * H * 512:] == 0x3039).all()
+    assert (lb[:G] == -7.0).all() and (lb[G + T * H:] == -7.0).all()
+    assert torch.equal(out.view(torch.int16), want_out.view(torch.int16)) and torch.equal(lse, want_lse)
+    dd.lse = None
+    out, _ = dd.run()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), want_out.view(torch.int16))
+    assert smla.read_error(dd.desc, dd.workspace) == 0
