@@ -341,3 +341,32 @@ def test_plan_launches_host_checks(L):
     assert L.smla_plan_launches(ctypes.byref(_desc(num_heads=8)), 152, ctypes.byref(p)) == 2
     assert p.kernel == 0  # zeroed on error
     assert smla.plan_launches(_desc(), 152).kernel == smla.SMLA_KERNEL_MMA
+
+
+def test_without_a_device_every_launching_call_fails_loudly(L):
+    # No CPU fallback: with no sm_103 device, every call that would launch returns
+    # SMLA_ERR_DEVICE after its argument checks, and only the host-only plan query answers.
+    # smla_workspace_size launches nothing and tells whether a device is present; with one,
+    # these dummy pointers must not reach a launch, so the test stops there.
+    n = ctypes.c_size_t(0)
+    if L.smla_workspace_size(ctypes.byref(_desc()), ctypes.byref(n)) != 8:
+        pytest.skip("an sm_103 device is present")
+    P = ctypes.c_void_p
+    v = ctypes.c_int32(0)
+    assert _decode_status(L, _desc()) == 8
+    assert L.smla_decode_noalloc(ctypes.byref(_desc()), P(16), P(16), P(16), P(16), None, None, P(16), None,
+                                 None) == 8
+    assert L.smla_pack_kv(1, 0, P(16), P(16), P(16), 4, P(16), 8, None) == 8
+    assert L.smla_pack_kv_fp8_tensor(P(16), P(16), P(16), 4, ctypes.c_float(1.0), P(16), 8, None) == 8
+    sd = smla.smla_store_desc()
+    sd.kv_format, sd.n, sd.num_slots, sd.max_position = smla.SMLA_KV_BF16, 4, 8, 16
+    assert L.smla_store_kv_normed(ctypes.byref(sd), P(16), P(16), P(16), P(16), P(16), P(16), P(16), None,
+                                  None) == 8
+    assert L.smla_gather_dequant(ctypes.byref(_desc()), P(16), P(16), P(16), None, P(16), None, None) == 8
+    xd = smla.make_indexer_desc(4, 1, 64, 64, 16, 8, 1024, 256)
+    assert L.smla_indexer_logits(ctypes.byref(xd), P(16), P(16), P(16), P(16), P(16), P(16), P(16), None) == 8
+    assert L.smla_indexer_topk(ctypes.byref(xd), P(16), P(16), P(16), None) == 8
+    assert L.smla_selftest_wait_timeout(P(16), 10, None) == 8
+    assert L.smla_noalloc_read_error(ctypes.byref(v), None) == 8
+    p = smla.smla_launch_plan()
+    assert L.smla_plan_launches(ctypes.byref(_desc()), 152, ctypes.byref(p)) == 0
