@@ -3,8 +3,9 @@
 A pin is only worth as much as the mistakes it would catch. Every case below edits a
 copy of `oracle/` the way a slip in writing it could have (a wrong exponent bias, a
 dropped term, a transposed index, a sign, an off-by-one), then runs the pin files
-(`test_oracle_pins.py`, `test_indexer_oracle_pins.py`) against that copy in a child
-process and expects them to fail. A control run of the unchanged copy must pass, and
+(`test_oracle_pins.py`, `test_indexer_oracle_pins.py`, and `test_workloads.py` for the
+oracle's view of a seeded problem) against that copy in a child process and expects them
+to fail. A control run of the unchanged copy must pass, and
 each planted edit must match its source text exactly once, so a later change to the
 oracle that moves the text makes this test fail rather than pass without planting
 anything. CPU only; the repository's own files are never modified.
@@ -18,9 +19,10 @@ import sys
 from concurrent.futures import ThreadPoolExecutor
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PIN_FILES = ("test_oracle_pins.py", "test_indexer_oracle_pins.py")
+PIN_FILES = ("test_oracle_pins.py", "test_indexer_oracle_pins.py", "test_workloads.py")
 SMLA = "smla_oracle.py"
 IX = "indexer_oracle.py"
+WO = "workload_oracle.py"
 
 # (name, file, [(text, replacement), ...]): each edit is one plausible mistake.
 MISTAKES = [
@@ -120,13 +122,18 @@ MISTAKES = [
     ("token's request row from the wrong end", IX, [("r, i = divmod(int(t), next_n)", "r, i = divmod(int(t), next_n)\n        i = next_n - 1 - i")]),
     ("top-k takes the smallest", IX, [('order = np.argsort(-logits, kind="stable")', 'order = np.argsort(logits, kind="stable")')]),
     ("top-k one short", IX, [("return np.sort(order[:k])", "return np.sort(order[:k - 1])")]),
+    # the oracle's view of a seeded problem's cache
+    ("cache row one slot along", WO, [("return self.rows[loc * self.P + phys % self.P]",
+                                       "return self.rows[loc * self.P + (phys + 1) % self.P]")]),
+    ("cache packed with fp32 scales", WO, [("O.pack_fp8_ds(_bits(lat), _bits(rope), scale_mode)",
+                                            "O.pack_fp8_ds(_bits(lat), _bits(rope), O.SCALE_FP32)")]),
 ]
 
 
 def _copy_tree(dst: str, file_name: str | None = None, edits=()):
     """Copy the oracle package and the pin files under dst, planting edits in file_name."""
-    shutil.copytree(os.path.join(ROOT, "oracle"), os.path.join(dst, "oracle"),
-                    ignore=shutil.ignore_patterns("__pycache__"))
+    for pkg in ("oracle", "workloads"):
+        shutil.copytree(os.path.join(ROOT, pkg), os.path.join(dst, pkg), ignore=shutil.ignore_patterns("__pycache__"))
     os.makedirs(os.path.join(dst, "tests"))
     for f in ("conftest.py",) + PIN_FILES:
         shutil.copy(os.path.join(ROOT, "tests", f), os.path.join(dst, "tests", f))

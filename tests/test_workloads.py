@@ -76,3 +76,26 @@ def test_magnitude_gains_multiply_the_draw_before_rounding():
     assert torch.allclose(lat1[0].float(), lat0[0].float() * 1e-4, rtol=1e-2)
     assert torch.allclose(lat1[4].float(), lat0[4].float() * 2.0, rtol=1e-2)
     assert torch.allclose(rope1[5].float(), rope0[5].float() * 7.0, rtol=1e-2)
+
+
+def test_oracle_cache_fetches_the_row_of_each_physical_slot():
+    # the oracle's cache of a problem returns, for physical slot s, the packed source row of
+    # page s // P at position s % P, whatever the order the slots are asked in
+    import numpy as np
+
+    import oracle as O
+    from oracle.workload_oracle import OracleCache
+
+    w = W.small_variant(W.WORKLOADS[2], num_requests=2, ctx_lo=300, ctx_hi=700, topk=128)
+    p = W.make_problem(w)
+    cache = OracleCache(p)
+    P = w.page_size
+    pages = sorted({int(x) for x in p.page_table.flatten().tolist() if 0 <= x < p.num_pages})
+    g = np.random.default_rng(5)
+    slots = np.array([pg * P + int(g.integers(P)) for pg in g.permutation(pages)[:12]], dtype=np.int64)
+    got = cache.fetch(slots)
+    for k, s in enumerate(slots.tolist()):
+        lat, rope = p.raw_pages([s // P])
+        bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+        want = O.pack_fp8_ds(bits(lat[s % P:s % P + 1]), bits(rope[s % P:s % P + 1]))
+        assert np.array_equal(got[k], want[0]), s
