@@ -122,6 +122,8 @@ MISTAKES = [
     ("token's request row from the wrong end", IX, [("r, i = divmod(int(t), next_n)", "r, i = divmod(int(t), next_n)\n        i = next_n - 1 - i")]),
     ("top-k takes the smallest", IX, [('order = np.argsort(-logits, kind="stable")', 'order = np.argsort(logits, kind="stable")')]),
     ("top-k one short", IX, [("return np.sort(order[:k])", "return np.sort(order[:k - 1])")]),
+    ("top-k ties to the highest index", IX, [('order = np.argsort(-logits, kind="stable")',
+                                              'order = n - 1 - np.argsort(-logits[::-1], kind="stable")')]),
     # the oracle's view of a seeded problem's cache
     ("cache row one slot along", WO, [("return self.rows[loc * self.P + phys % self.P]",
                                        "return self.rows[loc * self.P + (phys + 1) % self.P]")]),
