@@ -71,3 +71,61 @@ def test_fp8_parity_check_refuses_a_planted_error(case, kind):
     o, l = _planted(out, lse, kind)
     with pytest.raises(AssertionError):
         assert_fp8_parity(o, l, ref, vmax)
+
+
+# ----------------------------------------------------------------------------- indexer
+
+
+@pytest.fixture(scope="module")
+def ix_case():
+    from oracle import indexer_oracle as IX
+    import oracle as O
+    g = np.random.default_rng(3)
+    q = g.integers(0, 256, (64, 128), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0  # no NaN codes
+    kc = g.integers(0, 256, (600, 128), dtype=np.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0
+    keys = O.e4m3_decode(kc)
+    sc = 2.0 ** g.integers(-10, -4, 600).astype(np.float64)
+    wt = g.standard_normal(64) / 8
+    ref = IX.logits_of_token(q, wt, keys, sc)
+    bound = np.abs(wt) @ (np.abs(O.e4m3_decode(q)) @ np.abs(keys).T) * sc[None, :]
+    return ref, np.asarray(bound).reshape(-1), IX.topk_set(ref, 100)
+
+
+def test_logits_check_accepts_the_oracle_and_refuses_planted_errors(ix_case):
+    from test_gpu_indexer import _check_logits
+    ref, bound, _ = ix_case
+    row = torch.from_numpy(np.concatenate([ref, np.zeros(40)])).to(torch.float32)  # slots past n are not read
+    _check_logits(row, ref, bound)
+    for planted in ("off", "nan"):
+        bad = row.clone()
+        k = int(np.argmax(bound))
+        bad[k] = float("nan") if planted == "nan" else bad[k] + 3e-4 * float(bound[k])
+        with pytest.raises(AssertionError):
+            _check_logits(bad, ref, bound)
+
+
+@pytest.mark.parametrize("planted", ["duplicate", "a low value", "descending", "past the row", "short row padding"])
+def test_topk_check_accepts_the_oracle_and_refuses_planted_errors(ix_case, planted):
+    from test_gpu_indexer import _check_topk_valid
+    ref, bound, sel = ix_case
+    K = 100
+    _check_topk_valid(torch.from_numpy(sel.astype(np.int32)), ref, bound, K)
+    bad = sel.astype(np.int32).copy()
+    rr, bb = ref, bound
+    if planted == "duplicate":
+        bad[5] = bad[4]
+    elif planted == "a low value":
+        bad[np.argmax(ref[bad])] = int(np.argmin(ref))
+        bad.sort()
+    elif planted == "descending":
+        bad = bad[::-1].copy()
+    elif planted == "past the row":
+        bad[-1] = ref.shape[0]
+    elif planted == "short row padding":  # 60 visible slots: all of them, then -1 (here one slot missed)
+        rr, bb = ref[:60], bound[:60]
+        _check_topk_valid(torch.from_numpy(np.concatenate([np.arange(60), -np.ones(40)]).astype(np.int32)), rr, bb, K)
+        bad = np.concatenate([np.arange(59), -np.ones(41)]).astype(np.int32)
+    with pytest.raises(AssertionError):
+        _check_topk_valid(torch.from_numpy(bad), rr, bb, K)
