@@ -129,3 +129,32 @@ def test_topk_check_accepts_the_oracle_and_refuses_planted_errors(ix_case, plant
         bad = np.concatenate([np.arange(59), -np.ones(41)]).astype(np.int32)
     with pytest.raises(AssertionError):
         _check_topk_valid(torch.from_numpy(bad), rr, bb, K)
+
+
+# ----------------------------------------------------------------------------- operand range
+
+
+@pytest.mark.parametrize("planted", ["none", "row scaled by 0.97", "spread over a row", "lse shifted"])
+def test_scale_free_check_sees_errors_at_small_magnitudes(case, planted):
+    # outputs of keys scaled by 1e-5 are compared after dividing by the gain: errors far below
+    # the absolute tolerance of unscaled outputs must still be refused
+    from test_gpu_operand_range import _assert_close
+    ref, out, lse = case
+    gain = 1e-5
+    small = {"out": ref["out"] * gain, "lse": ref["lse"]}
+    o = (torch.from_numpy(ref["out"]) * gain).to(torch.bfloat16)
+    l = lse.clone()
+    if planted == "row scaled by 0.97":
+        o[1, 3] = (o[1, 3].double() * 0.97).to(torch.bfloat16)
+    elif planted == "spread over a row":
+        t, h = np.unravel_index(int(np.linalg.norm(ref["out"], axis=-1).argmin()), ref["out"].shape[:2])
+        g = torch.Generator().manual_seed(2)
+        o[t, h] = (o[t, h].double() + 0.006 * gain * torch.sign(torch.randn(512, generator=g))).to(torch.bfloat16)
+    elif planted == "lse shifted":
+        l[1, 1] -= 2e-3
+    if planted == "none":
+        _assert_close(o, l, small, out_scale=gain)
+    else:
+        assert np.abs(o.double().numpy() - small["out"]).max() < 1e-6  # invisible to an absolute bound
+        with pytest.raises(AssertionError):
+            _assert_close(o, l, small, out_scale=gain)
