@@ -14,8 +14,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def L():
-    if not os.path.exists(_build.LIB):
-        _build.build()
+    _build.build()  # incremental: recompiles only sources newer than their objects
     return smla.lib()
 
 
