@@ -369,3 +369,30 @@ def test_without_a_device_every_launching_call_fails_loudly(L):
     assert L.smla_noalloc_read_error(ctypes.byref(v), None) == 8
     p = smla.smla_launch_plan()
     assert L.smla_plan_launches(ctypes.byref(_desc()), 152, ctypes.byref(p)) == 0
+
+
+def test_descriptor_rules_one_violation_at_a_time(L):
+    # every field rule of smla_desc as the header states it, checked through the host-only plan
+    # query (which runs smla_decode's descriptor checks and touches no device): a valid
+    # descriptor passes, and each single violation gives its documented status
+    import numpy as np
+    g = np.random.default_rng(17)
+    violations = [
+        ("num_tokens", 0, 2), ("num_requests", 0, 2), ("next_n", 0, 2), ("topk", 0, 2),
+        ("num_heads", 0, 2), ("num_heads", 24, 2), ("num_heads", 144, 2), ("topk", 130, 2),
+        ("topk", 64 * 2048 + 4, 2), ("page_size", 3, 2), ("page_size", 8192, 2), ("num_pages", 0, 2),
+        ("num_pages", (1 << 31) + 1, 2), ("page_table_stride", 0, 2), ("kv_format", 3, 4),
+        ("sm_scale", float("inf"), 2), ("num_splits", -1, 2), ("num_splits", 65, 2), ("q_format", 2, 4),
+    ]
+    p = smla.smla_launch_plan()
+    for _ in range(200):
+        d = smla.make_desc(int(g.integers(1, 400)), 16 * int(g.integers(1, 9)), 4 * int(g.integers(1, 4097)),
+                           int(g.integers(1, 64)), 1 << int(g.integers(0, 13)), int(g.integers(1, 1 << 20)),
+                           int(g.integers(1, 4096)), int(g.integers(0, 3)), float(g.uniform(0.01, 1.0)),
+                           next_n=int(g.integers(1, 5)), num_splits=int(g.integers(0, 65)),
+                           kv_scale=float(g.uniform(0.001, 2.0)))
+        assert L.smla_plan_launches(ctypes.byref(d), 152, ctypes.byref(p)) == 0
+        assert 1 <= p.num_splits <= 64 and p.ctas[0] >= 1
+        field, value, status = violations[int(g.integers(len(violations)))]
+        setattr(d, field, value)
+        assert L.smla_plan_launches(ctypes.byref(d), 152, ctypes.byref(p)) == status, (field, value)
