@@ -28,7 +28,8 @@ Every function here is a plain definition evaluated in float64: there is no
 online softmax, no tiling and no split-K. Each one is pinned by
 tests/test_oracle_pins.py against something other than itself (closed forms,
 torch's number formats, dense float64 attention, brute force), so none is
-parity unpinned.
+parity unpinned; tests/test_oracle_planted_mistakes.py plants plausible slips in
+a copy of this module and requires a pin to fail for each.
 """
 from __future__ import annotations
 
