@@ -28,7 +28,10 @@ tie rule. The readings taken here (each one listed in the design notes):
 
 Every function is a plain definition in float64: products of E4M3 values are exact
 in float64 and so is a sum of 128 of them, so the only rounding is in the final
-weighted sum over heads.
+weighted sum over heads. tests/test_indexer_oracle_pins.py pins every function
+(hand-built pages, closed forms, scalar loops, torch's float8 decode, argpartition),
+and tests/test_oracle_planted_mistakes.py requires those pins to catch plausible
+slips planted in a copy of this module.
 """
 from __future__ import annotations
 
