@@ -110,7 +110,7 @@ typedef struct smla_desc {
 /* Human-readable name of a status (static string). */
 const char* smla_status_string(int32_t status);
 
-/* ABI version of this header (increments on any incompatible change; 2 added kv_scale,
+/* ABI version of this header (increments whenever the interface changes; 2 added kv_scale,
  * 3 added SMLA_ERR_TIMEOUT, SMLA_ERR_OPERAND_RANGE, SMLA_DEVERR_RANGE,
  * smla_noalloc_read_error, the indexer calls and smla_store_kv_normed; 4 added q_format and
  * q_scale in place of two reserved words; 5 added smla_plan_launches). */
